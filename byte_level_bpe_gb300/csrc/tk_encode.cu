@@ -1,0 +1,1200 @@
+// tk_encode.cu -- the encode path of libtk: safe chunking, specials, split,
+// byte-pair merge and ordered assembly, all as CUDA kernels on one stream.
+//
+// Method (what is computed) follows "tiktoken Deep Dive" ("The split
+// pattern", "Inside encode: a parts vector and a linear scan", "Special
+// tokens ...") and "Making Kimi K3 Tokenization 18x Faster For Million Token
+// Agentic Workloads" ("One native call for the whole serving path": typed
+// segments, 400k / 25k safe chunking).  How it is computed is GPU-first:
+//
+//  * split: every byte decides on its own whether a pre-token starts there.
+//    Trying the eight clauses left to right is equivalent to a start test
+//    that looks at the classes of at most four preceding and one following
+//    code point, plus three run-level facts: the position inside a run of
+//    numbers (mod 3), whether a run of CR/LF that opens a white-space run was
+//    taken by a preceding "other" run (clause 4's [\r\n]*), and whether the
+//    rest of a white-space run holds a CR/LF or reaches the piece end
+//    (clauses 5-7).  The number-run carry crosses tiles through a decoupled
+//    look-back chain; the white-space facts are read by walking the run.
+//  * merge: pre-tokens up to 64 bytes run the parts loop in one thread over
+//    token ids (a pair of pieces merges to the token whose bytes are their
+//    concatenation, looked up in a pair table built at load).  Longer
+//    pre-tokens get one CTA each and merge in rounds: all leftmost-chained
+//    occurrences of the current minimum-rank pair merge at once, stopping
+//    the round at the first merge that creates a pair of lower rank, which is
+//    exactly the sequence the one-at-a-time loop would take.
+//  * assembly: ids are staged at their pre-token's byte offset, the per
+//    pre-token counts are scanned, and a scatter writes the ids in order.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "tk_internal.cuh"
+#include "tk_unicode_table.h"
+
+namespace tk {
+
+// Split classes of a code point (3 bits) and flags for clause 1.
+enum : uint8_t { K_L = 0, K_N = 1, K_O = 2, K_NL = 3, K_SP = 4, K_WSO = 5, K_CONT = 6, K_OUT = 7 };
+enum : uint8_t { F_APOS = 0x08, F_C1 = 0x10, F_LL = 0x20, F_VR = 0x40, F_E = 0x80 };
+
+__device__ __forceinline__ uint32_t uni_class(uint32_t cp) {
+  if (cp >= 0x110000) return 0;
+  const uint32_t blk = __ldg(&tk_uni_index[cp >> 8]);
+  const uint32_t b = __ldg(&tk_uni_blocks[blk * 64 + ((cp & 255) >> 2)]);
+  return (b >> (2 * (cp & 3))) & 3;
+}
+
+// Class and clause-1 flags of a code point.
+__device__ __forceinline__ uint8_t kclass(uint32_t cp) {
+  if (cp < 128) {
+    if (cp == 0x20) return K_SP;
+    if (cp == 0x0A || cp == 0x0D) return K_NL;
+    if (cp == 0x09 || cp == 0x0B || cp == 0x0C) return K_WSO;
+    const uint32_t lc = cp | 0x20;
+    if (lc >= 'a' && lc <= 'z') {
+      uint8_t f = 0;
+      if (lc == 's' || lc == 'd' || lc == 'm' || lc == 't') f = F_C1;
+      else if (lc == 'l') f = F_LL;
+      else if (lc == 'v' || lc == 'r') f = F_VR;
+      else if (lc == 'e') f = F_E;
+      return K_L | f;
+    }
+    if (cp >= '0' && cp <= '9') return K_N;
+    if (cp == 0x27) return K_O | F_APOS;
+    return K_O;
+  }
+  const uint32_t u = uni_class(cp);
+  if (u == 1) return cp == 0x17F ? (uint8_t)(K_L | F_C1) : (uint8_t)K_L;  // U+017F folds to s
+  if (u == 2) return K_N;
+  if (u == 3) return K_WSO;  // non-ASCII white space is never CR, LF or U+0020
+  return K_O;
+}
+
+// Decodes the UTF-8 sequence that starts with b0; returns its length (1 when
+// malformed, with ok = false).
+__device__ __forceinline__ int utf8_seq(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3,
+                                        uint32_t& cp, bool& ok) {
+  ok = true;
+  if (b0 < 0x80) { cp = b0; return 1; }
+  const bool c1 = (b1 & 0xC0) == 0x80, c2 = (b2 & 0xC0) == 0x80, c3 = (b3 & 0xC0) == 0x80;
+  if (b0 >= 0xC2 && b0 <= 0xDF && c1) { cp = ((b0 & 0x1F) << 6) | (b1 & 0x3F); return 2; }
+  if (b0 >= 0xE0 && b0 <= 0xEF && c1 && c2) {
+    cp = ((b0 & 0x0F) << 12) | ((b1 & 0x3F) << 6) | (b2 & 0x3F);
+    if (cp >= 0x800 && (cp < 0xD800 || cp > 0xDFFF)) return 3;
+  } else if (b0 >= 0xF0 && b0 <= 0xF4 && c1 && c2 && c3) {
+    cp = ((b0 & 0x07) << 18) | ((b1 & 0x3F) << 12) | ((b2 & 0x3F) << 6) | (b3 & 0x3F);
+    if (cp >= 0x10000 && cp <= 0x10FFFF) return 4;
+  }
+  ok = false;
+  cp = 0xFFFD;
+  return 1;
+}
+
+__device__ __forceinline__ bool is_ws(uint8_t k) { k &= 7; return k == K_NL || k == K_SP || k == K_WSO; }
+
+// Python str.isspace() on a code point: \s plus U+001C..U+001F (the legacy
+// chunking rule came from a Python implementation).
+__device__ __forceinline__ bool py_isspace(uint32_t cp) {
+  if (cp >= 0x1C && cp <= 0x1F) return true;
+  if (cp < 128) return cp == 0x20 || (cp >= 0x09 && cp <= 0x0D);
+  return uni_class(cp) == 3;
+}
+
+__device__ __forceinline__ bool bit_get(const uint32_t* b, int64_t i) { return (b[i >> 5] >> (i & 31)) & 1u; }
+
+// --------------------------------------------------------------------------
+// Device view of one encode call.
+
+struct Call {
+  const uint8_t* text;
+  int64_t n;
+  const int64_t* seg_off;
+  const uint8_t* allow;
+  int64_t S;
+  int safe;
+  Tables T;
+  Work W;
+};
+
+// Index of the segment holding byte pos (largest s with seg_off[s] <= pos,
+// skipping empty segments).
+__device__ int64_t seg_of(const Call& c, int64_t pos) {
+  int64_t lo = 0, hi = c.S - 1;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) >> 1;
+    if (c.seg_off[mid] <= pos) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// First s in [0, S] with seg_off[s] >= pos.
+__device__ int64_t seg_lower(const Call& c, int64_t pos) {
+  int64_t lo = 0, hi = c.S + 1;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (c.seg_off[mid] < pos) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint8_t gbyte(const Call& c, int64_t p) {
+  return (p >= 0 && p < c.n) ? __ldg(&c.text[p]) : 0;
+}
+
+__device__ bool g_chunk_cut(const Call& c, int64_t pos) {
+  if (!c.safe) return false;
+  return bit_get(c.W.win_cut, pos) || bit_get(c.W.run_cut, pos);
+}
+
+// Length of the longest special that starts at pos inside an allow_special
+// segment, fits in the segment and crosses no chunk cut; 0 if none.  Reads
+// global memory (slow path, used outside the shared-memory window).
+__device__ int g_special_at(const Call& c, int64_t pos, int32_t* id) {
+  if (c.T.n_spec == 0 || pos < 0 || pos >= c.n) return 0;
+  const uint32_t b = gbyte(c, pos);
+  if (!((c.T.spec_first[b >> 5] >> (b & 31)) & 1u)) return 0;
+  const int64_t s = seg_of(c, pos);
+  if (!c.allow[s]) return 0;
+  const int64_t send = c.seg_off[s + 1];
+  int best = 0;
+  for (int k = 0; k < c.T.n_spec; k++) {
+    const int L = c.T.spec_off[k + 1] - c.T.spec_off[k];
+    if (L <= best || pos + L > send) continue;
+    bool m = true;
+    for (int j = 0; j < L && m; j++) m = gbyte(c, pos + j) == c.T.spec_bytes[c.T.spec_off[k] + j];
+    for (int j = 1; j < L && m; j++) m = !g_chunk_cut(c, pos + j);
+    if (m) { best = L; if (id) *id = c.T.spec_ids[k]; }
+  }
+  return best;
+}
+
+// Piece start at byte pos (pos is a code-point start): text start or end, a
+// segment start, a chunk cut, or the start or end of a special span.
+__device__ bool g_piece_start(const Call& c, int64_t pos) {
+  if (pos <= 0 || pos >= c.n) return true;
+  const int64_t s = seg_lower(c, pos);
+  if (s <= c.S && c.seg_off[s] == pos) return true;
+  if (g_chunk_cut(c, pos)) return true;
+  if (c.T.n_spec == 0) return false;
+  if (g_special_at(c, pos, nullptr)) return true;
+  for (int k = 0; k < c.T.n_spec; k++) {
+    const int L = c.T.spec_off[k + 1] - c.T.spec_off[k];
+    if (pos - L >= 0 && g_special_at(c, pos - L, nullptr) == L) return true;
+  }
+  return false;
+}
+
+__device__ uint8_t g_kc(const Call& c, int64_t pos, int* len) {
+  uint32_t cp;
+  bool ok;
+  const int L = utf8_seq(gbyte(c, pos), gbyte(c, pos + 1), gbyte(c, pos + 2), gbyte(c, pos + 3), cp, ok);
+  if (len) *len = L;
+  return kclass(cp);
+}
+
+__device__ int64_t g_prev(const Call& c, int64_t pos) {
+  for (int k = 1; k <= 3; k++)
+    if ((gbyte(c, pos - k) & 0xC0) != 0x80) return pos - k;
+  return pos - 1;
+}
+
+// --------------------------------------------------------------------------
+// Look-back helpers (one thread).
+
+struct SumOp {
+  __device__ static uint64_t id() { return 0; }
+  __device__ static uint64_t comb(uint64_t l, uint64_t r) { return l + r; }
+};
+// Number-run carry: bit 2 = the tile is one unbroken run of numbers, bits 0-1
+// = count of numbers at its end, mod 3.
+struct NRunOp {
+  __device__ static uint64_t id() { return 4; }
+  __device__ static uint64_t comb(uint64_t l, uint64_t r) {
+    if (!(r & 4)) return r;
+    return (l & 4) | (((l & 3) + (r & 3)) % 3);
+  }
+};
+// Segmented count: bit 40 = a head was seen, bits 0-39 = count since it.
+struct SegCountOp {
+  __device__ static uint64_t id() { return 0; }
+  __device__ static uint64_t comb(uint64_t l, uint64_t r) {
+    if (r >> 40) return r;
+    return (l & (1ull << 40)) | ((l & ((1ull << 40) - 1)) + r);
+  }
+};
+
+// Publishes the tile's aggregate, waits for the predecessors and returns the
+// exclusive prefix; publishes the inclusive prefix.  Waits are bounded.
+template <class Op>
+__device__ uint64_t chain_exclusive(uint64_t* desc, int64_t tile, uint64_t agg, Status* st, int kind) {
+  if (tile == 0) {
+    st_release_u64(&desc[0], DESC_PREFIX | agg);
+    return Op::id();
+  }
+  st_release_u64(&desc[tile], DESC_AGG | agg);
+  uint64_t acc = Op::id();
+  int64_t j = tile - 1;
+  uint32_t spins = 0;
+  while (j >= 0) {
+    const uint64_t d = ld_acquire_u64(&desc[j]);
+    const uint64_t state = d & ~DESC_VAL;
+    if (state == 0) {
+      if (++spins > SPIN_LIMIT) {
+        set_error(st, TK_E_TIMEOUT, kind);
+        break;
+      }
+      __nanosleep(64);
+      continue;
+    }
+    acc = Op::comb(d & DESC_VAL, acc);
+    if (state == DESC_PREFIX) break;
+    j--;
+  }
+  st_release_u64(&desc[tile], DESC_PREFIX | Op::comb(acc, agg));
+  return acc;
+}
+
+// --------------------------------------------------------------------------
+// Kernel: zero the status block and the look-back descriptors of one call.
+
+__global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int safe,
+                        int64_t n_cut_words) {
+  const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if (tid == 0) {
+    Status s = {};
+    s.err_pos = INT64_MAX;
+    *W.status = s;
+  }
+  for (int64_t i = tid; i < n_desc_split; i += stride) {
+    W.desc_a[i] = 0;
+    W.desc_b[i] = 0;
+    if (safe) { W.desc_w[i] = 0; W.desc_r[i] = 0; }
+  }
+  for (int64_t i = tid; i < n_desc_scan; i += stride) W.desc_c[i] = 0;
+  if (safe)
+    for (int64_t i = tid; i < n_cut_words; i += stride) { W.win_cut[i] = 0; W.run_cut[i] = 0; }
+}
+
+// Segment table check: seg_off[0] = 0, non-decreasing, seg_off[S] = n.
+__global__ void k_check_segments(Call c) {
+  const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  for (int64_t s = tid; s <= c.S; s += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t v = c.seg_off[s];
+    bool bad = (s == 0 && v != 0) || (s == c.S && v != c.n) || v < 0 || v > c.n;
+    if (s > 0 && c.seg_off[s - 1] > v) bad = true;
+    if (bad) set_error(c.W.status, TK_E_ARG, 1);
+  }
+}
+
+// --------------------------------------------------------------------------
+// Safe chunking: a segmented count of code points over the text.
+//   mode 0 (windows): heads are segment starts; a cut goes before every code
+//     point whose index since the head is a positive multiple of 400,000.
+//   mode 1 (runs): heads are segment starts, window cuts and changes of
+//     isspace(); a cut goes before every code point whose index in its run is
+//     a positive multiple of 25,000.
+// Tiles of 4 KiB, 256 threads x 16 bytes, persistent with dynamic tiles.
+
+__global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) {
+  __shared__ uint8_t s_text[TILE + 8];
+  __shared__ uint64_t s_agg[SPLIT_THREADS];
+  __shared__ int64_t s_tile;
+  __shared__ uint64_t s_carry;
+  __shared__ int64_t s_seg[2];
+  const int tid = threadIdx.x;
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  uint64_t* desc = mode == 0 ? c.W.desc_w : c.W.desc_r;
+  uint32_t* out = mode == 0 ? c.W.win_cut : c.W.run_cut;
+  const int64_t M = mode == 0 ? CHUNK_CHARS : RUN_CHARS;
+  for (;;) {
+    if (tid == 0) s_tile = atomicAdd(&c.W.status->tile_ctr[1 + mode], 1u);
+    __syncthreads();
+    const int64_t tile = s_tile;
+    if (tile >= ntiles) break;
+    const int64_t t0 = tile * TILE;
+    // bytes [t0 - 4, t0 + TILE + 4)
+    for (int x = tid; x < TILE + 8; x += SPLIT_THREADS) s_text[x] = gbyte(c, t0 - 4 + x);
+    if (tid == 0) {
+      s_seg[0] = seg_lower(c, t0);
+      s_seg[1] = seg_lower(c, t0 + TILE);
+    }
+    __syncthreads();
+    const int64_t slo = s_seg[0], shi = s_seg[1];
+    // per-thread aggregate over its 16 bytes
+    const int xb = 4 + tid * 16;
+    uint64_t agg = 0;
+    uint64_t heads = 0, starts = 0;  // bit j: byte xb + j is a head / code-point start
+    for (int j = 0; j < 16; j++) {
+      const int x = xb + j;
+      const int64_t pos = t0 + tid * 16 + j;
+      if (pos >= c.n) break;
+      const uint32_t b = s_text[x];
+      if ((b & 0xC0) == 0x80) continue;
+      starts |= 1ull << j;
+      bool head = false;
+      // segment start?
+      for (int64_t s = slo; s < shi && !head; s++) head = c.seg_off[s] == pos;
+      if (!head && pos == 0) head = true;
+      if (mode == 1 && !head) {
+        if (bit_get(c.W.win_cut, pos)) head = true;
+        else {
+          uint32_t cp, pcp;
+          bool ok;
+          utf8_seq(b, s_text[x + 1], s_text[x + 2], s_text[x + 3], cp, ok);
+          int px = x - 1;
+          while (px > x - 4 && (s_text[px] & 0xC0) == 0x80) px--;
+          utf8_seq(s_text[px], s_text[px + 1], s_text[px + 2], s_text[px + 3], pcp, ok);
+          head = py_isspace(cp) != py_isspace(pcp);
+        }
+      }
+      if (head) { heads |= 1ull << j; agg = 1ull << 40; }
+      agg += 1;
+    }
+    s_agg[tid] = agg;
+    __syncthreads();
+    if (tid == 0) {
+      // serial exclusive combine over 256 thread aggregates (cheap)
+      uint64_t run = SegCountOp::id();
+      for (int t = 0; t < SPLIT_THREADS; t++) {
+        const uint64_t a = s_agg[t];
+        s_agg[t] = run;
+        run = SegCountOp::comb(run, a);
+      }
+      s_carry = chain_exclusive<SegCountOp>(desc, tile, run, c.W.status, 2 + mode);
+    }
+    __syncthreads();
+    uint64_t v = SegCountOp::comb(s_carry, s_agg[tid]);
+    int64_t idx = (int64_t)(v & ((1ull << 40) - 1));
+    for (int j = 0; j < 16; j++) {
+      if (!((starts >> j) & 1)) continue;
+      if ((heads >> j) & 1) idx = 0;
+      if (idx > 0 && idx % M == 0) {
+        const int64_t pos = t0 + tid * 16 + j;
+        atomicOr(&out[pos >> 5], 1u << (pos & 31));
+      }
+      idx++;
+    }
+    __syncthreads();
+  }
+}
+
+// --------------------------------------------------------------------------
+// Split kernel: per 4 KiB tile, pre-token starts -> ordered records.
+
+struct SplitSmem {
+  uint8_t text[WIN + 16];
+  uint8_t kc[WIN];
+  uint32_t pst[WIN / 32];   // piece starts
+  uint32_t insp[WIN / 32];  // bytes inside special spans
+  uint32_t sst[WIN / 32];   // special span starts
+  uint32_t outb[TILE / 32]; // pre-token starts of the tile
+  uint32_t scan[SPLIT_THREADS];
+  uint32_t nagg[SPLIT_THREADS];
+  int64_t tile;
+  int64_t seg[2];
+  uint64_t ncarry;
+  uint64_t base;
+};
+
+// Special match of the longest special at window position x (all bytes must be
+// in the window); returns its length or 0.
+__device__ int win_special(const Call& c, const SplitSmem& sm, int x, int64_t pos) {
+  const uint32_t b = sm.text[x];
+  if (!((c.T.spec_first[b >> 5] >> (b & 31)) & 1u)) return 0;
+  const int64_t s = seg_of(c, pos);
+  if (!c.allow[s]) return 0;
+  const int64_t send = c.seg_off[s + 1];
+  int best = 0;
+  for (int k = 0; k < c.T.n_spec; k++) {
+    const int L = c.T.spec_off[k + 1] - c.T.spec_off[k];
+    if (L <= best || pos + L > send || x + L > WIN) continue;
+    bool m = true;
+    for (int j = 0; j < L && m; j++) m = sm.text[x + j] == c.T.spec_bytes[c.T.spec_off[k] + j];
+    // chunk cuts strictly inside the span forbid the match (pst holds only
+    // segment starts and chunk cuts at this point)
+    for (int j = 1; j < L && m; j++) m = !bit_get(sm.pst, x + j);
+    if (m) best = L;
+  }
+  return best;
+}
+
+// Accessors that read the window when the position is trusted, else global.
+struct Win {
+  const Call& c;
+  const SplitSmem& sm;
+  int64_t wlo;
+  __device__ bool trusted(int64_t p) const {
+    return p >= wlo + TRUST && p < wlo + WIN - TRUST;
+  }
+  __device__ uint8_t kc(int64_t p) const {
+    if (trusted(p)) return sm.kc[p - wlo];
+    if (p < 0 || p >= c.n) return K_OUT;
+    return g_kc(c, p, nullptr);
+  }
+  __device__ bool pst(int64_t p) const {
+    if (trusted(p)) return bit_get(sm.pst, p - wlo);
+    return g_piece_start(c, p);
+  }
+  __device__ int64_t prev(int64_t p) const {
+    if (trusted(p) && trusted(p - 4)) {
+      for (int k = 1; k <= 3; k++)
+        if ((sm.kc[p - k - wlo] & 7) != K_CONT) return p - k;
+      return p - 1;
+    }
+    return g_prev(c, p);
+  }
+  __device__ int64_t next(int64_t p) const {
+    if (trusted(p) && trusted(p + 4)) {
+      for (int k = 1; k <= 4; k++)
+        if ((sm.kc[p + k - wlo] & 7) != K_CONT) return p + k;
+      return p + 1;
+    }
+    int L;
+    g_kc(c, p, &L);
+    return p + L;
+  }
+};
+
+// Clause 1 at an apostrophe at j: the apostrophe starts a pre-token unless it
+// continues an "other" run or follows a space that starts one.
+__device__ __forceinline__ bool apos_starts(const Win& w, int64_t j) {
+  if (w.pst(j)) return true;
+  const uint8_t p = w.kc(w.prev(j)) & 7;
+  return p != K_O && p != K_SP;
+}
+
+// The start test.  x is a code-point start of ordinary text that is not a
+// piece start; nidx is its index inside its run of numbers (mod 3).
+__device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) {
+  const int64_t p1 = w.prev(x);
+  const uint8_t kp = w.kc(p1);
+  const uint8_t P = kp & 7, C = kx & 7;
+  switch (C) {
+    case K_N:
+      return P != K_N || nidx == 0;
+    case K_L: {
+      if (P == K_N || P == K_NL) return true;
+      if (P == K_SP || P == K_WSO) return false;
+      if (P == K_O) {
+        if (w.pst(p1)) return false;
+        const uint8_t P2 = w.kc(w.prev(p1)) & 7;
+        return P2 == K_O || P2 == K_SP;
+      }
+      // P == K_L: a start only right after a clause-1 contraction
+      if (w.pst(p1)) return false;
+      const int64_t p2 = w.prev(p1);
+      const uint8_t k2 = w.kc(p2);
+      if ((k2 & F_APOS) && (kp & F_C1) && apos_starts(w, p2)) return true;
+      if (w.pst(p2)) return false;
+      const int64_t p3 = w.prev(p2);
+      const uint8_t k3 = w.kc(p3);
+      if ((k3 & F_APOS) && (((k2 & F_LL) && (kp & F_LL)) || ((k2 & F_VR) && (kp & F_E))) &&
+          (k2 & 7) == K_L && apos_starts(w, p3))
+        return true;
+      return false;
+    }
+    case K_O:
+      return P == K_L || P == K_N || P == K_NL || P == K_WSO;
+    case K_NL:
+      return P == K_L || P == K_N;
+    default: {  // K_SP, K_WSO
+      if (P == K_L || P == K_N || P == K_O) return true;
+      if (P == K_NL) {
+        // taken by a preceding other-run's [\r\n]*?  walk back over CR/LF
+        int64_t j = p1;
+        bool absorbed;
+        for (;;) {
+          if ((w.kc(j) & 7) != K_NL) { absorbed = (w.kc(j) & 7) == K_O; break; }
+          if (w.pst(j)) { absorbed = false; break; }
+          j = w.prev(j);
+        }
+        if (absorbed) return true;
+        // else a start iff the rest of the run has no CR/LF and does not reach the piece end
+        int64_t q = x;
+        for (;;) {
+          const uint8_t kq = w.kc(q) & 7;
+          if (kq == K_NL) return false;
+          if (kq != K_SP && kq != K_WSO) return true;
+          q = w.next(q);
+          if (q >= w.c.n || w.pst(q)) return false;
+        }
+      }
+      // P is white space but not CR/LF: a start iff the next code point is in
+      // the piece and is not white space
+      const int64_t n1 = w.next(x);
+      if (n1 >= w.c.n || w.pst(n1)) return false;
+      return !is_ws(w.kc(n1));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
+  __shared__ SplitSmem sm;
+  const int tid = threadIdx.x;
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  const bool aligned = ((uintptr_t)c.text & 15) == 0;
+  for (;;) {
+    if (tid == 0) sm.tile = atomicAdd(&c.W.status->tile_ctr[0], 1u);
+    __syncthreads();
+    const int64_t tile = sm.tile;
+    if (tile >= ntiles) break;
+    const int64_t t0 = tile * TILE;
+    const int64_t wlo = t0 - HALO;
+    // 1. window bytes
+    for (int v = tid; v < (WIN + 16) / 16; v += SPLIT_THREADS) {
+      const int64_t p = wlo + 16 * v;
+      if (aligned && p >= 0 && p + 16 <= c.n) {
+        *reinterpret_cast<uint4*>(&sm.text[16 * v]) = __ldg(reinterpret_cast<const uint4*>(c.text + p));
+      } else {
+        for (int j = 0; j < 16; j++) sm.text[16 * v + j] = gbyte(c, p + j);
+      }
+    }
+    for (int i = tid; i < WIN / 32; i += SPLIT_THREADS) {
+      sm.insp[i] = 0;
+      sm.sst[i] = 0;
+      uint32_t v = 0;
+      const int64_t word = (wlo >> 5) + i;
+      if (c.safe && word >= 0 && (word << 5) < c.n) v = c.W.win_cut[word] | c.W.run_cut[word];
+      sm.pst[i] = v;
+    }
+    for (int i = tid; i < TILE / 32; i += SPLIT_THREADS) sm.outb[i] = 0;
+    if (tid == 0) {
+      sm.seg[0] = seg_lower(c, wlo);
+      sm.seg[1] = seg_lower(c, wlo + WIN);
+    }
+    __syncthreads();
+    // 2. segment starts (and the text end) are piece starts
+    for (int64_t s = sm.seg[0] + tid; s < sm.seg[1]; s += SPLIT_THREADS) {
+      const int64_t x = c.seg_off[s] - wlo;
+      if (x >= 0 && x < WIN) atomicOr(&sm.pst[x >> 5], 1u << (x & 31));
+    }
+    __syncthreads();
+    // 3. specials in allow_special segments: find, then mark
+    if (c.T.n_spec > 0) {
+      for (int x = tid; x < WIN; x += SPLIT_THREADS) {
+        const int64_t pos = wlo + x;
+        if (pos < 0 || pos >= c.n) continue;
+        if (win_special(c, sm, x, pos)) atomicOr(&sm.sst[x >> 5], 1u << (x & 31));
+      }
+      __syncthreads();
+      for (int x = tid; x < WIN; x += SPLIT_THREADS) {
+        if (!bit_get(sm.sst, x)) continue;
+        const int L = win_special(c, sm, x, wlo + x);
+        atomicOr(&sm.pst[x >> 5], 1u << (x & 31));
+        if (x + L < WIN) atomicOr(&sm.pst[(x + L) >> 5], 1u << ((x + L) & 31));
+        for (int j = 0; j < L; j++) atomicOr(&sm.insp[(x + j) >> 5], 1u << ((x + j) & 31));
+      }
+    }
+    // 4. classes (and UTF-8 validation of the tile's own bytes)
+    for (int x = tid; x < WIN; x += SPLIT_THREADS) {
+      const int64_t pos = wlo + x;
+      const uint32_t b = sm.text[x];
+      uint8_t k;
+      if (pos < 0 || pos >= c.n) {
+        k = K_OUT;
+      } else if ((b & 0xC0) == 0x80) {
+        k = K_CONT;
+        if (x >= HALO && x < HALO + TILE) {
+          // a continuation byte must be covered by a valid sequence
+          int j = x - 1;
+          while (j > x - 4 && (sm.text[j] & 0xC0) == 0x80) j--;
+          uint32_t cp;
+          bool ok;
+          const int L = utf8_seq(sm.text[j], sm.text[j + 1], sm.text[j + 2], sm.text[j + 3], cp, ok);
+          if ((sm.text[j] & 0xC0) == 0x80 || !ok || j + L <= x || wlo + j < 0) {
+            set_error(c.W.status, TK_E_UTF8, 0);
+            atomicMin((long long*)&c.W.status->err_pos, (long long)pos);
+          }
+        }
+      } else {
+        uint32_t cp;
+        bool ok;
+        utf8_seq(b, sm.text[x + 1], sm.text[x + 2], sm.text[x + 3], cp, ok);
+        if (!ok || pos + 1 > c.n) {
+          if (x >= HALO && x < HALO + TILE) {
+            set_error(c.W.status, TK_E_UTF8, 0);
+            atomicMin((long long*)&c.W.status->err_pos, (long long)pos);
+          }
+        }
+        k = kclass(cp);
+      }
+      sm.kc[x] = k;
+    }
+    __syncthreads();
+    // a multi-byte sequence cut by the text end is invalid too
+    // 5. number-run aggregate of this thread's 16 bytes
+    const int xb = HALO + tid * 16;
+    uint32_t nreset = 0, ncount = 0;
+    for (int j = 0; j < 16; j++) {
+      const int x = xb + j;
+      const uint8_t k = sm.kc[x] & 7;
+      if (k == K_CONT) continue;
+      if (k == K_OUT) break;
+      if (k != K_N || bit_get(sm.insp, x)) { nreset = 1; ncount = 0; continue; }
+      if (bit_get(sm.pst, x)) { nreset = 1; ncount = 0; }
+      ncount = (ncount + 1) % 3;
+    }
+    sm.nagg[tid] = (nreset ? 0u : 4u) | ncount;
+    __syncthreads();
+    if (tid == 0) {
+      uint64_t run = NRunOp::id();
+      for (int t = 0; t < SPLIT_THREADS; t++) {
+        const uint64_t a = sm.nagg[t];
+        sm.nagg[t] = (uint32_t)run;
+        run = NRunOp::comb(run, a);
+      }
+      sm.ncarry = chain_exclusive<NRunOp>(c.W.desc_a, tile, run, c.W.status, 4);
+    }
+    __syncthreads();
+    // 6. the start test for each code point of this thread
+    {
+      const Win w{c, sm, wlo};
+      const uint64_t pre = NRunOp::comb(sm.ncarry, sm.nagg[tid]);
+      uint32_t r = (uint32_t)(pre & 3);
+      uint32_t bits = 0;
+      for (int j = 0; j < 16; j++) {
+        const int x = xb + j;
+        const uint8_t k = sm.kc[x];
+        const uint8_t k7 = k & 7;
+        if (k7 == K_CONT) continue;
+        if (k7 == K_OUT) break;
+        const int64_t pos = wlo + x;
+        uint32_t nidx = 0;
+        const bool in_sp = bit_get(sm.insp, x);
+        if (k7 == K_N && !in_sp) {
+          if (bit_get(sm.pst, x)) r = 0;
+          nidx = r;
+          r = (r + 1) % 3;
+        } else {
+          r = 0;
+        }
+        bool s;
+        if (in_sp) s = bit_get(sm.sst, x);
+        else if (bit_get(sm.pst, x)) s = true;
+        else s = starts_here(w, pos, k, nidx);
+        if (s) bits |= 1u << j;
+      }
+      // 16 bits per thread: two threads share one 32-bit word
+      atomicOr(&sm.outb[tid >> 1], bits << (16 * (tid & 1)));
+    }
+    __syncthreads();
+    // 7. ordered records
+    const uint32_t mine = (sm.outb[tid >> 1] >> (16 * (tid & 1))) & 0xFFFFu;
+    sm.scan[tid] = __popc(mine);
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t run = 0;
+      for (int t = 0; t < SPLIT_THREADS; t++) {
+        const uint32_t a = sm.scan[t];
+        sm.scan[t] = run;
+        run += a;
+      }
+      sm.base = chain_exclusive<SumOp>(c.W.desc_b, tile, run, c.W.status, 5);
+      if (tile == ntiles - 1) {
+        const uint64_t total = sm.base + run;
+        c.W.status->n_ptok = (int64_t)total;
+        c.W.ptok[total] = (uint32_t)c.n;
+      }
+    }
+    __syncthreads();
+    {
+      uint64_t o = sm.base + sm.scan[tid];
+      for (int j = 0; j < 16; j++) {
+        if (!((mine >> j) & 1)) continue;
+        const int x = xb + j;
+        const uint32_t pos = (uint32_t)(wlo + x);
+        c.W.ptok[o++] = pos | (bit_get(sm.insp, x) ? PTOK_SPECIAL : 0u);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// --------------------------------------------------------------------------
+// Merge of short pre-tokens: the parts loop in one thread.
+
+__device__ int special_id_at(const Call& c, int64_t pos, int len) {
+  for (int k = 0; k < c.T.n_spec; k++) {
+    const int L = c.T.spec_off[k + 1] - c.T.spec_off[k];
+    if (L != len) continue;
+    bool m = true;
+    for (int j = 0; j < L && m; j++) m = gbyte(c, pos + j) == c.T.spec_bytes[c.T.spec_off[k] + j];
+    if (m) return c.T.spec_ids[k];
+  }
+  return -1;
+}
+
+__global__ void __launch_bounds__(128) k_merge_short(Call c) {
+  const int64_t P = c.W.status->n_ptok;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < P; k += stride) {
+    const uint32_t r0 = c.W.ptok[k];
+    const int64_t s = r0 & PTOK_MASK;
+    const int64_t e = c.W.ptok[k + 1] & PTOK_MASK;
+    const int n = (int)(e - s);
+    if (r0 & PTOK_SPECIAL) {
+      c.W.arena[s] = special_id_at(c, s, n);
+      c.W.cnt[k] = 1;
+      continue;
+    }
+    if (n > SHORT_MAX) {
+      const uint32_t slot = atomicAdd(&c.W.status->n_long, 1u);
+      c.W.long_list[slot] = (uint32_t)k;
+      continue;
+    }
+    uint32_t ids[SHORT_MAX], rk[SHORT_MAX];
+    uint32_t prevb = gbyte(c, s);
+    ids[0] = __ldg(&c.T.byte_id[prevb]);
+    for (int i = 1; i < n; i++) {
+      const uint32_t b = gbyte(c, s + i);
+      ids[i] = __ldg(&c.T.byte_id[b]);
+      rk[i - 1] = __ldg(&c.T.dense[(prevb << 8) | b]);
+      prevb = b;
+    }
+    rk[n - 1] = RANK_MAX;
+    int m = n;
+    while (m > 1) {
+      uint32_t best = RANK_MAX;
+      int bi = -1;
+      for (int i = 0; i + 1 < m; i++)
+        if (rk[i] < best) { best = rk[i]; bi = i; }
+      if (best == RANK_MAX) break;
+      ids[bi] = best;  // the merged piece is the token of that rank
+      for (int i = bi + 1; i + 1 < m; i++) { ids[i] = ids[i + 1]; rk[i] = rk[i + 1]; }
+      m--;
+      rk[bi] = (bi + 1 < m) ? pair_rank(c.T, ids[bi], ids[bi + 1]) : RANK_MAX;
+      if (bi > 0) rk[bi - 1] = pair_rank(c.T, ids[bi - 1], ids[bi]);
+    }
+    for (int i = 0; i < m; i++) c.W.arena[s + i] = (int32_t)ids[i];
+    c.W.cnt[k] = (uint32_t)m;
+  }
+}
+
+// --------------------------------------------------------------------------
+// Merge of long pre-tokens: one CTA per piece, exact rounds (see the file
+// header).  Arrays live in the workspace at the piece's byte offset.
+
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, uint32_t* red) {
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    v = (l < (int)(blockDim.x >> 5)) ? red[l] : RANK_MAX;
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (l == 0) red[0] = v;
+  }
+  __syncthreads();
+  const uint32_t r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// exclusive scan of per-thread values (int64) across the block; returns the
+// exclusive prefix, total in *tot.  op: 0 = sum, 1 = max.
+__device__ __forceinline__ int64_t block_scan_i64(int64_t v, int op, int64_t* red, int64_t* tot) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  int64_t x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (l >= o) x = op ? max(x, y) : x + y;
+  }
+  __syncthreads();
+  if (l == 31) red[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    int64_t y = (l < nw) ? red[l] : (op ? INT64_MIN : 0);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t z = __shfl_up_sync(0xffffffffu, y, o);
+      if (l >= o) y = op ? max(y, z) : y + z;
+    }
+    red[l] = y;  // inclusive over warps
+  }
+  __syncthreads();
+  const int64_t warp_excl = (w == 0) ? (op ? INT64_MIN : 0) : red[w - 1];
+  const int64_t incl = op ? max(warp_excl, x) : warp_excl + x;
+  const int64_t excl_in_warp = __shfl_up_sync(0xffffffffu, x, 1);
+  int64_t excl = (l == 0) ? warp_excl : (op ? max(warp_excl, excl_in_warp) : warp_excl + excl_in_warp);
+  *tot = red[(blockDim.x >> 5) - 1];
+  (void)incl;
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(LONG_THREADS) k_merge_long(Call c) {
+  __shared__ int64_t red64[LONG_THREADS / 32];
+  __shared__ uint32_t red32[LONG_THREADS / 32];
+  __shared__ uint32_t s_idx;
+  const int tid = threadIdx.x, T = blockDim.x;
+  for (;;) {
+    if (tid == 0) s_idx = atomicAdd(&c.W.status->long_next, 1u);
+    __syncthreads();
+    const uint32_t li = s_idx;
+    __syncthreads();
+    if (li >= c.W.status->n_long) break;
+    const int64_t k = c.W.long_list[li];
+    const int64_t s = c.W.ptok[k] & PTOK_MASK;
+    const int64_t e = c.W.ptok[k + 1] & PTOK_MASK;
+    int64_t n = e - s;
+    uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + s);
+    uint32_t* A_rk = c.W.lrk + s;
+    uint32_t* B_ids = c.W.lids2 + s;
+    uint32_t* B_rk = c.W.lrk2 + s;
+    uint8_t* sel = c.W.lsel + s;
+    uint8_t* chg = c.W.lchg + s;
+    for (int64_t i = tid; i < n; i += T) {
+      const uint32_t b = gbyte(c, s + i);
+      A_ids[i] = __ldg(&c.T.byte_id[b]);
+      A_rk[i] = (i + 1 < n) ? __ldg(&c.T.dense[(b << 8) | gbyte(c, s + i + 1)]) : RANK_MAX;
+    }
+    __syncthreads();
+    bool in_b = false;
+    for (uint32_t round = 0;; round++) {
+      const int64_t C = (n + T - 1) / T;
+      const int64_t lo = min(n, tid * C), hi = min(n, lo + C);
+      // (1) minimum rank
+      uint32_t m = RANK_MAX;
+      for (int64_t i = lo; i < hi; i++) m = min(m, A_rk[i]);
+      const uint32_t rs = block_min_u32(m, red32);
+      if (rs == RANK_MAX) break;
+      // (2) chains of rs-pairs: select every other pair from each chain's start
+      int64_t last_non = -1;
+      for (int64_t i = lo; i < hi; i++)
+        if (A_rk[i] != rs) last_non = i;
+      int64_t tot;
+      int64_t before = block_scan_i64(last_non, 1, red64, &tot);
+      int64_t ln = before;  // last non-candidate before this chunk
+      for (int64_t i = lo; i < hi; i++) {
+        if (A_rk[i] != rs) { ln = i; sel[i] = 0; }
+        else sel[i] = ((i - ln - 1) & 1) == 0;
+      }
+      __syncthreads();
+      // (3) first selected merge that creates a lower-ranked neighbour pair
+      uint32_t first_bad = 0xFFFFFFFFu;
+      for (int64_t i = lo; i < hi && first_bad == 0xFFFFFFFFu; i++) {
+        if (!sel[i]) continue;
+        bool bad = false;
+        if (i >= 1) {
+          const uint32_t left = (i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1];
+          bad = pair_rank(c.T, left, rs) < rs;
+        }
+        if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, A_ids[i + 2]) < rs;
+        if (bad) first_bad = (uint32_t)i;
+      }
+      const uint32_t limit = block_min_u32(first_bad, red32);
+      // (4) apply the merges at or before limit, compact into B
+      int64_t keep = 0;
+      for (int64_t i = lo; i < hi; i++) {
+        const bool removed = i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit;
+        keep += !removed;
+      }
+      int64_t dst = block_scan_i64(keep, 0, red64, &tot);
+      const int64_t n2 = tot;
+      for (int64_t i = lo; i < hi; i++) {
+        const bool removed = i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit;
+        if (removed) continue;
+        const bool merged = sel[i] && (uint64_t)i <= (uint64_t)limit;
+        B_ids[dst] = merged ? rs : A_ids[i];
+        B_rk[dst] = A_rk[i];
+        chg[dst] = merged;
+        dst++;
+      }
+      __syncthreads();
+      // (5) pair ranks next to merged pieces
+      const int64_t C2 = (n2 + T - 1) / T;
+      const int64_t lo2 = min(n2, tid * C2), hi2 = min(n2, lo2 + C2);
+      for (int64_t q = lo2; q < hi2; q++) {
+        if (q + 1 >= n2) B_rk[q] = RANK_MAX;
+        else if (chg[q] || chg[q + 1]) B_rk[q] = pair_rank(c.T, B_ids[q], B_ids[q + 1]);
+      }
+      __syncthreads();
+      uint32_t* t1 = A_ids; A_ids = B_ids; B_ids = t1;
+      uint32_t* t2 = A_rk; A_rk = B_rk; B_rk = t2;
+      in_b = !in_b;
+      n = n2;
+      if (round > (1u << 26)) { if (tid == 0) set_error(c.W.status, TK_E_LIMIT, 6); break; }
+    }
+    if (in_b) {
+      uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + s);
+      for (int64_t i = tid; i < n; i += T) dst[i] = A_ids[i];
+    }
+    if (tid == 0) c.W.cnt[k] = (uint32_t)n;
+    __syncthreads();
+  }
+}
+
+// --------------------------------------------------------------------------
+// Scatter: ids of pre-token k go to out[offs[k] .. offs[k] + cnt[k]).
+
+__global__ void k_scatter(Call c, int32_t* out, int64_t cap) {
+  const int64_t P = c.W.status->n_ptok;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < P; k += stride) {
+    const int64_t s = c.W.ptok[k] & PTOK_MASK;
+    const int64_t o = c.W.offs[k];
+    const uint32_t m = c.W.cnt[k];
+    for (uint32_t j = 0; j < m; j++)
+      if (o + j < cap) out[o + j] = c.W.arena[s + j];
+  }
+}
+
+// out_offsets[s] = index of segment s's first id; out_offsets[S] = total.
+__global__ void k_seg_offsets(Call c, int64_t* out_offsets) {
+  const int64_t P = c.W.status->n_ptok;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s <= c.S; s += stride) {
+    const int64_t pos = c.seg_off[s];
+    int64_t lo = 0, hi = P;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if ((int64_t)(c.W.ptok[mid] & PTOK_MASK) < pos) lo = mid + 1;
+      else hi = mid;
+    }
+    out_offsets[s] = c.W.offs[lo];
+    if (s == c.S) c.W.status->n_ids = c.W.offs[P];
+  }
+}
+
+}  // namespace tk
+
+// ============================================================================
+// Host side.
+
+using namespace tk;
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  tk_set_error("%s: %s", what, cudaGetErrorString(e));
+  return TK_E_CUDA;
+}
+
+#define TK_CUDA(call, what)                          \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, int64_t max_segments,
+                                   tk_workspace** out) {
+  if (!tok || !out || max_bytes < 0 || max_segments < 0) {
+    tk_set_error("tk_workspace_create: bad argument");
+    return TK_E_ARG;
+  }
+  *out = nullptr;
+  if (max_bytes > (int64_t)PTOK_MASK - 16) {
+    tk_set_error("tk_workspace_create: max_bytes %lld above 2^31 - 17", (long long)max_bytes);
+    return TK_E_LIMIT;
+  }
+  tk_workspace* ws = new (std::nothrow) tk_workspace();
+  if (!ws) return TK_E_NOMEM;
+  ws->tok = tok;
+  ws->device = tok->device;
+  ws->num_sms = tok->num_sms;
+  cudaSetDevice(tok->device);
+  const int64_t nb = std::max<int64_t>(max_bytes, 1);
+  const int64_t n_split_tiles = (nb + TILE - 1) / TILE + 1;
+  const int64_t n_scan_tiles = (nb + 1 + SCAN_TILE - 1) / SCAN_TILE + 1;
+  const int64_t cut_words = (nb + 64) / 32 + 1;
+  Work& w = ws->w;
+  w.max_bytes = max_bytes;
+  w.max_segments = max_segments;
+  struct Req { void** p; size_t bytes; };
+  Req reqs[] = {
+      {(void**)&w.status, sizeof(Status)},
+      {(void**)&w.desc_a, sizeof(uint64_t) * n_split_tiles},
+      {(void**)&w.desc_b, sizeof(uint64_t) * n_split_tiles},
+      {(void**)&w.desc_w, sizeof(uint64_t) * n_split_tiles},
+      {(void**)&w.desc_r, sizeof(uint64_t) * n_split_tiles},
+      {(void**)&w.desc_c, sizeof(uint64_t) * n_scan_tiles},
+      {(void**)&w.win_cut, sizeof(uint32_t) * cut_words},
+      {(void**)&w.run_cut, sizeof(uint32_t) * cut_words},
+      {(void**)&w.ptok, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.cnt, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.offs, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.arena, sizeof(int32_t) * (nb + 2)},
+      {(void**)&w.long_list, sizeof(uint32_t) * (nb / (SHORT_MAX + 1) + 2)},
+      {(void**)&w.lrk, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.lids2, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.lrk2, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.lsel, (size_t)nb + 2},
+      {(void**)&w.lchg, (size_t)nb + 2},
+      {(void**)&ws->d_stage_text, (size_t)nb + 16},
+      {(void**)&ws->d_stage_off, sizeof(int64_t) * (max_segments + 1)},
+      {(void**)&ws->d_stage_allow, (size_t)max_segments + 1},
+      {(void**)&ws->d_stage_ids, sizeof(int32_t) * nb},
+      {(void**)&ws->d_stage_offsets, sizeof(int64_t) * (max_segments + 1)},
+  };
+  for (auto& r : reqs) {
+    cudaError_t e = cudaMalloc(r.p, r.bytes);
+    if (e != cudaSuccess) {
+      tk_set_error("tk_workspace_create: cudaMalloc(%zu): %s", r.bytes, cudaGetErrorString(e));
+      tk_workspace_free(ws);
+      return TK_E_NOMEM;
+    }
+    ws->dev_mem[ws->n_dev++] = *r.p;
+  }
+  if (cudaMallocHost((void**)&ws->h_status, sizeof(Status)) != cudaSuccess) {
+    tk_workspace_free(ws);
+    tk_set_error("tk_workspace_create: cudaMallocHost failed");
+    return TK_E_NOMEM;
+  }
+  *out = ws;
+  return TK_OK;
+}
+
+extern "C" void tk_workspace_free(tk_workspace* ws) {
+  if (!ws) return;
+  for (int i = 0; i < ws->n_dev; i++) cudaFree(ws->dev_mem[i]);
+  if (ws->h_status) cudaFreeHost(ws->h_status);
+  delete ws;
+}
+
+// Launches the whole encode on `st` and reads back the status (one sync).
+static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_t* d_text, int64_t n,
+                         const int64_t* d_seg_off, const uint8_t* d_allow, int64_t S, int safe,
+                         int32_t* d_out, int64_t cap, int64_t* d_out_offsets, int64_t* h_n_ids,
+                         cudaStream_t st) {
+  Call c;
+  c.text = d_text;
+  c.n = n;
+  c.seg_off = d_seg_off;
+  c.allow = d_allow;
+  c.S = S;
+  c.safe = safe ? 1 : 0;
+  c.T = tok->t;
+  c.W = ws->w;
+  const int64_t n_split_tiles = (n + TILE - 1) / TILE;
+  const int64_t n_scan_tiles = (n + 1 + SCAN_TILE - 1) / SCAN_TILE + 1;
+  const int64_t cut_words = (n + 64) / 32 + 1;
+  const int sms = ws->num_sms;
+  const int seg_grid = (int)std::max<int64_t>(1, std::min<int64_t>((S + 256) / 256, (int64_t)sms * 4));
+  tk_prof_mark(ws, "k_reset", st);
+  k_reset<<<sms * 2, 256, 0, st>>>(ws->w, n_split_tiles + 1, n_scan_tiles, c.safe, cut_words);
+  tk_prof_mark(ws, "k_check_segments", st);
+  k_check_segments<<<seg_grid, 256, 0, st>>>(c);
+  if (n > 0) {
+    const int split_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * 6);
+    if (c.safe) {
+      tk_prof_mark(ws, "k_chunk_scan_windows", st);
+      k_chunk_scan<<<split_grid, SPLIT_THREADS, 0, st>>>(c, 0);
+      tk_prof_mark(ws, "k_chunk_scan_runs", st);
+      k_chunk_scan<<<split_grid, SPLIT_THREADS, 0, st>>>(c, 1);
+    }
+    tk_prof_mark(ws, "k_split", st);
+    k_split<<<split_grid, SPLIT_THREADS, 0, st>>>(c);
+    const int merge_grid = (int)std::min<int64_t>((n + 127) / 128, (int64_t)sms * 16);
+    tk_prof_mark(ws, "k_merge_short", st);
+    k_merge_short<<<merge_grid, 128, 0, st>>>(c);
+    tk_prof_mark(ws, "k_merge_long", st);
+    k_merge_long<<<sms * 2, LONG_THREADS, 0, st>>>(c);
+    tk_prof_mark(ws, "k_scan_u32", st);
+    int rc = tk_scan_u32(ws, ws->w.cnt, ws->w.offs, &ws->w.status->n_ptok, n, 3, st);
+    if (rc) return rc;
+    tk_prof_mark(ws, "k_scatter", st);
+    k_scatter<<<merge_grid, 256, 0, st>>>(c, d_out, cap);
+  } else {
+    // no text: one empty pre-token list
+    tk_prof_mark(ws, "k_scan_u32", st);
+    int rc = tk_scan_u32(ws, ws->w.cnt, ws->w.offs, &ws->w.status->n_ptok, 0, 3, st);
+    if (rc) return rc;
+  }
+  tk_prof_mark(ws, "k_seg_offsets", st);
+  k_seg_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets);
+  TK_CUDA(cudaGetLastError(), "encode launch");
+  TK_CUDA(cudaMemcpyAsync(ws->h_status, ws->w.status, sizeof(Status), cudaMemcpyDeviceToHost, st),
+          "status copy");
+  TK_CUDA(cudaStreamSynchronize(st), "encode");
+  tk_prof_finish(ws, st);
+  const Status& hs = *ws->h_status;
+  if (h_n_ids) *h_n_ids = hs.n_ids;
+  if (hs.code == TK_E_UTF8) {
+    tk_set_error("invalid UTF-8 at byte %lld", (long long)hs.err_pos);
+    return TK_E_UTF8;
+  }
+  if (hs.code) {
+    tk_set_error("encode failed on the device (code %d, site %d)", hs.code, hs.err_kind);
+    return hs.code;
+  }
+  if (hs.n_ids > cap) {
+    tk_set_error("output capacity %lld < %lld ids", (long long)cap, (long long)hs.n_ids);
+    return TK_E_CAPACITY;
+  }
+  return TK_OK;
+}
+
+extern "C" int tk_last_stats(const tk_workspace* ws, int64_t* n_pretokens, int64_t* n_ids,
+                             int64_t* n_long) {
+  if (!ws) return TK_E_ARG;
+  if (n_pretokens) *n_pretokens = ws->h_status->n_ptok;
+  if (n_ids) *n_ids = ws->h_status->n_ids;
+  if (n_long) *n_long = ws->h_status->n_long;
+  return TK_OK;
+}
+
+static int check_encode_args(const tk_tokenizer* tok, tk_workspace* ws, const void* text, int64_t n,
+                             const void* seg_off, const void* allow, int64_t S, const void* out,
+                             int64_t cap, const void* out_off) {
+  if (!tok || !ws || ws->tok != tok || n < 0 || S < 0 || cap < 0 || !seg_off || !out_off ||
+      (n > 0 && !text) || (S > 0 && !allow) || (cap > 0 && !out)) {
+    tk_set_error("tk_encode_segments: bad argument");
+    return TK_E_ARG;
+  }
+  if (n > ws->w.max_bytes || S > ws->w.max_segments) {
+    tk_set_error("tk_encode_segments: %lld bytes / %lld segments above the workspace limits %lld / %lld",
+                 (long long)n, (long long)S, (long long)ws->w.max_bytes, (long long)ws->w.max_segments);
+    return TK_E_LIMIT;
+  }
+  if (S == 0 && n != 0) {
+    tk_set_error("tk_encode_segments: text without segments");
+    return TK_E_ARG;
+  }
+  return TK_OK;
+}
+
+extern "C" int tk_encode_segments(const tk_tokenizer* tok, tk_workspace* ws, const uint8_t* d_text,
+                                  int64_t n_bytes, const int64_t* d_seg_off,
+                                  const uint8_t* d_allow_special, int64_t S, int tiktoken_safe,
+                                  int32_t* d_out_ids, int64_t out_capacity, int64_t* d_out_offsets,
+                                  int64_t* h_n_ids, void* cuda_stream) {
+  int rc = check_encode_args(tok, ws, d_text, n_bytes, d_seg_off, d_allow_special, S, d_out_ids,
+                             out_capacity, d_out_offsets);
+  if (rc) return rc;
+  cudaSetDevice(ws->device);
+  return encode_device(tok, ws, d_text, n_bytes, d_seg_off, d_allow_special, S, tiktoken_safe,
+                       d_out_ids, out_capacity, d_out_offsets, h_n_ids, (cudaStream_t)cuda_stream);
+}
+
+extern "C" int tk_encode_segments_host(const tk_tokenizer* tok, tk_workspace* ws, const uint8_t* h_text,
+                                       int64_t n_bytes, const int64_t* h_seg_off,
+                                       const uint8_t* h_allow_special, int64_t S, int tiktoken_safe,
+                                       int32_t* h_out_ids, int64_t out_capacity, int64_t* h_out_offsets,
+                                       int64_t* h_n_ids, void* cuda_stream) {
+  int rc = check_encode_args(tok, ws, h_text, n_bytes, h_seg_off, h_allow_special, S, h_out_ids,
+                             out_capacity, h_out_offsets);
+  if (rc) return rc;
+  cudaSetDevice(ws->device);
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  if (n_bytes) TK_CUDA(cudaMemcpyAsync(ws->d_stage_text, h_text, n_bytes, cudaMemcpyHostToDevice, st), "h2d text");
+  TK_CUDA(cudaMemcpyAsync(ws->d_stage_off, h_seg_off, sizeof(int64_t) * (S + 1), cudaMemcpyHostToDevice, st),
+          "h2d offsets");
+  if (S) TK_CUDA(cudaMemcpyAsync(ws->d_stage_allow, h_allow_special, S, cudaMemcpyHostToDevice, st), "h2d allow");
+  const int64_t dcap = std::min<int64_t>(out_capacity, std::max<int64_t>(ws->w.max_bytes, 1));
+  int64_t n_ids = 0;
+  rc = encode_device(tok, ws, ws->d_stage_text, n_bytes, ws->d_stage_off, ws->d_stage_allow, S,
+                     tiktoken_safe, ws->d_stage_ids, dcap, ws->d_stage_offsets, &n_ids, st);
+  if (h_n_ids) *h_n_ids = n_ids;
+  if (rc) return rc;
+  if (n_ids) TK_CUDA(cudaMemcpyAsync(h_out_ids, ws->d_stage_ids, sizeof(int32_t) * n_ids, cudaMemcpyDeviceToHost, st),
+                     "d2h ids");
+  TK_CUDA(cudaMemcpyAsync(h_out_offsets, ws->d_stage_offsets, sizeof(int64_t) * (S + 1), cudaMemcpyDeviceToHost, st),
+          "d2h offsets");
+  TK_CUDA(cudaStreamSynchronize(st), "encode (host buffers)");
+  return TK_OK;
+}

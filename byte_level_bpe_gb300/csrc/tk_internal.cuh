@@ -1,0 +1,173 @@
+// tk_internal.cuh -- definitions shared by the libtk translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tk.h"
+
+namespace tk {
+
+constexpr uint32_t RANK_MAX = 0xFFFFFFFFu;
+constexpr uint32_t MAX_ID = (1u << 20) - 2;  // ids and ranks fit the packed pair slots
+constexpr int MAX_SPECIAL = 64;               // longest special string, bytes
+constexpr int MAX_SPECIALS = 256;
+
+// Split tiles: 4 KiB of text per tile, 256 threads, 16 bytes per thread.  The
+// tile is loaded with HALO bytes on each side; piece starts (segment starts,
+// safe-chunking cuts, special spans) are exact for positions at least TRUST
+// bytes inside the loaded window (a special of up to 64 bytes must fit).
+constexpr int TILE = 4096;
+constexpr int SPLIT_THREADS = 256;
+constexpr int HALO = 128;
+constexpr int TRUST = 64;
+constexpr int WIN = TILE + 2 * HALO;
+
+constexpr int SHORT_MAX = 64;   // pre-tokens up to this length merge in one thread
+constexpr int LONG_THREADS = 512;
+constexpr int SCAN_THREADS = 256;
+constexpr int SCAN_ITEMS = 8;    // u32 counts per scan thread
+constexpr int SCAN_TILE = SCAN_THREADS * SCAN_ITEMS;
+
+constexpr int64_t CHUNK_CHARS = 400000;  // safe chunking: window length, characters
+constexpr int64_t RUN_CHARS = 25000;     // safe chunking: longest run, characters
+
+constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (x ~100 ns each)
+
+constexpr uint32_t PTOK_SPECIAL = 0x80000000u;
+constexpr uint32_t PTOK_MASK = 0x7FFFFFFFu;
+
+// Decoupled look-back descriptors: state in bits 63..62, value in 61..0.
+constexpr uint64_t DESC_AGG = 1ull << 62;
+constexpr uint64_t DESC_PREFIX = 2ull << 62;
+constexpr uint64_t DESC_VAL = (1ull << 62) - 1;
+
+// Device status block of one encode/decode (zeroed at the start of each call).
+struct Status {
+  int32_t code;      // first error (TK_E_*), 0 = none
+  int32_t err_kind;  // which wait timed out, for diagnostics
+  int64_t err_pos;   // smallest invalid UTF-8 byte offset (INT64_MAX if none)
+  int64_t n_ptok;    // pre-tokens found by the split
+  int64_t n_ids;     // ids produced (may exceed the output capacity)
+  uint32_t n_long;   // pre-tokens queued for the long-piece merge
+  uint32_t long_next;
+  uint32_t tile_ctr[8];  // dynamic tile counters of the persistent kernels
+};
+
+// Lookup tables of a tokenizer, in device memory (passed by value).
+struct Tables {
+  const uint32_t* byte_id;     // [256] id of each single byte
+  const uint32_t* dense;       // [65536] rank of the two-byte token (a<<8|b), or RANK_MAX
+  const uint64_t* pair_slots;  // open addressing: (a << 40) | (b << 20) | rank; empty = ~0
+  uint32_t pair_log2;          // log2(number of slots)
+  uint32_t pair_max_probe;     // longest probe sequence present in the table
+  const uint8_t* spec_bytes;   // specials, concatenated
+  const int32_t* spec_off;     // [n_spec + 1]
+  const int32_t* spec_ids;     // [n_spec]
+  int32_t n_spec;
+  uint32_t spec_first[8];      // 256-bit mask of the specials' first bytes
+  const uint32_t* tok_start;   // [max_id + 1] decode: byte offset in tok_bytes
+  const int32_t* tok_len;      // [max_id + 1] decode: length, -1 if the id is unused
+  const uint8_t* tok_bytes;
+  int64_t max_id;
+};
+
+// Device scratch of one encode (all sized from max_bytes / max_segments).
+struct Work {
+  Status* status;
+  uint64_t* desc_a;     // split: N-run carry chain, one per split tile
+  uint64_t* desc_b;     // split: pre-token count chain
+  uint64_t* desc_c;     // count scan chain
+  uint64_t* desc_w;     // safe chunking: window scan chain
+  uint64_t* desc_r;     // safe chunking: run scan chain
+  uint32_t* win_cut;    // bitmap: 400k-character window cuts
+  uint32_t* run_cut;    // bitmap: 25k-character run cuts
+  uint32_t* ptok;       // [max_bytes + 1] pre-token starts (bit 31: special)
+  uint32_t* cnt;        // [max_bytes + 1] ids per pre-token
+  uint32_t* offs;       // [max_bytes + 1] exclusive scan of cnt
+  int32_t* arena;       // [max_bytes] ids, staged at their pre-token's byte offset
+  uint32_t* long_list;  // pre-tokens for the long-piece merge
+  uint32_t* lrk;        // [max_bytes] long merge: pair ranks
+  uint32_t* lids2;      // [max_bytes] long merge: second id buffer
+  uint32_t* lrk2;       // [max_bytes] long merge: second rank buffer
+  uint8_t* lsel;        // [max_bytes] long merge: selection flags
+  uint8_t* lchg;        // [max_bytes] long merge: changed flags
+  int64_t max_bytes;
+  int64_t max_segments;
+};
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void set_error(Status* st, int code, int kind) {
+  if (atomicCAS(&st->code, 0, code) == 0) st->err_kind = kind;
+}
+
+// Open-addressing lookup of the rank of the token whose bytes are
+// bytes(a) || bytes(b), or RANK_MAX.
+__device__ __forceinline__ uint32_t pair_rank(const Tables& T, uint32_t a, uint32_t b) {
+  const uint64_t key = ((uint64_t)a << 20) | b;
+  uint64_t h = (key * 0x9E3779B97F4A7C15ull) >> (64 - T.pair_log2);
+  const uint64_t mask = (1ull << T.pair_log2) - 1;
+  for (uint32_t probe = 0; probe <= T.pair_max_probe; probe++) {
+    const uint64_t s = __ldg(&T.pair_slots[h]);
+    if (s == ~0ull) return RANK_MAX;
+    if ((s >> 20) == key) return (uint32_t)(s & 0xFFFFF);
+    h = (h + 1) & mask;
+  }
+  return RANK_MAX;
+}
+
+}  // namespace tk
+
+struct tk_tokenizer {
+  tk::Tables t;
+  void* dev_mem[16];
+  int n_dev;
+  int64_t n_ranks;
+  int device;
+  int num_sms;
+};
+
+struct tk_profile {
+  static constexpr int MAXK = 24;
+  int on;
+  int n;                      // kernels with totals
+  const char* names[MAXK];
+  double total_ms[MAXK];
+  int64_t launches[MAXK];
+  cudaEvent_t ev[MAXK + 1];   // events of the call in flight
+  const char* pending[MAXK];  // kernel names of the call in flight
+  int n_pending;
+};
+
+struct tk_workspace {
+  tk::Work w;
+  tk_profile prof;
+  const tk_tokenizer* tok;
+  void* dev_mem[32];
+  int n_dev;
+  tk::Status* h_status;     // pinned host copy of the status block
+  uint8_t* d_stage_text;    // staging for tk_encode_segments_host
+  int64_t* d_stage_off;
+  uint8_t* d_stage_allow;
+  int32_t* d_stage_ids;
+  int64_t* d_stage_offsets;
+  int device;
+  int num_sms;
+};
+
+// Internal C++ entry points shared between translation units.
+void tk_set_error(const char* fmt, ...);
+// Profiling helpers: mark() before a launch (records an event when profiling
+// is on); finish() after the call's synchronisation adds up the durations.
+void tk_prof_mark(tk_workspace* ws, const char* kernel, cudaStream_t st);
+void tk_prof_finish(tk_workspace* ws, cudaStream_t st);
+int tk_scan_u32(tk_workspace* ws, const uint32_t* d_in, uint32_t* d_out, const int64_t* d_n,
+                int64_t n_max, int chain_ctr, cudaStream_t st);

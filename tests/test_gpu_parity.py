@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path's ids equal the CPU oracle's, element by element.
+
+Every test calls the C ABI through the thin binding (byte_level_bpe_gb300)
+and compares with the oracle on the same seeded inputs. Integer work:
+bit-exact equality, no tolerance.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _gpu_ids(tk, segments, safe):
+    ids, off = tk.encode_segments(segments, tiktoken_safe=safe)
+    return ids.cpu().numpy(), off.cpu().numpy()
+
+
+def _compare(tk, enc, segments, safe):
+    g_ids, g_off = _gpu_ids(tk, segments, safe)
+    o_ids, o_off = enc.encode_segments(segments, tiktoken_safe=safe)
+    assert len(g_ids) == len(o_ids), (len(g_ids), len(o_ids))
+    if not np.array_equal(g_ids, o_ids):
+        k = int(np.argmax(g_ids != o_ids))
+        raise AssertionError(f"first mismatch at id {k}: gpu {g_ids[k-3:k+4]} oracle {o_ids[k-3:k+4]}")
+    assert np.array_equal(g_off, o_off)
+    return g_ids
+
+
+@pytest.fixture(scope="module")
+def full_gpu(full_table):
+    import byte_level_bpe_gb300 as tk
+    return tk.Tokenizer(full_table, workloads.SPECIALS, max_bytes=1 << 24, max_segments=8192)
+
+
+@pytest.fixture(scope="module")
+def tiny_gpu(tiny_table):
+    import byte_level_bpe_gb300 as tk
+    return tk.Tokenizer(tiny_table, max_bytes=1 << 20)
+
+
+def test_tiny_workload(tiny_gpu, tiny_enc):
+    _compare(tiny_gpu, tiny_enc, [(workloads.tiny_input(), False)], False)
+
+
+def test_full_table_workload(full_gpu, full_enc, full_table):
+    text = workloads.prose_text(full_table, 1 << 20, seed=2)
+    _compare(full_gpu, full_enc, [(text, False)], False)
+
+
+def test_agentic_small(full_gpu, full_enc, full_table):
+    segs = workloads.agentic_segments(full_table, seed=3, scale=0.05)
+    _compare(full_gpu, full_enc, segs, True)
+
+
+def test_agentic_full(full_gpu, full_enc, full_table):
+    segs = workloads.agentic_segments(full_table, seed=3)
+    assert max(len(s) for s, _ in segs) > 1_000_000
+    _compare(full_gpu, full_enc, segs, True)
+
+
+def test_multilingual(full_table):
+    import byte_level_bpe_gb300 as tk
+    ext = workloads.multilingual_table(full_table)
+    ranks = [(t, i) for i, t in enumerate(full_table)] + ext
+    enc = oracle.Encoding(ranks, workloads.SPECIALS)
+    gpu = tk.Tokenizer(ranks, workloads.SPECIALS, max_bytes=1 << 24)
+    text = workloads.multilingual_text(full_table)
+    _compare(gpu, enc, [(text, False)], False)
+
+
+def test_serving_scaled(full_gpu, full_enc, full_table):
+    text, off = workloads.serving_batch(full_table, seed=5, total=8 << 20, n_req=128)
+    segs = [(text[off[i]:off[i + 1]].tobytes(), False) for i in range(len(off) - 1)]
+    _compare(full_gpu, full_enc, segs, False)
+
+
+def test_serving_full_size_sampled(full_table, full_enc):
+    """The 256 MiB batch in the bench's launch configuration; sampled requests
+    are encoded one by one by the oracle (segments are independent)."""
+    import byte_level_bpe_gb300 as tk
+    text, off = workloads.serving_batch(full_table, seed=5)
+    gpu = tk.Tokenizer(full_table, workloads.SPECIALS, max_bytes=len(text), max_segments=len(off))
+    d_text = torch.from_numpy(text).cuda()
+    d_off = torch.from_numpy(off).cuda()
+    d_allow = torch.zeros(len(off) - 1, dtype=torch.uint8, device="cuda")
+    ids, g_off = gpu.encode_device(d_text, d_off, d_allow, tiktoken_safe=False)
+    ids = ids.cpu().numpy()
+    g_off = g_off.cpu().numpy()
+    rng = np.random.default_rng(0)
+    for r in rng.choice(len(off) - 1, size=24, replace=False):
+        seg = text[off[r]:off[r + 1]].tobytes()
+        exp = full_enc.encode(seg)
+        assert np.array_equal(ids[g_off[r]:g_off[r + 1]], exp), r
+    # properties at full size: ids decode back to the text
+    assert gpu.decode(torch.from_numpy(ids)) == text.tobytes()
+    gpu.close()
+
+
+# ---------------------------------------------------------------------------
+# Edge cases
+
+ALPHABET = ["a", "s", "L", "1", " ", "\n", "\r", "\t", "'", ".", "é", "ा", "\U0001F600",
+            " ", "\x00", "ſ", "१", "v", "e", "r", "l", "T", "<|endoftext|>", "中"]
+
+
+def test_random_segments_fuzz(full_gpu, full_enc):
+    rng = np.random.default_rng(11)
+    segs = []
+    for i in range(3000):
+        L = int(rng.integers(0, 40))
+        s = "".join(ALPHABET[j] for j in rng.integers(0, len(ALPHABET), size=L))
+        segs.append((s, bool(rng.integers(0, 2))))
+    _compare(full_gpu, full_enc, segs, False)
+    _compare(full_gpu, full_enc, segs, True)
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 15, 16, 17, 4095, 4096, 4097, 8191, 8193, 12288 + 5])
+def test_ragged_sizes(full_gpu, full_enc, full_table, n):
+    text = workloads.prose_text(full_table, n + 10, seed=n)[:n]
+    while n and (text[-1] & 0xC0) == 0x80:
+        text = text[:-1]
+    _compare(full_gpu, full_enc, [(text, False)], False)
+
+
+def test_empty_segments(full_gpu, full_enc):
+    segs = [("", True), ("", False), ("ab cd", False), ("", True), ("<|endoftext|>", True), ("", False)]
+    _compare(full_gpu, full_enc, segs, True)
+    _compare(full_gpu, full_enc, [("", False)], False)
+
+
+def test_tile_boundary_runs(full_gpu, full_enc):
+    """Runs that straddle 4 KiB tiles: digits (mod-3 grouping carried across
+    tiles), white space with CR/LF, other runs followed by CR/LF, specials,
+    contractions and multi-byte characters at the boundary."""
+    cases = []
+    for off in range(4080, 4100):
+        pad = "x" * (off - 3)
+        cases.append(pad + " " + "1234567890" * 3 + " end")
+        cases.append(pad + "..\n\n   word")
+        cases.append(pad + "\n\n    \n   \tcode")
+        cases.append(pad + "it's 'll 'VE don't")
+        cases.append(pad + "é中\U0001F600ſ'ſ")
+        cases.append(pad + "<|endoftext|><|fim_prefix|>")
+        cases.append(pad + "   \n")
+    for c in cases:
+        _compare(full_gpu, full_enc, [(c, True)], False)
+        _compare(full_gpu, full_enc, [(c, False)], True)
+
+
+def test_long_digit_and_space_runs(full_gpu, full_enc):
+    for text in ["7" * 20011, " " * 30000 + "x", "\n" * 9000 + "  " + "a" * 9000,
+                 "." * 5000 + "\n" * 5000 + " " * 5000 + "z", " " * 70001, "ab" * 40000]:
+        _compare(full_gpu, full_enc, [(text, False)], False)
+        _compare(full_gpu, full_enc, [(text, True)], True)
+
+
+def test_safe_chunking_window(full_gpu, full_enc):
+    text = "é" * 399_999 + "中" + "\U0001F600" * 5 + "x" * 10 + " " * 60_000 + "<|endoftext|>" + "y" * 26_000
+    _compare(full_gpu, full_enc, [(text, True)], True)
+    _compare(full_gpu, full_enc, [(text, False)], True)
+
+
+def test_invalid_utf8(full_gpu):
+    import byte_level_bpe_gb300 as tk
+    for bad, pos in [(b"ab\xffcd", 2), (b"abc\xc0\x80", 3), (b"\xed\xa0\x80", 0), (b"xy\xe4\xb8", 2),
+                     (b"\x80", 0), (b"a" * 5000 + b"\xf5", 5000)]:
+        with pytest.raises(tk.TkError) as ei:
+            full_gpu.encode(bad)
+        assert ei.value.code == tk.native.TK_E_UTF8
+        assert f"byte {pos}" in str(ei.value)
+
+
+def test_capacity_error_reports_count(full_gpu, full_enc):
+    import byte_level_bpe_gb300 as tk
+    text = b"hello world, this is a test"
+    exp = full_enc.encode(text)
+    d_text = torch.frombuffer(bytearray(text), dtype=torch.uint8).cuda()
+    d_off = torch.tensor([0, len(text)], dtype=torch.int64, device="cuda")
+    d_allow = torch.zeros(1, dtype=torch.uint8, device="cuda")
+    out = torch.empty(2, dtype=torch.int32, device="cuda")
+    with pytest.raises(tk.TkError) as ei:
+        full_gpu.encode_device(d_text, d_off, d_allow, False, out=out)
+    assert ei.value.code == tk.native.TK_E_CAPACITY
+    rc, n = tk.native.tk_encode_segments(full_gpu.handle, full_gpu.workspace, d_text.data_ptr(),
+                                         len(text), d_off.data_ptr(), d_allow.data_ptr(), 1, 0,
+                                         out.data_ptr(), 2, d_off.data_ptr() if False else
+                                         torch.empty(2, dtype=torch.int64, device="cuda").data_ptr(),
+                                         torch.cuda.current_stream().cuda_stream, raise_on_error=False)
+    assert rc == tk.native.TK_E_CAPACITY and n == len(exp)
+
+
+def test_unaligned_text_pointer(full_gpu, full_enc, full_table):
+    text = workloads.prose_text(full_table, 20000, seed=4)
+    buf = torch.frombuffer(bytearray(b"z" + text), dtype=torch.uint8).cuda()
+    d_text = buf[1:]
+    assert d_text.data_ptr() % 16 != 0
+    d_off = torch.tensor([0, len(text)], dtype=torch.int64, device="cuda")
+    d_allow = torch.zeros(1, dtype=torch.uint8, device="cuda")
+    ids, _ = full_gpu.encode_device(d_text, d_off, d_allow, False)
+    assert np.array_equal(ids.cpu().numpy(), full_enc.encode(text))
+
+
+def test_decode_round_trip_and_bad_id(full_gpu):
+    import byte_level_bpe_gb300 as tk
+    s = "NUL:\x00 emoji:\U0001F600 CJK:中文 replaced:\ud800 end <|endoftext|>"
+    ids, _ = full_gpu.encode_segments([(s, True)])
+    assert full_gpu.decode(ids) == s.encode("utf-8", "replace")
+    with pytest.raises(tk.TkError) as ei:
+        full_gpu.decode(np.array([65, 100256], np.int32))  # 100256 is in the reserved gap
+    assert ei.value.code == tk.native.TK_E_BADID
+
+
+def test_host_buffer_entry_point(full_gpu, full_enc, full_table):
+    segs = workloads.agentic_segments(full_table, seed=7, scale=0.01)
+    text, off, allow = workloads.pack_segments(segs)
+    ids, offs = full_gpu.encode_host(np.ascontiguousarray(text), off, allow, tiktoken_safe=True)
+    o_ids, o_off = full_enc.encode_segments(segs, tiktoken_safe=True)
+    assert np.array_equal(ids, o_ids) and np.array_equal(offs, o_off)
+
+
+def test_two_calls_in_a_row_reuse_workspace(full_gpu, full_enc, full_table):
+    a = workloads.prose_text(full_table, 50000, seed=8)
+    b = workloads.prose_text(full_table, 30000, seed=9)
+    for t in (a, b, a):
+        _compare(full_gpu, full_enc, [(t, False)], False)
