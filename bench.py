@@ -36,11 +36,12 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def make_workload(name, rank=0):
+def make_workload(name, rank=0, total_mb=256):
     import workloads
     table = workloads.full_table()
     if name == "serving":
-        text, off = workloads.serving_batch(table, seed=5 + 1000 * rank)
+        text, off = workloads.serving_batch(table, seed=5 + 1000 * rank, total=total_mb << 20,
+                                            n_req=max(16, 4096 * total_mb // 256))
         allow = np.zeros(len(off) - 1, np.uint8)
         desc = ("serving batch: 4,096 requests, log-normal lengths (median 8,192, max 400,000), "
                 "256 MiB total, 90% of each request repeats an earlier one; 100,256-rank "
@@ -109,11 +110,12 @@ class Clocks:
 # n = input bytes, p = pre-tokens, t = ids, s = segments.
 def kernel_bytes(name, n, p, t, s):
     return {
-        "k_split": n + 4 * (p + 1) + 8 * (s + 1),      # read text + segment table, write pre-token starts
-        "k_merge_short": 8 * p + n + 4 * t + 4 * p,    # read starts (2x4) and bytes, write ids and counts
-        "k_scan_u32": 8 * p,                           # read counts, write offsets
-        "k_scatter": 16 * p + 8 * t,                   # read starts, counts, offsets, staged ids; write ids
-        "k_seg_offsets": 16 * (s + 1),
+        # read the text and the segment table, write the pre-token start bitmap
+        "k_split": n + n // 8 + 8 * (s + 1),
+        # read the text and the start bitmap, write the ids and the segment offsets
+        "k_encode_tiles": n + n // 8 + 4 * t + 16 * (s + 1),
+        "k_chunk_scan_windows": n + n // 8,
+        "k_chunk_scan_runs": n + n // 8,
     }.get(name)
 
 
@@ -125,7 +127,7 @@ def run_gpu(args, rank, world):
 
     dev = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev)
-    table, text, off, allow, safe, desc = make_workload(args.workload, rank)
+    table, text, off, allow, safe, desc = make_workload(args.workload, rank, args.total_mb)
     n, S = int(text.size), int(off.size - 1)
     tok = tk.Tokenizer(table, {k: v for k, v in __import__("workloads").SPECIALS.items()},
                        max_bytes=n, max_segments=S)
@@ -176,14 +178,16 @@ def run_gpu(args, rank, world):
                                               h_out.ctypes.data, n, h_out_off.ctypes.data,
                                               stream.cuda_stream)[1]
 
-    host_step()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    e2e_steps = max(1, min(args.steps, 5))
-    for _ in range(e2e_steps):
+    e2e_ms = float("nan")
+    if not args.no_e2e:
         host_step()
-    torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_steps = max(1, min(args.steps, 5))
+        for _ in range(e2e_steps):
+            host_step()
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
     if world > 1:
         t = torch.tensor([e2e_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -224,6 +228,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="serving", choices=["serving", "agentic"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--total-mb", type=int, default=256,
+                    help="serving batch size in MiB (256 = the benchmark workload; smaller for profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -234,7 +242,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        table, text, off, allow, safe, desc = make_workload(args.workload, 0)
+        table, text, off, allow, safe, desc = make_workload(args.workload, 0, args.total_mb)
         for _ in range(max(0, min(args.warmup, 1))):
             pass
         rates = []
@@ -282,9 +290,11 @@ def main():
     launches = int(sum(v[1] for v in prof.values()))
     if rank != 0:
         return
-    cpu_mbs, cpu_tps, cpu_b, cpu_seg, cpu_s = oracle_sample_rate(r["table"], r["text"], r["off"],
-                                                                 r["allow"], r["safe"],
-                                                                 seconds=args.cpu_seconds)
+    cpu_mbs = cpu_tps = cpu_s = float("nan")
+    cpu_b = cpu_seg = 0
+    if not args.no_cpu_baseline:
+        cpu_mbs, cpu_tps, cpu_b, cpu_seg, cpu_s = oracle_sample_rate(
+            r["table"], r["text"], r["off"], r["allow"], r["safe"], seconds=args.cpu_seconds)
     e2e_val = total_n / (r["e2e_ms"] * 1e-3) / 1e6
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "MB/s", "n_gpus": world,
@@ -309,7 +319,16 @@ def main():
         "gpu_launches": launches,
         "clocks": r["clocks"],
     }
-    print(json.dumps(line))
+    print(json.dumps(_finite(line)))
+
+
+def _finite(x):
+    """NaN (a skipped leg) -> null, recursively."""
+    if isinstance(x, dict):
+        return {k: _finite(v) for k, v in x.items()}
+    if isinstance(x, float) and x != x:
+        return None
+    return x
 
 
 if __name__ == "__main__":

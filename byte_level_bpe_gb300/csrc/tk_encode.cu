@@ -197,8 +197,9 @@ __device__ uint8_t g_kc(const Call& c, int64_t pos, int* len) {
   return kclass(cp);
 }
 
+// Start of the code point before pos (a 4-byte sequence has its lead 4 back).
 __device__ int64_t g_prev(const Call& c, int64_t pos) {
-  for (int k = 1; k <= 3; k++)
+  for (int k = 1; k <= 4; k++)
     if ((gbyte(c, pos - k) & 0xC0) != 0x80) return pos - k;
   return pos - 1;
 }
@@ -206,14 +207,12 @@ __device__ int64_t g_prev(const Call& c, int64_t pos) {
 // --------------------------------------------------------------------------
 // Look-back helpers (one thread).
 
-struct SumOp {
-  __device__ static uint64_t id() { return 0; }
-  __device__ static uint64_t comb(uint64_t l, uint64_t r) { return l + r; }
-};
 // Number-run carry: bit 2 = the tile is one unbroken run of numbers, bits 0-1
 // = count of numbers at its end, mod 3.
 struct NRunOp {
   __device__ static uint64_t id() { return 4; }
+  __device__ static uint64_t reset_id() { return 0; }          // before the text: no run
+  __device__ static bool resets(uint64_t v) { return !(v & 4); }
   __device__ static uint64_t comb(uint64_t l, uint64_t r) {
     if (!(r & 4)) return r;
     return (l & 4) | (((l & 3) + (r & 3)) % 3);
@@ -222,53 +221,25 @@ struct NRunOp {
 // Segmented count: bit 40 = a head was seen, bits 0-39 = count since it.
 struct SegCountOp {
   __device__ static uint64_t id() { return 0; }
+  __device__ static uint64_t reset_id() { return 1ull << 40; }  // before the text: a head
+  __device__ static bool resets(uint64_t v) { return (v >> 40) != 0; }
   __device__ static uint64_t comb(uint64_t l, uint64_t r) {
     if (r >> 40) return r;
     return (l & (1ull << 40)) | ((l & ((1ull << 40) - 1)) + r);
   }
 };
 
-// Publishes the tile's aggregate, waits for the predecessors and returns the
-// exclusive prefix; publishes the inclusive prefix.  Waits are bounded.
-template <class Op>
-__device__ uint64_t chain_exclusive(uint64_t* desc, int64_t tile, uint64_t agg, Status* st, int kind) {
-  if (tile == 0) {
-    st_release_u64(&desc[0], DESC_PREFIX | agg);
-    return Op::id();
-  }
-  st_release_u64(&desc[tile], DESC_AGG | agg);
-  uint64_t acc = Op::id();
-  int64_t j = tile - 1;
-  uint32_t spins = 0;
-  while (j >= 0) {
-    const uint64_t d = ld_acquire_u64(&desc[j]);
-    const uint64_t state = d & ~DESC_VAL;
-    if (state == 0) {
-      if (++spins > SPIN_LIMIT) {
-        set_error(st, TK_E_TIMEOUT, kind);
-        break;
-      }
-      __nanosleep(64);
-      continue;
-    }
-    acc = Op::comb(d & DESC_VAL, acc);
-    if (state == DESC_PREFIX) break;
-    j--;
-  }
-  st_release_u64(&desc[tile], DESC_PREFIX | Op::comb(acc, agg));
-  return acc;
-}
-
 // --------------------------------------------------------------------------
 // Kernel: zero the status block and the look-back descriptors of one call.
 
 __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int safe,
-                        int64_t n_cut_words) {
+                        int64_t n_cut_words, int64_t n_tiles) {
   const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (tid == 0) {
     Status s = {};
     s.err_pos = INT64_MAX;
+    s.n_tiles = n_tiles;
     *W.status = s;
   }
   for (int64_t i = tid; i < n_desc_split; i += stride) {
@@ -358,15 +329,19 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) 
     }
     s_agg[tid] = agg;
     __syncthreads();
-    if (tid == 0) {
-      // serial exclusive combine over 256 thread aggregates (cheap)
+    if (tid < 32) {
       uint64_t run = SegCountOp::id();
-      for (int t = 0; t < SPLIT_THREADS; t++) {
-        const uint64_t a = s_agg[t];
-        s_agg[t] = run;
-        run = SegCountOp::comb(run, a);
+      if (tid == 0) {
+        // exclusive combine over the 256 thread aggregates
+        for (int t = 0; t < SPLIT_THREADS; t++) {
+          const uint64_t a = s_agg[t];
+          s_agg[t] = run;
+          run = SegCountOp::comb(run, a);
+        }
       }
-      s_carry = chain_exclusive<SegCountOp>(desc, tile, run, c.W.status, 2 + mode);
+      run = __shfl_sync(0xffffffffu, run, 0);
+      const uint64_t carry = carry_walk_warp<SegCountOp>(desc, tile, run, c.W.status, 2 + mode);
+      if (tid == 0) s_carry = carry;
     }
     __syncthreads();
     uint64_t v = SegCountOp::comb(s_carry, s_agg[tid]);
@@ -399,7 +374,7 @@ struct SplitSmem {
   int64_t tile;
   int64_t seg[2];
   uint64_t ncarry;
-  uint64_t base;
+  uint32_t first;  // first pre-token start of the tile (tile-relative), or all ones
 };
 
 // Special match of the longest special at window position x (all bytes must be
@@ -443,7 +418,7 @@ struct Win {
   }
   __device__ int64_t prev(int64_t p) const {
     if (trusted(p) && trusted(p - 4)) {
-      for (int k = 1; k <= 3; k++)
+      for (int k = 1; k <= 4; k++)
         if ((sm.kc[p - k - wlo] & 7) != K_CONT) return p - k;
       return p - 1;
     }
@@ -537,6 +512,7 @@ __device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) 
 __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
   __shared__ SplitSmem sm;
   const int tid = threadIdx.x;
+  if (tid == 0) sm.first = 0xFFFFFFFFu;
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const bool aligned = ((uintptr_t)c.text & 15) == 0;
   for (;;) {
@@ -640,16 +616,34 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
       if (bit_get(sm.pst, x)) { nreset = 1; ncount = 0; }
       ncount = (ncount + 1) % 3;
     }
-    sm.nagg[tid] = (nreset ? 0u : 4u) | ncount;
-    __syncthreads();
-    if (tid == 0) {
-      uint64_t run = NRunOp::id();
-      for (int t = 0; t < SPLIT_THREADS; t++) {
-        const uint64_t a = sm.nagg[t];
-        sm.nagg[t] = (uint32_t)run;
-        run = NRunOp::comb(run, a);
+    {
+      // exclusive block scan of the number-run aggregates (warp shuffles)
+      uint32_t x = (nreset ? 0u : 4u) | ncount;
+      const uint32_t v = x;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if ((tid & 31) >= o) x = (uint32_t)NRunOp::comb(y, x);
       }
-      sm.ncarry = chain_exclusive<NRunOp>(c.W.desc_a, tile, run, c.W.status, 4);
+      if ((tid & 31) == 31) sm.scan[tid >> 5] = x;
+      __syncthreads();
+      if (tid < 32) {
+        uint64_t run = NRunOp::id();
+        if (tid == 0) {
+          for (int w = 0; w < SPLIT_THREADS / 32; w++) {
+            const uint64_t a = sm.scan[w];
+            sm.scan[w] = (uint32_t)run;
+            run = NRunOp::comb(run, a);
+          }
+        }
+        run = __shfl_sync(0xffffffffu, run, 0);
+        const uint64_t carry = carry_walk_warp<NRunOp>(c.W.desc_a, tile, run, c.W.status, 4);
+        if (tid == 0) sm.ncarry = carry;
+      }
+      __syncthreads();
+      uint32_t e = __shfl_up_sync(0xffffffffu, x, 1);
+      if ((tid & 31) == 0) e = (uint32_t)NRunOp::id();
+      (void)v;
+      sm.nagg[tid] = (uint32_t)NRunOp::comb(sm.scan[tid >> 5], e);
     }
     __syncthreads();
     // 6. the start test for each code point of this thread
@@ -684,283 +678,758 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
       atomicOr(&sm.outb[tid >> 1], bits << (16 * (tid & 1)));
     }
     __syncthreads();
-    // 7. ordered records
-    const uint32_t mine = (sm.outb[tid >> 1] >> (16 * (tid & 1))) & 0xFFFFu;
-    sm.scan[tid] = __popc(mine);
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t run = 0;
-      for (int t = 0; t < SPLIT_THREADS; t++) {
-        const uint32_t a = sm.scan[t];
-        sm.scan[t] = run;
-        run += a;
-      }
-      sm.base = chain_exclusive<SumOp>(c.W.desc_b, tile, run, c.W.status, 5);
-      if (tile == ntiles - 1) {
-        const uint64_t total = sm.base + run;
-        c.W.status->n_ptok = (int64_t)total;
-        c.W.ptok[total] = (uint32_t)c.n;
-      }
+    // 7. start bitmaps of the tile and the position of its first start
+    for (int i = tid; i < TILE / 32; i += SPLIT_THREADS) {
+      const int64_t word = (t0 >> 5) + i;
+      const uint32_t w = sm.outb[i];
+      c.W.pbits[word] = w;
+      if (c.T.n_spec) c.W.sbits[word] = w & sm.sst[(HALO >> 5) + i];
+      if (w) atomicMin(&sm.first, (uint32_t)(32 * i + __ffs(w) - 1));
     }
     __syncthreads();
-    {
-      uint64_t o = sm.base + sm.scan[tid];
-      for (int j = 0; j < 16; j++) {
-        if (!((mine >> j) & 1)) continue;
-        const int x = xb + j;
-        const uint32_t pos = (uint32_t)(wlo + x);
-        c.W.ptok[o++] = pos | (bit_get(sm.insp, x) ? PTOK_SPECIAL : 0u);
-      }
+    if (tid == 0) {
+      c.W.tile_first[tile] = sm.first;
+      sm.first = 0xFFFFFFFFu;
     }
     __syncthreads();
   }
 }
 
 // --------------------------------------------------------------------------
-// Merge of short pre-tokens: the parts loop in one thread.
+// Merging.  Pieces are token ids; the merged piece of a pair of rank r is the
+// token r (rank = id), so the parts loop never touches bytes after its first
+// round ("Inside encode: a parts vector and a linear scan").
 
-__device__ int special_id_at(const Call& c, int64_t pos, int len) {
-  for (int k = 0; k < c.T.n_spec; k++) {
-    const int L = c.T.spec_off[k + 1] - c.T.spec_off[k];
+// The parts loop of one pre-token of n <= SHORT_MAX bytes in one thread: the
+// first round reads the dense two-byte table, later rounds the pair table;
+// the leftmost minimum merges and only its two neighbours are re-ranked.
+// Returns the number of ids written to out.
+__device__ __forceinline__ int merge_thread(const Tables& T, const uint8_t* b, int n, int32_t* out) {
+  uint32_t ids[SHORT_MAX], rk[SHORT_MAX];
+  uint32_t prevb = b[0];
+  ids[0] = __ldg(&T.byte_id[prevb]);
+  for (int i = 1; i < n; i++) {
+    const uint32_t x = b[i];
+    ids[i] = __ldg(&T.byte_id[x]);
+    rk[i - 1] = __ldg(&T.dense[(prevb << 8) | x]);
+    prevb = x;
+  }
+  rk[n - 1] = RANK_MAX;
+  int m = n;
+  while (m > 1) {
+    uint32_t best = RANK_MAX;
+    int bi = -1;
+    for (int i = 0; i + 1 < m; i++)
+      if (rk[i] < best) { best = rk[i]; bi = i; }
+    if (best == RANK_MAX) break;
+    ids[bi] = best;
+    for (int i = bi + 1; i + 1 < m; i++) { ids[i] = ids[i + 1]; rk[i] = rk[i + 1]; }
+    m--;
+    rk[bi] = (bi + 1 < m) ? pair_rank(T, ids[bi], ids[bi + 1]) : RANK_MAX;
+    if (bi > 0) rk[bi - 1] = pair_rank(T, ids[bi - 1], ids[bi]);
+  }
+  for (int i = 0; i < m; i++) out[i] = (int32_t)ids[i];
+  return m;
+}
+
+// The same loop for a pre-token of n <= W bytes with every array in
+// registers: fully unrolled, dynamic positions handled by predicated selects.
+// b must have W readable bytes.
+template <int W>
+__device__ __forceinline__ int merge_reg(const MergeTabs T, const uint8_t* b, int n, int32_t* out) {
+  uint32_t ids[W], rk[W];
+#pragma unroll
+  for (int i = 0; i < W; i++) {
+    uint32_t v = 0;
+    if (i < n) v = __ldg(&T.byte_id[b[i]]);
+    ids[i] = v;
+  }
+#pragma unroll
+  for (int i = 0; i < W - 1; i++) {
+    uint32_t v = RANK_MAX;
+    if (i + 1 < n) v = __ldg(&T.dense[((uint32_t)b[i] << 8) | b[i + 1]]);
+    rk[i] = v;
+  }
+  rk[W - 1] = RANK_MAX;
+  int m = n;
+  while (m > 1) {
+    // leftmost minimum (strict <)
+    uint32_t best = rk[0];
+    int bi = 0;
+#pragma unroll
+    for (int i = 1; i < W - 1; i++) {
+      const bool lt = rk[i] < best;
+      best = lt ? rk[i] : best;
+      bi = lt ? i : bi;
+    }
+    if (best == RANK_MAX) break;
+    // piece bi becomes the token `best`; pieces after bi + 1 move down one
+#pragma unroll
+    for (int i = 0; i < W - 1; i++) {
+      const uint32_t nid = (i == bi) ? best : ((i > bi) ? ids[i + 1] : ids[i]);
+      const uint32_t nrk = (i > bi) ? rk[i + 1] : rk[i];
+      ids[i] = nid;
+      rk[i] = nrk;
+    }
+    rk[W - 1] = RANK_MAX;
+    m--;
+    // re-rank the pairs at bi and bi - 1
+    uint32_t a_prev = 0, a = 0, a_next = 0;
+#pragma unroll
+    for (int i = 0; i < W; i++) {
+      a_prev = (i == bi - 1) ? ids[i] : a_prev;
+      a = (i == bi) ? ids[i] : a;
+      a_next = (i == bi + 1) ? ids[i] : a_next;
+    }
+    const uint32_t r0 = (bi + 1 < m) ? pair_rank(T, a, a_next) : RANK_MAX;
+    const uint32_t r1 = (bi > 0) ? pair_rank(T, a_prev, a) : RANK_MAX;
+#pragma unroll
+    for (int i = 0; i < W; i++) rk[i] = (i == bi) ? r0 : ((i == bi - 1) ? r1 : rk[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < W; i++)
+    if (i < m) out[i] = (int32_t)ids[i];
+  return m;
+}
+
+// One pre-token of 1..16 bytes: closed forms for one and two bytes (the
+// loop's result written out), else the register loop of the smallest width.
+__device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, int n, int32_t* out) {
+  const uint32_t b0 = b[0];
+  if (n == 1) {
+    out[0] = (int32_t)__ldg(&T.byte_id[b0]);
+    return 1;
+  }
+  if (n == 2) {
+    const uint32_t b1 = b[1];
+    const uint32_t r = __ldg(&T.dense[(b0 << 8) | b1]);
+    if (r != RANK_MAX) {
+      out[0] = (int32_t)r;
+      return 1;
+    }
+    out[0] = (int32_t)__ldg(&T.byte_id[b0]);
+    out[1] = (int32_t)__ldg(&T.byte_id[b1]);
+    return 2;
+  }
+  if (n <= 4) return merge_reg<4>(T, b, n, out);
+  if (n <= 8) return merge_reg<8>(T, b, n, out);
+  return merge_reg<16>(T, b, n, out);
+}
+
+// Length class of a pre-token for the tile's work list (warps then run
+// pieces of one class together).
+__device__ __forceinline__ int len_class(int n) {
+  return n == 1 ? 0 : n == 2 ? 1 : n <= 4 ? 2 : n <= 8 ? 3 : n <= 16 ? 4 : 5;
+}
+
+// The loop for one pre-token of up to SHORT_MAX bytes on caller-provided
+// shared scratch (ids, rk of SHORT_MAX entries each).
+__device__ __noinline__ int merge_scratch(const MergeTabs T, const uint8_t* b, int n, uint32_t* ids, uint32_t* rk,
+                             int32_t* out) {
+  uint32_t prevb = b[0];
+  ids[0] = __ldg(&T.byte_id[prevb]);
+  for (int i = 1; i < n; i++) {
+    const uint32_t x = b[i];
+    ids[i] = __ldg(&T.byte_id[x]);
+    rk[i - 1] = __ldg(&T.dense[(prevb << 8) | x]);
+    prevb = x;
+  }
+  rk[n - 1] = RANK_MAX;
+  int m = n;
+  while (m > 1) {
+    uint32_t best = RANK_MAX;
+    int bi = -1;
+    for (int i = 0; i + 1 < m; i++) {
+      const uint32_t r = rk[i];
+      if (r < best) { best = r; bi = i; }
+    }
+    if (best == RANK_MAX) break;
+    ids[bi] = best;
+    for (int i = bi + 1; i + 1 < m; i++) { ids[i] = ids[i + 1]; rk[i] = rk[i + 1]; }
+    m--;
+    rk[bi] = (bi + 1 < m) ? pair_rank(T, ids[bi], ids[bi + 1]) : RANK_MAX;
+    if (bi > 0) rk[bi - 1] = pair_rank(T, ids[bi - 1], ids[bi]);
+  }
+  for (int i = 0; i < m; i++) out[i] = (int32_t)ids[i];
+  return m;
+}
+
+// Cooperative groups for the round merge: a warp (no block barriers) or the
+// whole CTA.
+struct WarpGroup {
+  __device__ int rank() const { return threadIdx.x & 31; }
+  __device__ int size() const { return 32; }
+  __device__ void sync() const { __syncwarp(); }
+  __device__ uint32_t min_u32(uint32_t v) const {
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+  }
+  // exclusive scan (op 0 = sum, 1 = max) with the group total in *tot
+  __device__ int64_t excl(int64_t v, int op, int64_t* tot) const {
+    const int l = threadIdx.x & 31;
+    int64_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (l >= o) x = op ? max(x, y) : x + y;
+    }
+    *tot = __shfl_sync(0xffffffffu, x, 31);
+    const int64_t e = __shfl_up_sync(0xffffffffu, x, 1);
+    return l == 0 ? (op ? INT64_MIN : 0) : e;
+  }
+};
+
+struct BlockGroup {
+  int64_t* red64;  // [blockDim / 32]
+  uint32_t* red32;
+  __device__ int rank() const { return threadIdx.x; }
+  __device__ int size() const { return blockDim.x; }
+  __device__ void sync() const { __syncthreads(); }
+  __device__ uint32_t min_u32(uint32_t v) const {
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red32[w] = v;
+    __syncthreads();
+    if (w == 0) {
+      v = (l < (int)(blockDim.x >> 5)) ? red32[l] : RANK_MAX;
+      for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+      if (l == 0) red32[0] = v;
+    }
+    __syncthreads();
+    const uint32_t r = red32[0];
+    __syncthreads();
+    return r;
+  }
+  __device__ int64_t excl(int64_t v, int op, int64_t* tot) const {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int64_t idv = op ? INT64_MIN : 0;
+    int64_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (l >= o) x = op ? max(x, y) : x + y;
+    }
+    __syncthreads();
+    if (l == 31) red64[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int64_t y = (l < nw) ? red64[l] : idv;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t z = __shfl_up_sync(0xffffffffu, y, o);
+        if (l >= o) y = op ? max(y, z) : y + z;
+      }
+      if (l < nw) red64[l] = y;
+    }
+    __syncthreads();
+    const int64_t we = w ? red64[w - 1] : idv;
+    const int64_t le = __shfl_up_sync(0xffffffffu, x, 1);
+    const int64_t e = (l == 0) ? we : (op ? max(we, le) : we + le);
+    *tot = red64[nw - 1];
+    __syncthreads();
+    return e;
+  }
+};
+
+// Exact round merge of the pre-token text[s .. s+n) by a group (see the file
+// header).  Works in the workspace at the piece's byte offset; the ids end in
+// arena[s ..].  Returns the number of ids.
+template <class G>
+__device__ int64_t merge_rounds(const Call& c, const G& g, int64_t s, int64_t n) {
+  uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + s);
+  uint32_t* A_rk = c.W.lrk + s;
+  uint32_t* B_ids = c.W.lids2 + s;
+  uint32_t* B_rk = c.W.lrk2 + s;
+  uint8_t* sel = c.W.lsel + s;
+  uint8_t* chg = c.W.lchg + s;
+  const int T = g.size(), tid = g.rank();
+  const int64_t n0 = n;
+  for (int64_t i = tid; i < n; i += T) {
+    const uint32_t b = gbyte(c, s + i);
+    A_ids[i] = __ldg(&c.T.byte_id[b]);
+    A_rk[i] = (i + 1 < n) ? __ldg(&c.T.dense[(b << 8) | gbyte(c, s + i + 1)]) : RANK_MAX;
+  }
+  g.sync();
+  bool in_b = false;
+  for (int64_t round = 0;; round++) {
+    const int64_t C = (n + T - 1) / T;
+    const int64_t lo = min(n, tid * C), hi = min(n, lo + C);
+    // (1) the minimum pair rank
+    uint32_t m = RANK_MAX;
+    for (int64_t i = lo; i < hi; i++) m = min(m, A_rk[i]);
+    const uint32_t rs = g.min_u32(m);
+    if (rs == RANK_MAX) break;
+    // (2) chains of rs-pairs: every other pair from each chain's start
+    int64_t last_non = -1;
+    for (int64_t i = lo; i < hi; i++)
+      if (A_rk[i] != rs) last_non = i;
+    int64_t tot;
+    const int64_t before = g.excl(last_non, 1, &tot);
+    int64_t ln = before < -1 ? -1 : before;
+    for (int64_t i = lo; i < hi; i++) {
+      if (A_rk[i] != rs) { ln = i; sel[i] = 0; }
+      else sel[i] = ((i - ln - 1) & 1) == 0;
+    }
+    g.sync();
+    // (3) the first selected merge that creates a neighbour pair of lower rank
+    uint32_t first_bad = 0xFFFFFFFFu;
+    for (int64_t i = lo; i < hi && first_bad == 0xFFFFFFFFu; i++) {
+      if (!sel[i]) continue;
+      bool bad = false;
+      if (i >= 1) {
+        const uint32_t left = (i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1];
+        bad = pair_rank(c.T, left, rs) < rs;
+      }
+      if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, A_ids[i + 2]) < rs;
+      if (bad) first_bad = (uint32_t)i;
+    }
+    const uint32_t limit = g.min_u32(first_bad);
+    // (4) merge the selected pairs up to limit, compacting into B
+    int64_t keep = 0;
+    for (int64_t i = lo; i < hi; i++)
+      keep += !(i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit);
+    int64_t dst = g.excl(keep, 0, &tot);
+    const int64_t n2 = tot;
+    for (int64_t i = lo; i < hi; i++) {
+      if (i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit) continue;
+      const bool merged = sel[i] && (uint64_t)i <= (uint64_t)limit;
+      B_ids[dst] = merged ? rs : A_ids[i];
+      B_rk[dst] = A_rk[i];
+      chg[dst] = merged;
+      dst++;
+    }
+    g.sync();
+    // (5) re-rank the pairs next to merged pieces
+    const int64_t C2 = (n2 + T - 1) / T;
+    const int64_t lo2 = min(n2, tid * C2), hi2 = min(n2, lo2 + C2);
+    for (int64_t q = lo2; q < hi2; q++) {
+      if (q + 1 >= n2) B_rk[q] = RANK_MAX;
+      else if (chg[q] || chg[q + 1]) B_rk[q] = pair_rank(c.T, B_ids[q], B_ids[q + 1]);
+    }
+    g.sync();
+    uint32_t* t1 = A_ids; A_ids = B_ids; B_ids = t1;
+    uint32_t* t2 = A_rk; A_rk = B_rk; B_rk = t2;
+    in_b = !in_b;
+    n = n2;
+    // every round merges at least one pair, so n0 rounds always suffice
+    if (round > n0) { if (tid == 0) set_error(c.W.status, TK_E_LIMIT, 6); break; }
+  }
+  if (in_b) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + s);
+    for (int64_t i = tid; i < n; i += T) dst[i] = A_ids[i];
+    g.sync();
+  }
+  return n;
+}
+
+// --------------------------------------------------------------------------
+// Fused encode of one 4 KiB tile: the pre-tokens that start in the tile are
+// merged (one thread each up to SHORT_MAX bytes, one warp up to MEDIUM_MAX,
+// the whole CTA above), their ids compacted in shared memory, the tile's
+// output offset taken by decoupled look-back, and the ids written in order.
+
+constexpr int ETHREADS = 256;
+constexpr int EPAD = 96;                 // bytes loaded past the tile (short pieces, specials)
+constexpr int MEDIUM_MAX = 1024;
+constexpr int MAX_GP = TILE / (SHORT_MAX + 1) + 2;  // pieces merged through global memory
+constexpr int REG_MAX = 16;  // pieces up to this length merge in registers
+constexpr uint32_t NO_START = 0xFFFFFFFFu;
+constexpr int64_t STG = TILE + SHORT_MAX + 8;       // staging slot per tile (u32 entries)
+
+struct GPiece {
+  uint32_t rel, len, cnt, short_excl, full_excl;
+};
+
+struct EncSmem {
+  uint8_t text[TILE + EPAD + 16];
+  uint32_t pb[(TILE + EPAD) / 32 + 1];  // pre-token starts in [t0, t0 + TILE + EPAD)
+  uint32_t sb[TILE / 32];               // special starts
+  uint32_t gb[TILE / 32];               // starts of pieces merged through global memory
+  uint8_t cnt[TILE];                    // ids of the short piece starting at each byte
+  uint8_t plen[TILE];                   // length of the short piece starting at each byte
+  uint32_t cls_cnt[8];                  // work list: pieces per length class, then cursors
+  int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
+  int32_t outs[TILE + SHORT_MAX];       // work list (x | len << 16), then compacted ids
+  uint32_t scr_ids[ETHREADS / 32][SHORT_MAX];  // per-warp scratch for 17..64-byte pieces
+  uint32_t scr_rk[ETHREADS / 32][SHORT_MAX];
+  GPiece gp[MAX_GP];
+  uint32_t th_full[ETHREADS];
+  uint32_t th_short[ETHREADS];
+  uint32_t warp_tot[2 * ETHREADS / 32];
+  int64_t red64[ETHREADS / 32];
+  uint32_t red32[ETHREADS / 32];
+  int n_gp;
+  uint32_t n_starts;
+  int64_t tile;
+  uint64_t base;
+  uint32_t tile_full, tile_short;
+  int64_t seg[2];
+};
+
+__device__ int32_t special_id_smem(const Tables& T, const uint8_t* b, int len) {
+  for (int k = 0; k < T.n_spec; k++) {
+    const int L = T.spec_off[k + 1] - T.spec_off[k];
     if (L != len) continue;
     bool m = true;
-    for (int j = 0; j < L && m; j++) m = gbyte(c, pos + j) == c.T.spec_bytes[c.T.spec_off[k] + j];
-    if (m) return c.T.spec_ids[k];
+    for (int j = 0; j < L && m; j++) m = b[j] == T.spec_bytes[T.spec_off[k] + j];
+    if (m) return T.spec_ids[k];
   }
   return -1;
 }
 
-__global__ void __launch_bounds__(128) k_merge_short(Call c) {
-  const int64_t P = c.W.status->n_ptok;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < P; k += stride) {
-    const uint32_t r0 = c.W.ptok[k];
-    const int64_t s = r0 & PTOK_MASK;
-    const int64_t e = c.W.ptok[k + 1] & PTOK_MASK;
-    const int n = (int)(e - s);
-    if (r0 & PTOK_SPECIAL) {
-      c.W.arena[s] = special_id_at(c, s, n);
-      c.W.cnt[k] = 1;
-      continue;
+// Ids before byte x of the tile (x in [0, TILE)), counted from the tile start.
+__device__ uint32_t ids_before(const EncSmem& sm, int x) {
+  const int t = x >> 4;
+  uint32_t r = sm.th_full[t];
+  for (int y = t << 4; y < x; y++) {
+    if (!((sm.pb[y >> 5] >> (y & 31)) & 1u)) continue;  // not a pre-token start
+    if ((sm.gb[y >> 5] >> (y & 31)) & 1u) {
+      for (int g = 0; g < sm.n_gp; g++)
+        if ((int)sm.gp[g].rel == y) r += sm.gp[g].cnt;
+    } else {
+      r += sm.cnt[y];
     }
-    if (n > SHORT_MAX) {
-      const uint32_t slot = atomicAdd(&c.W.status->n_long, 1u);
-      c.W.long_list[slot] = (uint32_t)k;
-      continue;
-    }
-    uint32_t ids[SHORT_MAX], rk[SHORT_MAX];
-    uint32_t prevb = gbyte(c, s);
-    ids[0] = __ldg(&c.T.byte_id[prevb]);
-    for (int i = 1; i < n; i++) {
-      const uint32_t b = gbyte(c, s + i);
-      ids[i] = __ldg(&c.T.byte_id[b]);
-      rk[i - 1] = __ldg(&c.T.dense[(prevb << 8) | b]);
-      prevb = b;
-    }
-    rk[n - 1] = RANK_MAX;
-    int m = n;
-    while (m > 1) {
-      uint32_t best = RANK_MAX;
-      int bi = -1;
-      for (int i = 0; i + 1 < m; i++)
-        if (rk[i] < best) { best = rk[i]; bi = i; }
-      if (best == RANK_MAX) break;
-      ids[bi] = best;  // the merged piece is the token of that rank
-      for (int i = bi + 1; i + 1 < m; i++) { ids[i] = ids[i + 1]; rk[i] = rk[i + 1]; }
-      m--;
-      rk[bi] = (bi + 1 < m) ? pair_rank(c.T, ids[bi], ids[bi + 1]) : RANK_MAX;
-      if (bi > 0) rk[bi - 1] = pair_rank(c.T, ids[bi - 1], ids[bi]);
-    }
-    for (int i = 0; i < m; i++) c.W.arena[s + i] = (int32_t)ids[i];
-    c.W.cnt[k] = (uint32_t)m;
   }
-}
-
-// --------------------------------------------------------------------------
-// Merge of long pre-tokens: one CTA per piece, exact rounds (see the file
-// header).  Arrays live in the workspace at the piece's byte offset.
-
-__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, uint32_t* red) {
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) red[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    v = (l < (int)(blockDim.x >> 5)) ? red[l] : RANK_MAX;
-    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (l == 0) red[0] = v;
-  }
-  __syncthreads();
-  const uint32_t r = red[0];
-  __syncthreads();
   return r;
 }
 
-// exclusive scan of per-thread values (int64) across the block; returns the
-// exclusive prefix, total in *tot.  op: 0 = sum, 1 = max.
-__device__ __forceinline__ int64_t block_scan_i64(int64_t v, int op, int64_t* red, int64_t* tot) {
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  int64_t x = v;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (l >= o) x = op ? max(x, y) : x + y;
-  }
-  __syncthreads();
-  if (l == 31) red[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    const int nw = blockDim.x >> 5;
-    int64_t y = (l < nw) ? red[l] : (op ? INT64_MIN : 0);
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t z = __shfl_up_sync(0xffffffffu, y, o);
-      if (l >= o) y = op ? max(y, z) : y + z;
-    }
-    red[l] = y;  // inclusive over warps
-  }
-  __syncthreads();
-  const int64_t warp_excl = (w == 0) ? (op ? INT64_MIN : 0) : red[w - 1];
-  const int64_t incl = op ? max(warp_excl, x) : warp_excl + x;
-  const int64_t excl_in_warp = __shfl_up_sync(0xffffffffu, x, 1);
-  int64_t excl = (l == 0) ? warp_excl : (op ? max(warp_excl, excl_in_warp) : warp_excl + excl_in_warp);
-  *tot = red[(blockDim.x >> 5) - 1];
-  (void)incl;
-  __syncthreads();
-  return excl;
-}
-
-__global__ void __launch_bounds__(LONG_THREADS) k_merge_long(Call c) {
-  __shared__ int64_t red64[LONG_THREADS / 32];
-  __shared__ uint32_t red32[LONG_THREADS / 32];
-  __shared__ uint32_t s_idx;
-  const int tid = threadIdx.x, T = blockDim.x;
+__global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  EncSmem& sm = *reinterpret_cast<EncSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  const bool aligned = ((uintptr_t)c.text & 15) == 0;
   for (;;) {
-    if (tid == 0) s_idx = atomicAdd(&c.W.status->long_next, 1u);
+    if (tid == 0) sm.tile = atomicAdd(&c.W.status->tile_ctr[4], 1u);
     __syncthreads();
-    const uint32_t li = s_idx;
-    __syncthreads();
-    if (li >= c.W.status->n_long) break;
-    const int64_t k = c.W.long_list[li];
-    const int64_t s = c.W.ptok[k] & PTOK_MASK;
-    const int64_t e = c.W.ptok[k + 1] & PTOK_MASK;
-    int64_t n = e - s;
-    uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + s);
-    uint32_t* A_rk = c.W.lrk + s;
-    uint32_t* B_ids = c.W.lids2 + s;
-    uint32_t* B_rk = c.W.lrk2 + s;
-    uint8_t* sel = c.W.lsel + s;
-    uint8_t* chg = c.W.lchg + s;
-    for (int64_t i = tid; i < n; i += T) {
-      const uint32_t b = gbyte(c, s + i);
-      A_ids[i] = __ldg(&c.T.byte_id[b]);
-      A_rk[i] = (i + 1 < n) ? __ldg(&c.T.dense[(b << 8) | gbyte(c, s + i + 1)]) : RANK_MAX;
+    const int64_t tile = sm.tile;
+    if (tile >= ntiles) break;
+    const int64_t t0 = tile * TILE;
+    // 1. bytes, start bits (positions >= n read as no start), special starts
+    for (int v = tid; v < (TILE + EPAD + 16) / 16; v += ETHREADS) {
+      const int64_t p = t0 + 16 * v;
+      if (aligned && p + 16 <= c.n) {
+        *reinterpret_cast<uint4*>(&sm.text[16 * v]) = __ldg(reinterpret_cast<const uint4*>(c.text + p));
+      } else {
+        for (int j = 0; j < 16; j++) sm.text[16 * v + j] = gbyte(c, p + j);
+      }
+    }
+    for (int i = tid; i < (TILE + EPAD) / 32 + 1; i += ETHREADS) {
+      const int64_t p = t0 + 32 * i;
+      uint32_t w = 0;
+      if (p < c.n) {
+        w = c.W.pbits[(t0 >> 5) + i];
+        if (p + 32 > c.n) w &= (1u << (c.n - p)) - 1u;
+      }
+      sm.pb[i] = w;
+    }
+    for (int i = tid; i < TILE / 32; i += ETHREADS) {
+      sm.sb[i] = c.T.n_spec ? c.W.sbits[(t0 >> 5) + i] : 0u;
+      sm.gb[i] = 0;
+    }
+    if (tid < 8) sm.cls_cnt[tid] = 0;
+    if (tid == 0) {
+      sm.n_gp = 0;
+      sm.n_starts = 0;
+      sm.seg[0] = seg_lower(c, t0);
+      sm.seg[1] = (tile == ntiles - 1) ? c.S + 1 : seg_lower(c, t0 + TILE);
     }
     __syncthreads();
-    bool in_b = false;
-    for (uint32_t round = 0;; round++) {
-      const int64_t C = (n + T - 1) / T;
-      const int64_t lo = min(n, tid * C), hi = min(n, lo + C);
-      // (1) minimum rank
-      uint32_t m = RANK_MAX;
-      for (int64_t i = lo; i < hi; i++) m = min(m, A_rk[i]);
-      const uint32_t rs = block_min_u32(m, red32);
-      if (rs == RANK_MAX) break;
-      // (2) chains of rs-pairs: select every other pair from each chain's start
-      int64_t last_non = -1;
-      for (int64_t i = lo; i < hi; i++)
-        if (A_rk[i] != rs) last_non = i;
-      int64_t tot;
-      int64_t before = block_scan_i64(last_non, 1, red64, &tot);
-      int64_t ln = before;  // last non-candidate before this chunk
-      for (int64_t i = lo; i < hi; i++) {
-        if (A_rk[i] != rs) { ln = i; sel[i] = 0; }
-        else sel[i] = ((i - ln - 1) & 1) == 0;
-      }
-      __syncthreads();
-      // (3) first selected merge that creates a lower-ranked neighbour pair
-      uint32_t first_bad = 0xFFFFFFFFu;
-      for (int64_t i = lo; i < hi && first_bad == 0xFFFFFFFFu; i++) {
-        if (!sel[i]) continue;
-        bool bad = false;
-        if (i >= 1) {
-          const uint32_t left = (i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1];
-          bad = pair_rank(c.T, left, rs) < rs;
+    // 2. each thread: its pre-tokens (starts in bytes [16 tid, 16 tid + 16))
+    const int xb = tid * 16;
+    const uint32_t my = (sm.pb[xb >> 5] >> (xb & 31)) & 0xFFFFu;
+    // 2a. ends and length classes of this thread's pre-tokens
+    for (uint32_t bits = my; bits; bits &= bits - 1) {
+      const int x = xb + __ffs(bits) - 1;
+      // end: the next start bit, else the first start of a later tile, else n
+      int64_t e = -1;
+      {
+        int y = x + 1;
+        while (y < TILE + EPAD) {
+          const uint32_t w = sm.pb[y >> 5] >> (y & 31);
+          if (w) { y += __ffs(w) - 1; break; }
+          y = (y | 31) + 1;
         }
-        if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, A_ids[i + 2]) < rs;
-        if (bad) first_bad = (uint32_t)i;
+        if (y < TILE + EPAD) e = t0 + y;
+        else if (t0 + TILE + EPAD >= c.n) e = c.n;
+        else {
+          for (int64_t k = tile + 1; k < ntiles && e < 0; k++) {
+            const uint32_t f = c.W.tile_first[k];
+            if (f != NO_START) e = k * TILE + f;
+          }
+          if (e < 0) e = c.n;
+        }
       }
-      const uint32_t limit = block_min_u32(first_bad, red32);
-      // (4) apply the merges at or before limit, compact into B
-      int64_t keep = 0;
-      for (int64_t i = lo; i < hi; i++) {
-        const bool removed = i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit;
-        keep += !removed;
+      const int64_t len = e - (t0 + x);
+      sm.plen[x] = 0;
+      if ((sm.sb[x >> 5] >> (x & 31)) & 1u) {
+        sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)len);
+        sm.cnt[x] = 1;
+      } else if (len <= SHORT_MAX) {
+        sm.plen[x] = (uint8_t)len;
+        atomicAdd(&sm.cls_cnt[len_class((int)len)], 1u);
+      } else {
+        // merged earlier by k_merge_global: ids in the arena, count in cnt[]
+        const int g = atomicAdd(&sm.n_gp, 1);
+        sm.gp[g] = GPiece{(uint32_t)x, (uint32_t)len, c.W.cnt[t0 + x], 0u, 0u};
+        atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
+        sm.cnt[x] = 0;
       }
-      int64_t dst = block_scan_i64(keep, 0, red64, &tot);
-      const int64_t n2 = tot;
-      for (int64_t i = lo; i < hi; i++) {
-        const bool removed = i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit;
-        if (removed) continue;
-        const bool merged = sel[i] && (uint64_t)i <= (uint64_t)limit;
-        B_ids[dst] = merged ? rs : A_ids[i];
-        B_rk[dst] = A_rk[i];
-        chg[dst] = merged;
-        dst++;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t run = 0;
+      for (int k = 0; k < 6; k++) {
+        const uint32_t a = sm.cls_cnt[k];
+        sm.cls_cnt[k] = run;
+        run += a;
+      }
+      sm.cls_cnt[6] = run;               // list length
+      sm.cls_cnt[7] = sm.cls_cnt[5];     // first entry of the 17..64-byte class
+    }
+    __syncthreads();
+    uint32_t* list = reinterpret_cast<uint32_t*>(sm.outs);
+    for (uint32_t bits = my; bits; bits &= bits - 1) {
+      const int x = xb + __ffs(bits) - 1;
+      const int len = sm.plen[x];
+      if (len) list[atomicAdd(&sm.cls_cnt[len_class(len)], 1u)] = (uint32_t)x | ((uint32_t)len << 16);
+    }
+    __syncthreads();
+    // 2b. the list, class by class: 1..16 bytes one thread each, 17..64 bytes
+    //     one warp each (its first lane, on the warp's shared scratch)
+    {
+      const uint32_t n_list = sm.cls_cnt[6], first_mid = sm.cls_cnt[7];
+      const MergeTabs MT(c.T);
+      for (uint32_t i = tid; i < first_mid; i += ETHREADS) {
+        const uint32_t ent = list[i];
+        const int x = ent & 0xFFFF, len = ent >> 16;
+        sm.cnt[x] = (uint8_t)merge_small(MT, &sm.text[x], len, &sm.stage[x]);
+      }
+      for (uint32_t i = first_mid + warp; i < n_list; i += ETHREADS / 32) {
+        if (lane == 0) {
+          const uint32_t ent = list[i];
+          const int x = ent & 0xFFFF, len = ent >> 16;
+          sm.cnt[x] = (uint8_t)merge_scratch(MT, &sm.text[x], len, sm.scr_ids[warp], sm.scr_rk[warp],
+                                             &sm.stage[x]);
+        }
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    uint32_t my_short = 0;
+    for (uint32_t bits = my; bits; bits &= bits - 1) {
+      const int x = xb + __ffs(bits) - 1;
+      if (!((sm.gb[x >> 5] >> (x & 31)) & 1u)) my_short += sm.cnt[x];
+    }
+    atomicAdd(&sm.n_starts, (uint32_t)__popc(my));
+    __syncthreads();
+    const int ngp = sm.n_gp;
+    if (tid == 0) {
+      atomicAdd((unsigned long long*)&c.W.status->n_ptok, (unsigned long long)sm.n_starts);
+      if (ngp) atomicAdd(&c.W.status->n_long, (uint32_t)ngp);
+    }
+    // 4. per-thread totals -> block scan -> tile total -> look-back
+    uint32_t my_full = my_short;
+    for (uint32_t bits = my; bits; bits &= bits - 1) {
+      const int x = xb + __ffs(bits) - 1;
+      if ((sm.gb[x >> 5] >> (x & 31)) & 1u)
+        for (int g = 0; g < ngp; g++)
+          if ((int)sm.gp[g].rel == x) my_full += sm.gp[g].cnt;
+    }
+    {
+      uint32_t a = my_full, b = my_short;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t ya = __shfl_up_sync(0xffffffffu, a, o);
+        const uint32_t yb = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) { a += ya; b += yb; }
+      }
+      if (lane == 31) { sm.warp_tot[warp] = a; sm.warp_tot[ETHREADS / 32 + warp] = b; }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t ra = 0, rb = 0;
+        for (int w = 0; w < ETHREADS / 32; w++) {
+          const uint32_t ta = sm.warp_tot[w], tb = sm.warp_tot[ETHREADS / 32 + w];
+          sm.warp_tot[w] = ra;
+          sm.warp_tot[ETHREADS / 32 + w] = rb;
+          ra += ta;
+          rb += tb;
+        }
+        sm.tile_full = ra;
+        sm.tile_short = rb;
       }
       __syncthreads();
-      // (5) pair ranks next to merged pieces
-      const int64_t C2 = (n2 + T - 1) / T;
-      const int64_t lo2 = min(n2, tid * C2), hi2 = min(n2, lo2 + C2);
-      for (int64_t q = lo2; q < hi2; q++) {
-        if (q + 1 >= n2) B_rk[q] = RANK_MAX;
-        else if (chg[q] || chg[q + 1]) B_rk[q] = pair_rank(c.T, B_ids[q], B_ids[q + 1]);
+      sm.th_full[tid] = sm.warp_tot[warp] + a - my_full;
+      sm.th_short[tid] = sm.warp_tot[ETHREADS / 32 + warp] + b - my_short;
+    }
+    __syncthreads();
+    // 5. compaction of short ids; offsets of the global pieces
+    {
+      uint32_t f = sm.th_full[tid], s = sm.th_short[tid];
+      for (uint32_t bits = my; bits; bits &= bits - 1) {
+        const int x = xb + __ffs(bits) - 1;
+        if ((sm.gb[x >> 5] >> (x & 31)) & 1u) {
+          for (int g = 0; g < ngp; g++)
+            if ((int)sm.gp[g].rel == x) {
+              sm.gp[g].short_excl = s;
+              sm.gp[g].full_excl = f;
+              f += sm.gp[g].cnt;
+            }
+          continue;
+        }
+        const uint32_t m = sm.cnt[x];
+        for (uint32_t j = 0; j < m; j++) sm.outs[s + j] = sm.stage[x + j];
+        s += m;
+        f += m;
       }
-      __syncthreads();
-      uint32_t* t1 = A_ids; A_ids = B_ids; B_ids = t1;
-      uint32_t* t2 = A_rk; A_rk = B_rk; B_rk = t2;
-      in_b = !in_b;
-      n = n2;
-      if (round > (1u << 26)) { if (tid == 0) set_error(c.W.status, TK_E_LIMIT, 6); break; }
     }
-    if (in_b) {
-      uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + s);
-      for (int64_t i = tid; i < n; i += T) dst[i] = A_ids[i];
+    __syncthreads();
+    // 6. the tile's output to its staging slot: short ids in order, the table
+    //    of pieces merged through global memory at the slot's end; the tile's
+    //    id count; segment offsets relative to the tile
+    uint32_t* slot = c.W.staging + tile * STG;
+    for (uint32_t q = tid; q < sm.tile_short; q += ETHREADS) slot[q] = (uint32_t)sm.outs[q];
+    for (int g = tid; g < ngp; g += ETHREADS) {
+      uint32_t* e = slot + STG - 4 * (g + 1);
+      e[0] = sm.gp[g].short_excl;
+      e[1] = sm.gp[g].full_excl;
+      e[2] = sm.gp[g].rel;
+      e[3] = sm.gp[g].cnt;
     }
-    if (tid == 0) c.W.cnt[k] = (uint32_t)n;
+    if (tid == 0) {
+      c.W.tile_count[tile] = sm.tile_full;
+      c.W.tile_meta[tile] = sm.tile_short | ((uint32_t)ngp << 24);
+    }
+    for (int64_t s = sm.seg[0] + tid; s < sm.seg[1]; s += ETHREADS) {
+      const int64_t x = c.seg_off[s] - t0;
+      c.W.seg_rel[s] = (x >= TILE) ? sm.tile_full : ids_before(sm, (int)x);
+    }
     __syncthreads();
   }
 }
 
-// --------------------------------------------------------------------------
-// Scatter: ids of pre-token k go to out[offs[k] .. offs[k] + cnt[k]).
-
-__global__ void k_scatter(Call c, int32_t* out, int64_t cap) {
-  const int64_t P = c.W.status->n_ptok;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < P; k += stride) {
-    const int64_t s = c.W.ptok[k] & PTOK_MASK;
-    const int64_t o = c.W.offs[k];
-    const uint32_t m = c.W.cnt[k];
-    for (uint32_t j = 0; j < m; j++)
-      if (o + j < cap) out[o + j] = c.W.arena[s + j];
+// Ordered output: each tile's staged ids go to out[tile_base + ...], with the
+// ids of its long pieces inserted from the arena.
+__global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int64_t cap) {
+  __shared__ uint32_t s_gp[MAX_GP * 4];
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const uint64_t base = c.W.tile_base[tile];
+    const uint32_t meta = c.W.tile_meta[tile];
+    const uint32_t n_short = meta & 0xFFFFFFu;
+    const int ngp = (int)(meta >> 24);
+    const uint32_t* slot = c.W.staging + tile * STG;
+    for (int i = threadIdx.x; i < 4 * ngp; i += blockDim.x) s_gp[i] = slot[STG - 4 * ngp + i];
+    __syncthreads();
+    for (uint32_t q = threadIdx.x; q < n_short; q += blockDim.x) {
+      uint64_t pos = base + q;
+      for (int g = 0; g < ngp; g++) {
+        const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
+        if (e[0] <= q) pos += e[3];
+      }
+      if (pos < (uint64_t)cap) out[pos] = (int32_t)slot[q];
+    }
+    for (int g = 0; g < ngp; g++) {
+      const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
+      const uint64_t o = base + e[1];
+      const int32_t* src = c.W.arena + tile * TILE + e[2];
+      for (uint32_t j = threadIdx.x; j < e[3]; j += blockDim.x)
+        if (o + j < (uint64_t)cap) out[o + j] = src[j];
+    }
+    __syncthreads();
   }
 }
 
-// out_offsets[s] = index of segment s's first id; out_offsets[S] = total.
+// out_offsets[s] = the tile base of the tile that holds segment s's start plus
+// the ids before it in that tile; n_ids = total.
 __global__ void k_seg_offsets(Call c, int64_t* out_offsets) {
-  const int64_t P = c.W.status->n_ptok;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s <= c.S; s += stride) {
-    const int64_t pos = c.seg_off[s];
-    int64_t lo = 0, hi = P;
-    while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if ((int64_t)(c.W.ptok[mid] & PTOK_MASK) < pos) lo = mid + 1;
-      else hi = mid;
-    }
-    out_offsets[s] = c.W.offs[lo];
-    if (s == c.S) c.W.status->n_ids = c.W.offs[P];
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s <= c.S;
+       s += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = min(c.seg_off[s] / TILE, ntiles - 1);
+    out_offsets[s] = (int64_t)c.W.tile_base[tile] + c.W.seg_rel[s];
   }
+  if (blockIdx.x == 0 && threadIdx.x == 0) c.W.status->n_ids = c.W.tile_base[ntiles];
+}
+
+// End of the pre-token that starts at byte p: the next start bit, else the
+// first start of a later split tile, else n (reads the start bitmap).
+__device__ int64_t piece_end(const Call& c, int64_t p, int64_t ntiles) {
+  const int64_t tile = p / TILE;
+  const int64_t tend = min(c.n, (tile + 1) * TILE);
+  int64_t y = p + 1;
+  while (y < tend) {
+    const uint32_t w = c.W.pbits[y >> 5] >> (y & 31);
+    if (w) return min(c.n, y + __ffs(w) - 1);
+    y = (y | 31) + 1;
+  }
+  for (int64_t k = tile + 1; k < ntiles; k++) {
+    const uint32_t f = c.W.tile_first[k];
+    if (f != NO_START) return k * TILE + f;
+  }
+  return c.n;
+}
+
+// Pre-tokens longer than SHORT_MAX bytes -> two work lists (medium: one warp
+// each, long: one CTA each), as (start, length) pairs.
+__global__ void k_find_long(Call c) {
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  const int64_t nthreads = ntiles * (TILE / 16);
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < nthreads;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t x0 = t * 16;
+    if (x0 >= c.n) continue;
+    uint32_t bits = (c.W.pbits[x0 >> 5] >> (x0 & 31)) & 0xFFFFu;
+    if (x0 + 16 > c.n) bits &= (1u << (c.n - x0)) - 1u;
+    for (; bits; bits &= bits - 1) {
+      const int64_t p = x0 + __ffs(bits) - 1;
+      // quick reject: another start within SHORT_MAX bytes
+      const int64_t e = piece_end(c, p, ntiles);
+      if (e - p <= SHORT_MAX) continue;
+      if (c.T.n_spec && bit_get(c.W.sbits, p)) continue;  // specials are one id
+      if (e - p <= MEDIUM_MAX) {
+        const uint32_t k = atomicAdd(&c.W.status->n_medium, 1u);
+        c.W.long_list[2 * k] = (uint32_t)p;
+        c.W.long_list[2 * k + 1] = (uint32_t)(e - p);
+      } else {
+        const uint32_t k = atomicAdd(&c.W.status->n_biglong, 1u);
+        c.W.big_list[2 * k] = (uint32_t)p;
+        c.W.big_list[2 * k + 1] = (uint32_t)(e - p);
+      }
+    }
+  }
+}
+
+// Merges the listed pieces: each CTA first takes long pieces (all threads),
+// then each warp takes medium pieces.  ids -> arena[start ..], count -> cnt[start].
+__global__ void __launch_bounds__(ETHREADS) k_merge_global(Call c) {
+  __shared__ int64_t red64[ETHREADS / 32];
+  __shared__ uint32_t red32[ETHREADS / 32];
+  __shared__ uint32_t s_idx;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t n_big = c.W.status->n_biglong, n_med = c.W.status->n_medium;
+  for (;;) {
+    if (tid == 0) s_idx = atomicAdd(&c.W.status->big_next, 1u);
+    __syncthreads();
+    const uint32_t k = s_idx;
+    __syncthreads();
+    if (k >= n_big) break;
+    const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
+    const int64_t m = merge_rounds(c, BlockGroup{red64, red32}, p, len);
+    if (tid == 0) c.W.cnt[p] = (uint32_t)m;
+  }
+  for (;;) {
+    uint32_t k = 0;
+    if (lane == 0) k = atomicAdd(&c.W.status->medium_next, 1u);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    if (k >= n_med) break;
+    const int64_t p = c.W.long_list[2 * k], len = c.W.long_list[2 * k + 1];
+    const int64_t m = merge_rounds(c, WarpGroup{}, p, len);
+    if (lane == 0) c.W.cnt[p] = (uint32_t)m;
+  }
+}
+
+// Offsets of an encode with no text: every segment is empty.
+__global__ void k_empty_offsets(Call c, int64_t* out_offsets) {
+  for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s <= c.S; s += (int64_t)gridDim.x * blockDim.x)
+    out_offsets[s] = 0;
 }
 
 }  // namespace tk
@@ -1015,11 +1484,19 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.desc_c, sizeof(uint64_t) * n_scan_tiles},
       {(void**)&w.win_cut, sizeof(uint32_t) * cut_words},
       {(void**)&w.run_cut, sizeof(uint32_t) * cut_words},
-      {(void**)&w.ptok, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.pbits, sizeof(uint32_t) * cut_words},
+      {(void**)&w.sbits, sizeof(uint32_t) * cut_words},
+      {(void**)&w.tile_first, sizeof(uint32_t) * n_split_tiles},
       {(void**)&w.cnt, sizeof(uint32_t) * (nb + 2)},
       {(void**)&w.offs, sizeof(uint32_t) * (nb + 2)},
       {(void**)&w.arena, sizeof(int32_t) * (nb + 2)},
-      {(void**)&w.long_list, sizeof(uint32_t) * (nb / (SHORT_MAX + 1) + 2)},
+      {(void**)&w.long_list, sizeof(uint32_t) * 2 * (nb / (SHORT_MAX + 1) + 2)},
+      {(void**)&w.staging, sizeof(uint32_t) * (size_t)(n_split_tiles * STG)},
+      {(void**)&w.tile_count, sizeof(uint32_t) * (n_split_tiles + 1)},
+      {(void**)&w.tile_base, sizeof(uint32_t) * (n_split_tiles + 2)},
+      {(void**)&w.tile_meta, sizeof(uint32_t) * (n_split_tiles + 1)},
+      {(void**)&w.seg_rel, sizeof(uint32_t) * (max_segments + 2)},
+      {(void**)&w.big_list, sizeof(uint32_t) * 2 * (nb / (MEDIUM_MAX + 1) + 2)},
       {(void**)&w.lrk, sizeof(uint32_t) * (nb + 2)},
       {(void**)&w.lids2, sizeof(uint32_t) * (nb + 2)},
       {(void**)&w.lrk2, sizeof(uint32_t) * (nb + 2)},
@@ -1076,11 +1553,14 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   const int sms = ws->num_sms;
   const int seg_grid = (int)std::max<int64_t>(1, std::min<int64_t>((S + 256) / 256, (int64_t)sms * 4));
   tk_prof_mark(ws, "k_reset", st);
-  k_reset<<<sms * 2, 256, 0, st>>>(ws->w, n_split_tiles + 1, n_scan_tiles, c.safe, cut_words);
+  k_reset<<<sms * 2, 256, 0, st>>>(ws->w, n_split_tiles + 1, n_scan_tiles, c.safe, cut_words,
+                                   n_split_tiles);
   tk_prof_mark(ws, "k_check_segments", st);
   k_check_segments<<<seg_grid, 256, 0, st>>>(c);
   if (n > 0) {
-    const int split_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * 6);
+    int split_per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&split_per_sm, k_split, SPLIT_THREADS, 0);
+    const int split_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(split_per_sm, 1));
     if (c.safe) {
       tk_prof_mark(ws, "k_chunk_scan_windows", st);
       k_chunk_scan<<<split_grid, SPLIT_THREADS, 0, st>>>(c, 0);
@@ -1089,24 +1569,28 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     }
     tk_prof_mark(ws, "k_split", st);
     k_split<<<split_grid, SPLIT_THREADS, 0, st>>>(c);
-    const int merge_grid = (int)std::min<int64_t>((n + 127) / 128, (int64_t)sms * 16);
-    tk_prof_mark(ws, "k_merge_short", st);
-    k_merge_short<<<merge_grid, 128, 0, st>>>(c);
-    tk_prof_mark(ws, "k_merge_long", st);
-    k_merge_long<<<sms * 2, LONG_THREADS, 0, st>>>(c);
+    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(EncSmem)), "smem attribute");
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_encode_tiles, ETHREADS, sizeof(EncSmem));
+    const int enc_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(per_sm, 1));
+    tk_prof_mark(ws, "k_find_long", st);
+    k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 16) + 255) / 256, (int64_t)sms * 16), 256, 0, st>>>(c);
+    tk_prof_mark(ws, "k_merge_global", st);
+    k_merge_global<<<sms * 4, ETHREADS, 0, st>>>(c);
+    tk_prof_mark(ws, "k_encode_tiles", st);
+    k_encode_tiles<<<enc_grid, ETHREADS, sizeof(EncSmem), st>>>(c);
     tk_prof_mark(ws, "k_scan_u32", st);
-    int rc = tk_scan_u32(ws, ws->w.cnt, ws->w.offs, &ws->w.status->n_ptok, n, 3, st);
+    int rc = tk_scan_u32(ws, ws->w.tile_count, ws->w.tile_base, &ws->w.status->n_tiles, n_split_tiles, 3, st);
     if (rc) return rc;
-    tk_prof_mark(ws, "k_scatter", st);
-    k_scatter<<<merge_grid, 256, 0, st>>>(c, d_out, cap);
+    tk_prof_mark(ws, "k_copy_out", st);
+    k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * 8), ETHREADS, 0, st>>>(c, d_out, cap);
+    tk_prof_mark(ws, "k_seg_offsets", st);
+    k_seg_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets);
   } else {
-    // no text: one empty pre-token list
-    tk_prof_mark(ws, "k_scan_u32", st);
-    int rc = tk_scan_u32(ws, ws->w.cnt, ws->w.offs, &ws->w.status->n_ptok, 0, 3, st);
-    if (rc) return rc;
+    tk_prof_mark(ws, "k_empty_offsets", st);
+    k_empty_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets);
   }
-  tk_prof_mark(ws, "k_seg_offsets", st);
-  k_seg_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets);
   TK_CUDA(cudaGetLastError(), "encode launch");
   TK_CUDA(cudaMemcpyAsync(ws->h_status, ws->w.status, sizeof(Status), cudaMemcpyDeviceToHost, st),
           "status copy");

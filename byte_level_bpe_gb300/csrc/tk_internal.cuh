@@ -23,7 +23,6 @@ constexpr int TRUST = 64;
 constexpr int WIN = TILE + 2 * HALO;
 
 constexpr int SHORT_MAX = 64;   // pre-tokens up to this length merge in one thread
-constexpr int LONG_THREADS = 512;
 constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_ITEMS = 8;    // u32 counts per scan thread
 constexpr int SCAN_TILE = SCAN_THREADS * SCAN_ITEMS;
@@ -48,9 +47,13 @@ struct Status {
   int64_t err_pos;   // smallest invalid UTF-8 byte offset (INT64_MAX if none)
   int64_t n_ptok;    // pre-tokens found by the split
   int64_t n_ids;     // ids produced (may exceed the output capacity)
-  uint32_t n_long;   // pre-tokens queued for the long-piece merge
-  uint32_t long_next;
+  uint32_t n_long;   // pre-tokens merged through global memory (medium + long)
+  uint32_t n_medium;    // work list sizes and cursors of k_merge_global
+  uint32_t n_biglong;
+  uint32_t medium_next;
+  uint32_t big_next;
   uint32_t tile_ctr[8];  // dynamic tile counters of the persistent kernels
+  int64_t n_tiles;       // split tiles of this call (element count of the tile scan)
 };
 
 // Lookup tables of a tokenizer, in device memory (passed by value).
@@ -81,11 +84,19 @@ struct Work {
   uint64_t* desc_r;     // safe chunking: run scan chain
   uint32_t* win_cut;    // bitmap: 400k-character window cuts
   uint32_t* run_cut;    // bitmap: 25k-character run cuts
-  uint32_t* ptok;       // [max_bytes + 1] pre-token starts (bit 31: special)
-  uint32_t* cnt;        // [max_bytes + 1] ids per pre-token
-  uint32_t* offs;       // [max_bytes + 1] exclusive scan of cnt
-  int32_t* arena;       // [max_bytes] ids, staged at their pre-token's byte offset
-  uint32_t* long_list;  // pre-tokens for the long-piece merge
+  uint32_t* pbits;      // bitmap: pre-token starts (written by the split)
+  uint32_t* sbits;      // bitmap: special-token starts
+  uint32_t* tile_first; // per split tile: first pre-token start (tile-relative) or ~0
+  uint32_t* cnt;        // [max_bytes + 1] decode: bytes per id
+  uint32_t* offs;       // [max_bytes + 1] decode: exclusive scan of cnt
+  int32_t* arena;       // [max_bytes] ids of pieces merged through global memory, at their byte offset
+  uint32_t* long_list;  // (start, length) of pre-tokens of SHORT_MAX+1 .. MEDIUM_MAX bytes
+  uint32_t* big_list;   // (start, length) of pre-tokens longer than MEDIUM_MAX bytes
+  uint32_t* staging;    // per split tile: compacted short ids, long-piece table at the end
+  uint32_t* tile_count; // per split tile: ids (then: exclusive scan -> tile_base)
+  uint32_t* tile_base;  // [n_tiles + 1]
+  uint32_t* tile_meta;  // per split tile: short ids (low 24 bits) | long pieces << 24
+  uint32_t* seg_rel;    // [max_segments + 1] ids before each segment start, within its tile
   uint32_t* lrk;        // [max_bytes] long merge: pair ranks
   uint32_t* lids2;      // [max_bytes] long merge: second id buffer
   uint32_t* lrk2;       // [max_bytes] long merge: second rank buffer
@@ -109,9 +120,116 @@ __device__ __forceinline__ void set_error(Status* st, int code, int kind) {
   if (atomicCAS(&st->code, 0, code) == 0) st->err_kind = kind;
 }
 
+struct SumOp {
+  __device__ static uint64_t id() { return 0; }
+  __device__ static uint64_t comb(uint64_t l, uint64_t r) { return l + r; }
+};
+// Decoupled look-back, run by all 32 lanes of one warp: publishes the tile's
+// aggregate, inspects 32 predecessors per step (ballots for their states, an
+// ordered shuffle reduction for their values) until it meets an inclusive
+// prefix, publishes its own inclusive prefix and returns the exclusive one on
+// every lane.  Waits are bounded (TK_E_TIMEOUT).
+template <class Op>
+__device__ uint64_t chain_exclusive_warp(uint64_t* desc, int64_t tile, uint64_t agg, Status* st,
+                                         int kind) {
+  const int lane = threadIdx.x & 31;
+  if (tile == 0) {
+    if (lane == 0) st_release_u64(&desc[0], DESC_PREFIX | agg);
+    return Op::id();
+  }
+  if (lane == 0) st_release_u64(&desc[tile], DESC_AGG | agg);
+  uint64_t acc = Op::id();
+  int64_t j = tile - 1;
+  uint32_t spins = 0;
+  for (;;) {
+    const int64_t idx = j - lane;  // lane 0 = nearest predecessor
+    const uint64_t d = (idx >= 0) ? ld_acquire_u64(&desc[idx]) : (DESC_PREFIX | Op::id());
+    const uint64_t state = d & ~DESC_VAL;
+    const uint32_t pmask = __ballot_sync(0xffffffffu, state == DESC_PREFIX);
+    const uint32_t rmask = __ballot_sync(0xffffffffu, state != 0);
+    const int fp = pmask ? __ffs(pmask) - 1 : 31;
+    const uint32_t need = (fp == 31) ? 0xffffffffu : ((2u << fp) - 1u);
+    if ((rmask & need) != need) {
+      if (++spins > SPIN_LIMIT) {
+        if (lane == 0) set_error(st, TK_E_TIMEOUT, kind);
+        break;
+      }
+      __nanosleep(32);
+      continue;
+    }
+    // combine lanes fp..0 in tile order (a higher lane is an earlier tile)
+    uint64_t x = (lane <= fp) ? (d & DESC_VAL) : Op::id();
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_down_sync(0xffffffffu, x, o);
+      if (lane + o < 32) x = Op::comb(y, x);
+    }
+    acc = Op::comb(__shfl_sync(0xffffffffu, x, 0), acc);
+    if (pmask) break;
+    j -= 32;
+  }
+  if (lane == 0) st_release_u64(&desc[tile], DESC_PREFIX | Op::comb(acc, agg));
+  return acc;
+}
+
+// The tables the merge loop reads, passed by value into the hot loops.
+struct MergeTabs {
+  const uint32_t* byte_id;
+  const uint32_t* dense;
+  const uint64_t* pair_slots;
+  uint32_t pair_log2;
+  uint32_t pair_max_probe;
+  __device__ __host__ explicit MergeTabs(const Tables& T)
+      : byte_id(T.byte_id), dense(T.dense), pair_slots(T.pair_slots), pair_log2(T.pair_log2),
+        pair_max_probe(T.pair_max_probe) {}
+};
+
+// Carry of an operator whose aggregate can "reset" (the number-run and the
+// segmented code-point counts): publishes the tile's aggregate and combines
+// the predecessors' aggregates backwards only until one that resets (the
+// carry cannot depend on anything before it).  No inclusive prefixes are
+// published or awaited, so a tile waits only for the few predecessors its
+// carry really depends on, each of which publishes early.  Run by one warp;
+// `resets(v)` tells whether aggregate v resets.  Bounded waits.
+template <class Op>
+__device__ uint64_t carry_walk_warp(uint64_t* desc, int64_t tile, uint64_t agg, Status* st, int kind) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) st_release_u64(&desc[tile], DESC_AGG | agg);
+  uint64_t acc = Op::id();
+  int64_t j = tile - 1;
+  uint32_t spins = 0;
+  while (j >= 0) {
+    const int64_t idx = j - lane;
+    const uint64_t d = (idx >= 0) ? ld_acquire_u64(&desc[idx]) : (DESC_AGG | Op::reset_id());
+    const bool ready = (d & ~DESC_VAL) != 0;
+    const uint64_t v = d & DESC_VAL;
+    const uint32_t rst = __ballot_sync(0xffffffffu, ready && Op::resets(v));
+    const uint32_t rdy = __ballot_sync(0xffffffffu, ready);
+    const int fr = rst ? __ffs(rst) - 1 : 31;
+    const uint32_t need = (fr == 31) ? 0xffffffffu : ((2u << fr) - 1u);
+    if ((rdy & need) != need) {
+      if (++spins > SPIN_LIMIT) {
+        if (lane == 0) set_error(st, TK_E_TIMEOUT, kind);
+        break;
+      }
+      __nanosleep(32);
+      continue;
+    }
+    uint64_t x = (lane <= fr) ? v : Op::id();
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_down_sync(0xffffffffu, x, o);
+      if (lane + o < 32) x = Op::comb(y, x);
+    }
+    acc = Op::comb(__shfl_sync(0xffffffffu, x, 0), acc);
+    if (rst) break;
+    j -= 32;
+  }
+  return acc;
+}
+
 // Open-addressing lookup of the rank of the token whose bytes are
 // bytes(a) || bytes(b), or RANK_MAX.
-__device__ __forceinline__ uint32_t pair_rank(const Tables& T, uint32_t a, uint32_t b) {
+template <class TT>
+__device__ __forceinline__ uint32_t pair_rank(const TT& T, uint32_t a, uint32_t b) {
   const uint64_t key = ((uint64_t)a << 20) | b;
   uint64_t h = (key * 0x9E3779B97F4A7C15ull) >> (64 - T.pair_log2);
   const uint64_t mask = (1ull << T.pair_log2) - 1;

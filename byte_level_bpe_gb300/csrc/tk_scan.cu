@@ -60,32 +60,9 @@ k_scan_u32(const uint32_t* __restrict__ in, uint32_t* __restrict__ out, const in
     __syncthreads();
     const uint32_t tile_total = s_warp[SCAN_THREADS / 32 - 1];
     const uint32_t excl = (warp ? s_warp[warp - 1] : 0u) + x - sum;
-    if (tid == 0) {
-      uint64_t prefix = 0;
-      if (tile == 0) {
-        st_release_u64(&desc[0], DESC_PREFIX | tile_total);
-      } else {
-        st_release_u64(&desc[tile], DESC_AGG | tile_total);
-        int64_t j = tile - 1;
-        uint32_t spins = 0;
-        while (j >= 0) {
-          const uint64_t d = ld_acquire_u64(&desc[j]);
-          const uint64_t state = d & ~DESC_VAL;
-          if (state == 0) {
-            if (++spins > SPIN_LIMIT) {
-              set_error(st, TK_E_TIMEOUT, 10 + ctr);
-              break;
-            }
-            __nanosleep(64);
-            continue;
-          }
-          prefix += d & DESC_VAL;
-          if (state == DESC_PREFIX) break;
-          j--;
-        }
-        st_release_u64(&desc[tile], DESC_PREFIX | (prefix + tile_total));
-      }
-      s_prefix = prefix;
+    if (warp == 0) {
+      const uint64_t prefix = chain_exclusive_warp<SumOp>(desc, tile, tile_total, st, 10 + ctr);
+      if (lane == 0) s_prefix = prefix;
     }
     __syncthreads();
     uint32_t run = (uint32_t)s_prefix + excl;

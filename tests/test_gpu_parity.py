@@ -20,10 +20,21 @@ def _gpu_ids(tk, segments, safe):
     return ids.cpu().numpy(), off.cpu().numpy()
 
 
+def _first_bad_segment(segments, g_ids, g_off, o_ids, o_off):
+    for k, (s, allow) in enumerate(segments):
+        a = g_ids[g_off[k]:g_off[k + 1]]
+        b = o_ids[o_off[k]:o_off[k + 1]]
+        if len(a) != len(b) or not np.array_equal(a, b):
+            return f"segment {k} {s!r} allow={allow}: gpu {a.tolist()} oracle {b.tolist()}"
+    return "no differing segment"
+
+
 def _compare(tk, enc, segments, safe):
     g_ids, g_off = _gpu_ids(tk, segments, safe)
     o_ids, o_off = enc.encode_segments(segments, tiktoken_safe=safe)
-    assert len(g_ids) == len(o_ids), (len(g_ids), len(o_ids))
+    if len(g_ids) != len(o_ids) or not np.array_equal(g_off, o_off):
+        raise AssertionError(f"{len(g_ids)} vs {len(o_ids)} ids; " +
+                             _first_bad_segment(segments, g_ids, g_off, o_ids, o_off)[:3000])
     if not np.array_equal(g_ids, o_ids):
         k = int(np.argmax(g_ids != o_ids))
         raise AssertionError(f"first mismatch at id {k}: gpu {g_ids[k-3:k+4]} oracle {o_ids[k-3:k+4]}")
