@@ -26,6 +26,7 @@
 //  * assembly: ids are staged at their pre-token's byte offset, the per
 //    pre-token counts are scanned, and a scatter writes the ids in order.
 #include <stdarg.h>
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -263,6 +264,19 @@ __global__ void k_check_segments(Call c) {
   }
 }
 
+// Per split tile, the first segment index at or after t0 - HALO, t0,
+// t0 + TILE and t0 + TILE + HALO (four binary searches per tile, in parallel,
+// so that no tile kernel searches on its critical path).
+__global__ void k_tile_segs(Call c) {
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < 4 * ntiles;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = i >> 2, k = i & 3;
+    const int64_t pos = tile * TILE + (k == 0 ? -HALO : k == 1 ? 0 : k == 2 ? TILE : TILE + HALO);
+    c.W.tile_segs[i] = (uint32_t)seg_lower(c, pos);
+  }
+}
+
 // --------------------------------------------------------------------------
 // Safe chunking: a segmented count of code points over the text.
 //   mode 0 (windows): heads are segment starts; a cut goes before every code
@@ -292,8 +306,8 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) 
     // bytes [t0 - 4, t0 + TILE + 4)
     for (int x = tid; x < TILE + 8; x += SPLIT_THREADS) s_text[x] = gbyte(c, t0 - 4 + x);
     if (tid == 0) {
-      s_seg[0] = seg_lower(c, t0);
-      s_seg[1] = seg_lower(c, t0 + TILE);
+      s_seg[0] = c.W.tile_segs[4 * tile + 1];
+      s_seg[1] = c.W.tile_segs[4 * tile + 2];
     }
     __syncthreads();
     const int64_t slo = s_seg[0], shi = s_seg[1];
@@ -340,6 +354,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) 
         }
       }
       run = __shfl_sync(0xffffffffu, run, 0);
+      if (tid == 0) st_release_u64(&desc[tile], DESC_AGG | run);
       const uint64_t carry = carry_walk_warp<SegCountOp>(desc, tile, run, c.W.status, 2 + mode);
       if (tid == 0) s_carry = carry;
     }
@@ -376,6 +391,7 @@ struct SplitSmem {
   uint64_t ncarry;
   uint32_t first;  // first pre-token start of the tile (tile-relative), or all ones
 };
+static_assert(offsetof(SplitSmem, kc) % 4 == 0, "class bytes are read as words");
 
 // Special match of the longest special at window position x (all bytes must be
 // in the window); returns its length or 0.
@@ -509,14 +525,61 @@ __device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) 
   }
 }
 
+// Eight bit-planes of four class bytes: bit j of the result is bit i of byte j.
+__device__ __forceinline__ uint32_t gather_plane(uint32_t w, int i) {
+  return (((w >> i) & 0x01010101u) * 0x10204080u) >> 28;
+}
+
+// The start test for 16 ASCII code points at once (window bytes x0 .. x0+15,
+// no piece start or special byte within 4 before and 4 after).  Bit k of each
+// mask is window byte x0 - 4 + k; the rules are those of starts_here, with the
+// number groups found by propagating run starts in steps of 3.  r is the
+// index in its number run of the code point at x0.  Returns the start bits of
+// the 16 bytes; *slow receives the bytes whose test needs the white-space
+// walks (CR/LF followed by other white space).
+__device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t r, uint32_t* slow) {
+  const uint32_t p0 = P[0], p1 = P[1], p2 = P[2];
+  const uint32_t L = ~p0 & ~p1 & ~p2, N = p0 & ~p1 & ~p2, O = ~p0 & p1 & ~p2, NL = p0 & p1 & ~p2;
+  const uint32_t SP = ~p0 & ~p1 & p2, WSO = p0 & ~p1 & p2;
+  const uint32_t APOS = P[3], C1 = P[4], LLf = P[5], VR = P[6], E = P[7];
+  const uint32_t SPW = SP | WSO, WS = NL | SPW, OS = O | SP;
+  // numbers: group starts at run start + 3k
+  const uint32_t N1 = N << 1, N2 = N << 2;
+  uint32_t G = N & ~N1 & ~1u;
+  if ((N >> 4) & (N >> 3) & 1u) {  // the run at x0 began earlier: its index there is r
+    const int first = 4 + (int)((3u - r) % 3u);
+    const uint32_t span = ((2u << first) - 1u) & ~0xFu;  // bits 4..first
+    if ((N & span) == span) G |= 1u << first;
+  }
+#pragma unroll
+  for (int it = 0; it < 7; it++) G |= (G << 3) & N & N1 & N2;
+  const uint32_t S_N = G & N;
+  const uint32_t S_L =
+      L & ((N << 1) | (NL << 1) | ((O << 1) & (OS << 2)) |
+           ((L << 1) & (C1 << 1) & (APOS << 2) & ~(OS << 3)) |
+           ((L << 1) & (APOS << 3) & (((LLf << 2) & (LLf << 1)) | ((VR << 2) & (E << 1))) & ~(OS << 4)));
+  const uint32_t S_O = O & ((L | N | NL | WSO) << 1);
+  const uint32_t S_NL = NL & ((L | N) << 1);
+  const uint32_t S_W = SPW & (((L | N | O) << 1) | ((SPW << 1) & ~(WS >> 1)));
+  const uint32_t sl = SPW & (NL << 1);
+  *slow = (sl >> 4) & 0xFFFFu;
+  return ((S_N | S_L | S_O | S_NL | S_W) & ~sl) >> 4 & 0xFFFFu;
+}
+
 __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
   __shared__ SplitSmem sm;
+  __shared__ uint8_t s_asc[128];
+  __shared__ int s_any_allow;
   const int tid = threadIdx.x;
   if (tid == 0) sm.first = 0xFFFFFFFFu;
+  if (tid < 128) s_asc[tid] = kclass((uint32_t)tid);
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const bool aligned = ((uintptr_t)c.text & 15) == 0;
   for (;;) {
-    if (tid == 0) sm.tile = atomicAdd(&c.W.status->tile_ctr[0], 1u);
+    if (tid == 0) {
+      sm.tile = atomicAdd(&c.W.status->tile_ctr[0], 1u);
+      s_any_allow = 0;
+    }
     __syncthreads();
     const int64_t tile = sm.tile;
     if (tile >= ntiles) break;
@@ -540,19 +603,19 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
       sm.pst[i] = v;
     }
     for (int i = tid; i < TILE / 32; i += SPLIT_THREADS) sm.outb[i] = 0;
-    if (tid == 0) {
-      sm.seg[0] = seg_lower(c, wlo);
-      sm.seg[1] = seg_lower(c, wlo + WIN);
-    }
+    const int64_t seg_lo = c.W.tile_segs[4 * tile], seg_hi = c.W.tile_segs[4 * tile + 3];
     __syncthreads();
-    // 2. segment starts (and the text end) are piece starts
-    for (int64_t s = sm.seg[0] + tid; s < sm.seg[1]; s += SPLIT_THREADS) {
+    // 2. segment starts (and the text end) are piece starts; note whether any
+    //    segment overlapping the window allows specials
+    for (int64_t s = seg_lo + tid; s < seg_hi; s += SPLIT_THREADS) {
       const int64_t x = c.seg_off[s] - wlo;
       if (x >= 0 && x < WIN) atomicOr(&sm.pst[x >> 5], 1u << (x & 31));
+      if (s < c.S && c.allow[s]) s_any_allow = 1;
     }
+    if (tid == 0 && seg_lo > 0 && c.allow[seg_lo - 1]) s_any_allow = 1;
     __syncthreads();
     // 3. specials in allow_special segments: find, then mark
-    if (c.T.n_spec > 0) {
+    if (c.T.n_spec > 0 && s_any_allow) {
       for (int x = tid; x < WIN; x += SPLIT_THREADS) {
         const int64_t pos = wlo + x;
         if (pos < 0 || pos >= c.n) continue;
@@ -574,6 +637,8 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
       uint8_t k;
       if (pos < 0 || pos >= c.n) {
         k = K_OUT;
+      } else if (b < 0x80) {
+        k = s_asc[b];
       } else if ((b & 0xC0) == 0x80) {
         k = K_CONT;
         if (x >= HALO && x < HALO + TILE) {
@@ -592,18 +657,15 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
         uint32_t cp;
         bool ok;
         utf8_seq(b, sm.text[x + 1], sm.text[x + 2], sm.text[x + 3], cp, ok);
-        if (!ok || pos + 1 > c.n) {
-          if (x >= HALO && x < HALO + TILE) {
-            set_error(c.W.status, TK_E_UTF8, 0);
-            atomicMin((long long*)&c.W.status->err_pos, (long long)pos);
-          }
+        if (!ok && x >= HALO && x < HALO + TILE) {
+          set_error(c.W.status, TK_E_UTF8, 0);
+          atomicMin((long long*)&c.W.status->err_pos, (long long)pos);
         }
         k = kclass(cp);
       }
       sm.kc[x] = k;
     }
     __syncthreads();
-    // a multi-byte sequence cut by the text end is invalid too
     // 5. number-run aggregate of this thread's 16 bytes
     const int xb = HALO + tid * 16;
     uint32_t nreset = 0, ncount = 0;
@@ -619,7 +681,6 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
     {
       // exclusive block scan of the number-run aggregates (warp shuffles)
       uint32_t x = (nreset ? 0u : 4u) | ncount;
-      const uint32_t v = x;
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if ((tid & 31) >= o) x = (uint32_t)NRunOp::comb(y, x);
@@ -628,51 +689,95 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
       __syncthreads();
       if (tid < 32) {
         uint64_t run = NRunOp::id();
+        int resolved = 0;
+        uint32_t cnt = 0;
         if (tid == 0) {
           for (int w = 0; w < SPLIT_THREADS / 32; w++) {
             const uint64_t a = sm.scan[w];
             sm.scan[w] = (uint32_t)run;
             run = NRunOp::comb(run, a);
           }
+          st_release_u64(&c.W.desc_a[tile], DESC_AGG | run);
+          // the number run that ends before t0, counted in the window if it
+          // starts there (it almost always does)
+          int p = HALO - 1;
+          while (p > HALO - 5 && (sm.kc[p] & 7) == K_CONT) p--;
+          for (;;) {
+            if (p < TRUST) break;
+            if ((sm.kc[p] & 7) != K_N || bit_get(sm.insp, p)) { resolved = 1; break; }
+            cnt++;
+            if (bit_get(sm.pst, p)) { resolved = 1; break; }
+            const int q = p;
+            p--;
+            while (p > q - 5 && (sm.kc[p] & 7) == K_CONT) p--;
+          }
         }
-        run = __shfl_sync(0xffffffffu, run, 0);
-        const uint64_t carry = carry_walk_warp<NRunOp>(c.W.desc_a, tile, run, c.W.status, 4);
+        resolved = __shfl_sync(0xffffffffu, resolved, 0);
+        uint64_t carry;
+        if (resolved) carry = cnt % 3;
+        else carry = carry_walk_warp<NRunOp>(c.W.desc_a, tile, 0, c.W.status, 4);
         if (tid == 0) sm.ncarry = carry;
       }
       __syncthreads();
       uint32_t e = __shfl_up_sync(0xffffffffu, x, 1);
       if ((tid & 31) == 0) e = (uint32_t)NRunOp::id();
-      (void)v;
       sm.nagg[tid] = (uint32_t)NRunOp::comb(sm.scan[tid >> 5], e);
     }
     __syncthreads();
-    // 6. the start test for each code point of this thread
+    // 6. the start test: 16 ASCII bytes at once where possible, else per code point
     {
       const Win w{c, sm, wlo};
       const uint64_t pre = NRunOp::comb(sm.ncarry, sm.nagg[tid]);
       uint32_t r = (uint32_t)(pre & 3);
       uint32_t bits = 0;
-      for (int j = 0; j < 16; j++) {
-        const int x = xb + j;
-        const uint8_t k = sm.kc[x];
-        const uint8_t k7 = k & 7;
-        if (k7 == K_CONT) continue;
-        if (k7 == K_OUT) break;
-        const int64_t pos = wlo + x;
-        uint32_t nidx = 0;
-        const bool in_sp = bit_get(sm.insp, x);
-        if (k7 == K_N && !in_sp) {
-          if (bit_get(sm.pst, x)) r = 0;
-          nidx = r;
-          r = (r + 1) % 3;
-        } else {
-          r = 0;
+      bool fast = wlo + xb + 20 <= c.n;
+      uint32_t P[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (fast) {
+        const int b0 = xb - 4;
+        const uint64_t both = ((uint64_t)(sm.pst[(b0 >> 5) + 1] | sm.insp[(b0 >> 5) + 1]) << 32) |
+                              (sm.pst[b0 >> 5] | sm.insp[b0 >> 5]);
+        fast = ((both >> (b0 & 31)) & 0xFFFFFFu) == 0;
+      }
+      if (fast) {
+        const uint32_t* kw = reinterpret_cast<const uint32_t*>(&sm.kc[xb - 4]);
+#pragma unroll
+        for (int j = 0; j < 6; j++) {
+          const uint32_t wv = kw[j];
+#pragma unroll
+          for (int i = 0; i < 8; i++) P[i] |= gather_plane(wv, i) << (4 * j);
         }
-        bool s;
-        if (in_sp) s = bit_get(sm.sst, x);
-        else if (bit_get(sm.pst, x)) s = true;
-        else s = starts_here(w, pos, k, nidx);
-        if (s) bits |= 1u << j;
+        fast = (P[1] & P[2] & 0xFFFFFFu) == 0;  // no continuation bytes or text end
+      }
+      if (fast) {
+        uint32_t slow;
+        bits = starts_ascii16(P, r, &slow);
+        for (; slow; slow &= slow - 1) {
+          const int j = __ffs(slow) - 1;
+          if (starts_here(w, wlo + xb + j, sm.kc[xb + j], 0)) bits |= 1u << j;
+        }
+      } else {
+        for (int j = 0; j < 16; j++) {
+          const int x = xb + j;
+          const uint8_t k = sm.kc[x];
+          const uint8_t k7 = k & 7;
+          if (k7 == K_CONT) continue;
+          if (k7 == K_OUT) break;
+          const int64_t pos = wlo + x;
+          uint32_t nidx = 0;
+          const bool in_sp = bit_get(sm.insp, x);
+          if (k7 == K_N && !in_sp) {
+            if (bit_get(sm.pst, x)) r = 0;
+            nidx = r;
+            r = (r + 1) % 3;
+          } else {
+            r = 0;
+          }
+          bool s;
+          if (in_sp) s = bit_get(sm.sst, x);
+          else if (bit_get(sm.pst, x)) s = true;
+          else s = starts_here(w, pos, k, nidx);
+          if (s) bits |= 1u << j;
+        }
       }
       // 16 bits per thread: two threads share one 32-bit word
       atomicOr(&sm.outb[tid >> 1], bits << (16 * (tid & 1)));
@@ -1129,8 +1234,8 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     if (tid == 0) {
       sm.n_gp = 0;
       sm.n_starts = 0;
-      sm.seg[0] = seg_lower(c, t0);
-      sm.seg[1] = (tile == ntiles - 1) ? c.S + 1 : seg_lower(c, t0 + TILE);
+      sm.seg[0] = c.W.tile_segs[4 * tile + 1];
+      sm.seg[1] = (tile == ntiles - 1) ? c.S + 1 : c.W.tile_segs[4 * tile + 2];
     }
     __syncthreads();
     // 2. each thread: its pre-tokens (starts in bytes [16 tid, 16 tid + 16))
@@ -1496,6 +1601,7 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.tile_base, sizeof(uint32_t) * (n_split_tiles + 2)},
       {(void**)&w.tile_meta, sizeof(uint32_t) * (n_split_tiles + 1)},
       {(void**)&w.seg_rel, sizeof(uint32_t) * (max_segments + 2)},
+      {(void**)&w.tile_segs, sizeof(uint32_t) * 4 * (n_split_tiles + 1)},
       {(void**)&w.big_list, sizeof(uint32_t) * 2 * (nb / (MEDIUM_MAX + 1) + 2)},
       {(void**)&w.lrk, sizeof(uint32_t) * (nb + 2)},
       {(void**)&w.lids2, sizeof(uint32_t) * (nb + 2)},
@@ -1561,6 +1667,8 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     int split_per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&split_per_sm, k_split, SPLIT_THREADS, 0);
     const int split_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(split_per_sm, 1));
+    tk_prof_mark(ws, "k_tile_segs", st);
+    k_tile_segs<<<(int)std::min<int64_t>((4 * n_split_tiles + 255) / 256, (int64_t)sms * 8), 256, 0, st>>>(c);
     if (c.safe) {
       tk_prof_mark(ws, "k_chunk_scan_windows", st);
       k_chunk_scan<<<split_grid, SPLIT_THREADS, 0, st>>>(c, 0);

@@ -97,6 +97,8 @@ struct Work {
   uint32_t* tile_base;  // [n_tiles + 1]
   uint32_t* tile_meta;  // per split tile: short ids (low 24 bits) | long pieces << 24
   uint32_t* seg_rel;    // [max_segments + 1] ids before each segment start, within its tile
+  uint32_t* tile_segs;  // per split tile: first segment index at or after t0 - HALO, t0,
+                        // t0 + TILE, t0 + TILE + HALO
   uint32_t* lrk;        // [max_bytes] long merge: pair ranks
   uint32_t* lids2;      // [max_bytes] long merge: second id buffer
   uint32_t* lrk2;       // [max_bytes] long merge: second rank buffer
@@ -184,7 +186,8 @@ struct MergeTabs {
 };
 
 // Carry of an operator whose aggregate can "reset" (the number-run and the
-// segmented code-point counts): publishes the tile's aggregate and combines
+// segmented code-point counts): every tile publishes its aggregate first
+// (st_release of DESC_AGG | agg); this walk then combines
 // the predecessors' aggregates backwards only until one that resets (the
 // carry cannot depend on anything before it).  No inclusive prefixes are
 // published or awaited, so a tile waits only for the few predecessors its
@@ -193,7 +196,7 @@ struct MergeTabs {
 template <class Op>
 __device__ uint64_t carry_walk_warp(uint64_t* desc, int64_t tile, uint64_t agg, Status* st, int kind) {
   const int lane = threadIdx.x & 31;
-  if (lane == 0) st_release_u64(&desc[tile], DESC_AGG | agg);
+  (void)agg;
   uint64_t acc = Op::id();
   int64_t j = tile - 1;
   uint32_t spins = 0;
