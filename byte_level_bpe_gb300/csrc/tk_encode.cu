@@ -251,6 +251,7 @@ __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int s
   for (int64_t i = tid; i < n_desc_scan; i += stride) W.desc_c[i] = 0;
   if (safe)
     for (int64_t i = tid; i < n_cut_words; i += stride) { W.win_cut[i] = 0; W.run_cut[i] = 0; }
+  for (int64_t i = tid; i < (2ll << W.dtab_log2); i += stride) W.dtab[i] = 0ull;
 }
 
 // Segment table check: seg_off[0] = 0, non-decreasing, seg_off[S] = n.
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
     for (int v = tid; v < (WIN + 16) / 16; v += SPLIT_THREADS) {
       const int64_t p = wlo + 16 * v;
       if (aligned && p >= 0 && p + 16 <= c.n) {
-        *reinterpret_cast<uint4*>(&sm.text[16 * v]) = __ldg(reinterpret_cast<const uint4*>(c.text + p));
+        *reinterpret_cast<uint4*>(&sm.text[16 * v]) = ld_na_v4(c.text + p);
       } else {
         for (int j = 0; j < 16; j++) sm.text[16 * v + j] = gbyte(c, p + j);
       }
@@ -852,7 +853,7 @@ __device__ __forceinline__ int merge_reg(const MergeTabs T, const uint8_t* b, in
 #pragma unroll
   for (int i = 0; i < W - 1; i++) {
     uint32_t v = RANK_MAX;
-    if (i + 1 < n) v = __ldg(&T.dense[((uint32_t)b[i] << 8) | b[i + 1]]);
+    if (i + 1 < n) v = dense_rank(T, b[i], b[i + 1]);
     rk[i] = v;
   }
   rk[W - 1] = RANK_MAX;
@@ -897,6 +898,29 @@ __device__ __forceinline__ int merge_reg(const MergeTabs T, const uint8_t* b, in
   return m;
 }
 
+// Three bytes: the parts loop written out.  First round: ranks r01, r12 of the
+// two byte pairs; the leftmost minimum merges; then the one remaining pair.
+struct Ids3 {
+  uint32_t n, a, b, c;
+};
+__device__ __forceinline__ Ids3 merge3(const MergeTabs T, const uint8_t* b) {
+  const uint32_t b0 = b[0], b1 = b[1], b2 = b[2];
+  const uint32_t r01 = dense_rank(T, b0, b1), r12 = dense_rank(T, b1, b2);
+  const uint32_t i0 = __ldg(&T.byte_id[b0]), i1 = __ldg(&T.byte_id[b1]), i2 = __ldg(&T.byte_id[b2]);
+  if (r01 == RANK_MAX && r12 == RANK_MAX) return Ids3{3u, i0, i1, i2};
+  const bool left = r01 <= r12;
+  const uint32_t a = left ? r01 : i0, c = left ? i2 : r12;
+  const uint32_t r = pair_rank(T, a, c);
+  if (r != RANK_MAX) return Ids3{1u, r, 0u, 0u};
+  return Ids3{2u, a, c, 0u};
+}
+
+__device__ __forceinline__ void put3(int32_t* out, const Ids3& m) {
+  out[0] = (int32_t)m.a;
+  if (m.n > 1) out[1] = (int32_t)m.b;
+  if (m.n > 2) out[2] = (int32_t)m.c;
+}
+
 // One pre-token of 1..16 bytes: closed forms for one and two bytes (the
 // loop's result written out), else the register loop of the smallest width.
 __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, int n, int32_t* out) {
@@ -907,7 +931,7 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
   }
   if (n == 2) {
     const uint32_t b1 = b[1];
-    const uint32_t r = __ldg(&T.dense[(b0 << 8) | b1]);
+    const uint32_t r = dense_rank(T, b0, b1);
     if (r != RANK_MAX) {
       out[0] = (int32_t)r;
       return 1;
@@ -916,6 +940,11 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
     out[1] = (int32_t)__ldg(&T.byte_id[b1]);
     return 2;
   }
+  if (n == 3) {
+    const Ids3 m = merge3(T, b);
+    put3(out, m);
+    return (int)m.n;
+  }
   if (n <= 4) return merge_reg<4>(T, b, n, out);
   if (n <= 8) return merge_reg<8>(T, b, n, out);
   return merge_reg<16>(T, b, n, out);
@@ -923,8 +952,9 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
 
 // Length class of a pre-token for the tile's work list (warps then run
 // pieces of one class together).
+constexpr int N_CLASSES = 7;  // 1, 2, 3, 4, 5-8, 9-16, 17-64 bytes
 __device__ __forceinline__ int len_class(int n) {
-  return n == 1 ? 0 : n == 2 ? 1 : n <= 4 ? 2 : n <= 8 ? 3 : n <= 16 ? 4 : 5;
+  return n <= 4 ? n - 1 : n <= 8 ? 4 : n <= 16 ? 5 : 6;
 }
 
 // The loop for one pre-token of up to SHORT_MAX bytes on caller-provided
@@ -936,7 +966,7 @@ __device__ __noinline__ int merge_scratch(const MergeTabs T, const uint8_t* b, i
   for (int i = 1; i < n; i++) {
     const uint32_t x = b[i];
     ids[i] = __ldg(&T.byte_id[x]);
-    rk[i - 1] = __ldg(&T.dense[(prevb << 8) | x]);
+    rk[i - 1] = dense_rank(T, prevb, x);
     prevb = x;
   }
   rk[n - 1] = RANK_MAX;
@@ -957,6 +987,33 @@ __device__ __noinline__ int merge_scratch(const MergeTabs T, const uint8_t* b, i
   }
   for (int i = 0; i < m; i++) out[i] = (int32_t)ids[i];
   return m;
+}
+
+// Four pair lookups at once: the first probe of each is issued before any is
+// examined (independent loads in flight), the rare longer probes after.
+__device__ __forceinline__ void pair_rank4(const Tables& T, const uint32_t a[4], const uint32_t b[4],
+                                           uint32_t r[4]) {
+  const uint64_t mask = (1ull << T.pair_log2) - 1;
+  uint64_t key[4], h[4], sl[4];
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    key[k] = ((uint64_t)a[k] << 20) | b[k];
+    h[k] = (key[k] * 0x9E3779B97F4A7C15ull) >> (64 - T.pair_log2);
+    sl[k] = __ldg(&T.pair_slots[h[k]]);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    if (sl[k] == ~0ull) { r[k] = RANK_MAX; continue; }
+    if ((sl[k] >> 20) == key[k]) { r[k] = (uint32_t)(sl[k] & 0xFFFFF); continue; }
+    r[k] = RANK_MAX;
+    uint64_t hh = (h[k] + 1) & mask;
+    for (uint32_t probe = 1; probe <= T.pair_max_probe; probe++) {
+      const uint64_t v = __ldg(&T.pair_slots[hh]);
+      if (v == ~0ull) break;
+      if ((v >> 20) == key[k]) { r[k] = (uint32_t)(v & 0xFFFFF); break; }
+      hh = (hh + 1) & mask;
+    }
+  }
 }
 
 // Cooperative groups for the round merge: a warp (no block barriers) or the
@@ -1075,16 +1132,28 @@ __device__ int64_t merge_rounds(const Call& c, const G& g, int64_t s, int64_t n)
     }
     g.sync();
     // (3) the first selected merge that creates a neighbour pair of lower rank
+    //     (its left and right pairs looked up four selected merges at a time)
     uint32_t first_bad = 0xFFFFFFFFu;
-    for (int64_t i = lo; i < hi && first_bad == 0xFFFFFFFFu; i++) {
-      if (!sel[i]) continue;
-      bool bad = false;
-      if (i >= 1) {
-        const uint32_t left = (i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1];
-        bad = pair_rank(c.T, left, rs) < rs;
+    for (int64_t i = lo; i < hi && first_bad == 0xFFFFFFFFu;) {
+      int64_t at[4];
+      uint32_t la[4], lb[4], ra[4], rb[4], lr[4], rr[4];
+      int k = 0;
+      for (; i < hi && k < 4; i++) {
+        if (!sel[i]) continue;
+        at[k] = i;
+        la[k] = (i >= 1) ? ((i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1]) : 0u;
+        lb[k] = rs;
+        ra[k] = rs;
+        rb[k] = (i + 2 < n) ? A_ids[i + 2] : 0u;
+        k++;
       }
-      if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, A_ids[i + 2]) < rs;
-      if (bad) first_bad = (uint32_t)i;
+      for (int q = k; q < 4; q++) { at[q] = -1; la[q] = lb[q] = ra[q] = rb[q] = 0u; }
+      pair_rank4(c.T, la, lb, lr);
+      pair_rank4(c.T, ra, rb, rr);
+      for (int q = 0; q < k; q++) {
+        const bool bad = (at[q] >= 1 && lr[q] < rs) || (at[q] + 2 < n && rr[q] < rs);
+        if (bad) { first_bad = (uint32_t)at[q]; break; }
+      }
     }
     const uint32_t limit = g.min_u32(first_bad);
     // (4) merge the selected pairs up to limit, compacting into B
@@ -1105,9 +1174,21 @@ __device__ int64_t merge_rounds(const Call& c, const G& g, int64_t s, int64_t n)
     // (5) re-rank the pairs next to merged pieces
     const int64_t C2 = (n2 + T - 1) / T;
     const int64_t lo2 = min(n2, tid * C2), hi2 = min(n2, lo2 + C2);
-    for (int64_t q = lo2; q < hi2; q++) {
-      if (q + 1 >= n2) B_rk[q] = RANK_MAX;
-      else if (chg[q] || chg[q + 1]) B_rk[q] = pair_rank(c.T, B_ids[q], B_ids[q + 1]);
+    for (int64_t q = lo2; q < hi2;) {
+      int64_t at[4];
+      uint32_t a4[4], b4[4], r4[4];
+      int k = 0;
+      for (; q < hi2 && k < 4; q++) {
+        if (q + 1 >= n2) { B_rk[q] = RANK_MAX; continue; }
+        if (!(chg[q] || chg[q + 1])) continue;
+        at[k] = q;
+        a4[k] = B_ids[q];
+        b4[k] = B_ids[q + 1];
+        k++;
+      }
+      for (int j = k; j < 4; j++) { at[j] = -1; a4[j] = b4[j] = 0u; }
+      pair_rank4(c.T, a4, b4, r4);
+      for (int j = 0; j < k; j++) B_rk[at[j]] = r4[j];
     }
     g.sync();
     uint32_t* t1 = A_ids; A_ids = B_ids; B_ids = t1;
@@ -1138,9 +1219,12 @@ constexpr int MAX_GP = TILE / (SHORT_MAX + 1) + 2;  // pieces merged through glo
 constexpr int REG_MAX = 16;  // pieces up to this length merge in registers
 constexpr uint32_t NO_START = 0xFFFFFFFFu;
 constexpr int64_t STG = TILE + SHORT_MAX + 8;       // staging slot per tile (u32 entries)
+constexpr uint32_t DTAB_LOG2 = 18;                  // dedup table of long pieces: 2^18 slots
 
 struct GPiece {
-  uint32_t rel, len, cnt, short_excl, full_excl;
+  uint32_t rel;  // start in the tile
+  uint32_t src;  // start of the piece whose ids it uses (in the arena)
+  uint32_t cnt, short_excl, full_excl;
 };
 
 struct EncSmem {
@@ -1150,7 +1234,7 @@ struct EncSmem {
   uint32_t gb[TILE / 32];               // starts of pieces merged through global memory
   uint8_t cnt[TILE];                    // ids of the short piece starting at each byte
   uint8_t plen[TILE];                   // length of the short piece starting at each byte
-  uint32_t cls_cnt[8];                  // work list: pieces per length class, then cursors
+  uint32_t cls_cnt[16];                 // work list: class starts [0..N], then fill cursors
   int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
   int32_t outs[TILE + SHORT_MAX];       // work list (x | len << 16), then compacted ids
   uint32_t scr_ids[ETHREADS / 32][SHORT_MAX];  // per-warp scratch for 17..64-byte pieces
@@ -1212,7 +1296,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     for (int v = tid; v < (TILE + EPAD + 16) / 16; v += ETHREADS) {
       const int64_t p = t0 + 16 * v;
       if (aligned && p + 16 <= c.n) {
-        *reinterpret_cast<uint4*>(&sm.text[16 * v]) = __ldg(reinterpret_cast<const uint4*>(c.text + p));
+        *reinterpret_cast<uint4*>(&sm.text[16 * v]) = ld_na_v4(c.text + p);
       } else {
         for (int j = 0; j < 16; j++) sm.text[16 * v + j] = gbyte(c, p + j);
       }
@@ -1230,7 +1314,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       sm.sb[i] = c.T.n_spec ? c.W.sbits[(t0 >> 5) + i] : 0u;
       sm.gb[i] = 0;
     }
-    if (tid < 8) sm.cls_cnt[tid] = 0;
+    if (tid < 16) sm.cls_cnt[tid] = 0;
     if (tid == 0) {
       sm.n_gp = 0;
       sm.n_starts = 0;
@@ -1272,43 +1356,99 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
         sm.plen[x] = (uint8_t)len;
         atomicAdd(&sm.cls_cnt[len_class((int)len)], 1u);
       } else {
-        // merged earlier by k_merge_global: ids in the arena, count in cnt[]
+        // merged earlier by k_merge_big / k_merge_medium: ids in the arena, count in cnt[]
         const int g = atomicAdd(&sm.n_gp, 1);
-        sm.gp[g] = GPiece{(uint32_t)x, (uint32_t)len, c.W.cnt[t0 + x], 0u, 0u};
+        const uint32_t src = c.W.gsrc[t0 + x];
+        sm.gp[g] = GPiece{(uint32_t)x, src, c.W.cnt[src], 0u, 0u};
         atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
         sm.cnt[x] = 0;
       }
     }
     __syncthreads();
     if (tid == 0) {
+      // class k occupies list[cls_cnt[k] .. cls_cnt[k + 1]); cls_cnt[N_CLASSES] = length.
+      // The fill below advances cursor k from the start of class k to its end.
       uint32_t run = 0;
-      for (int k = 0; k < 6; k++) {
+      for (int k = 0; k < N_CLASSES; k++) {
         const uint32_t a = sm.cls_cnt[k];
         sm.cls_cnt[k] = run;
+        sm.cls_cnt[N_CLASSES + 1 + k] = run;
         run += a;
       }
-      sm.cls_cnt[6] = run;               // list length
-      sm.cls_cnt[7] = sm.cls_cnt[5];     // first entry of the 17..64-byte class
+      sm.cls_cnt[N_CLASSES] = run;
     }
     __syncthreads();
     uint32_t* list = reinterpret_cast<uint32_t*>(sm.outs);
     for (uint32_t bits = my; bits; bits &= bits - 1) {
       const int x = xb + __ffs(bits) - 1;
       const int len = sm.plen[x];
-      if (len) list[atomicAdd(&sm.cls_cnt[len_class(len)], 1u)] = (uint32_t)x | ((uint32_t)len << 16);
+      if (len) list[atomicAdd(&sm.cls_cnt[N_CLASSES + 1 + len_class(len)], 1u)] = (uint32_t)x | ((uint32_t)len << 16);
     }
     __syncthreads();
-    // 2b. the list, class by class: 1..16 bytes one thread each, 17..64 bytes
-    //     one warp each (its first lane, on the warp's shared scratch)
+    // 2b. the list, class by class (class k is list[cls_cnt[k] .. cls_cnt[k + 1])).
+    //     One and two bytes: four
+    //     pieces per thread at a time; three bytes: two at a time; up to 16
+    //     bytes: the register loop; 17..64 bytes: one warp each (its first
+    //     lane, on the warp's shared scratch).
     {
-      const uint32_t n_list = sm.cls_cnt[6], first_mid = sm.cls_cnt[7];
       const MergeTabs MT(c.T);
-      for (uint32_t i = tid; i < first_mid; i += ETHREADS) {
+      const uint32_t e0 = sm.cls_cnt[1], e1 = sm.cls_cnt[2], e2 = sm.cls_cnt[3];
+      const uint32_t e5 = sm.cls_cnt[6], e6 = sm.cls_cnt[7];
+      for (uint32_t i = tid; i < e0; i += 4 * ETHREADS) {
+        uint32_t x[4], v[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const uint32_t ii = i + k * ETHREADS;
+          x[k] = ii < e0 ? (list[ii] & 0xFFFFu) : 0u;
+          v[k] = __ldg(&MT.byte_id[sm.text[x[k]]]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          if (i + k * ETHREADS < e0) {
+            sm.stage[x[k]] = (int32_t)v[k];
+            sm.cnt[x[k]] = 1;
+          }
+      }
+      for (uint32_t i = e0 + tid; i < e1; i += 4 * ETHREADS) {
+        uint32_t x[4], r[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const uint32_t ii = i + k * ETHREADS;
+          x[k] = ii < e1 ? (list[ii] & 0xFFFFu) : 0u;
+          r[k] = dense_rank(MT, sm.text[x[k]], sm.text[x[k] + 1]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          if (i + k * ETHREADS >= e1) continue;
+          if (r[k] != RANK_MAX) {
+            sm.stage[x[k]] = (int32_t)r[k];
+            sm.cnt[x[k]] = 1;
+          } else {
+            sm.stage[x[k]] = (int32_t)__ldg(&MT.byte_id[sm.text[x[k]]]);
+            sm.stage[x[k] + 1] = (int32_t)__ldg(&MT.byte_id[sm.text[x[k] + 1]]);
+            sm.cnt[x[k]] = 2;
+          }
+        }
+      }
+      for (uint32_t i = e1 + tid; i < e2; i += 2 * ETHREADS) {
+        const uint32_t i2 = i + ETHREADS;
+        const uint32_t xa = list[i] & 0xFFFFu;
+        const uint32_t xb2 = i2 < e2 ? (list[i2] & 0xFFFFu) : xa;
+        const Ids3 ma = merge3(MT, &sm.text[xa]);
+        const Ids3 mb = merge3(MT, &sm.text[xb2]);
+        put3(&sm.stage[xa], ma);
+        sm.cnt[xa] = (uint8_t)ma.n;
+        if (i2 < e2) {
+          put3(&sm.stage[xb2], mb);
+          sm.cnt[xb2] = (uint8_t)mb.n;
+        }
+      }
+      for (uint32_t i = e2 + tid; i < e5; i += ETHREADS) {
         const uint32_t ent = list[i];
         const int x = ent & 0xFFFF, len = ent >> 16;
         sm.cnt[x] = (uint8_t)merge_small(MT, &sm.text[x], len, &sm.stage[x]);
       }
-      for (uint32_t i = first_mid + warp; i < n_list; i += ETHREADS / 32) {
+      for (uint32_t i = e5 + warp; i < e6; i += ETHREADS / 32) {
         if (lane == 0) {
           const uint32_t ent = list[i];
           const int x = ent & 0xFFFF, len = ent >> 16;
@@ -1395,7 +1535,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       uint32_t* e = slot + STG - 4 * (g + 1);
       e[0] = sm.gp[g].short_excl;
       e[1] = sm.gp[g].full_excl;
-      e[2] = sm.gp[g].rel;
+      e[2] = sm.gp[g].src;
       e[3] = sm.gp[g].cnt;
     }
     if (tid == 0) {
@@ -1434,7 +1574,7 @@ __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int
     for (int g = 0; g < ngp; g++) {
       const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
       const uint64_t o = base + e[1];
-      const int32_t* src = c.W.arena + tile * TILE + e[2];
+      const int32_t* src = c.W.arena + e[2];
       for (uint32_t j = threadIdx.x; j < e[3]; j += blockDim.x)
         if (o + j < (uint64_t)cap) out[o + j] = src[j];
     }
@@ -1473,43 +1613,125 @@ __device__ int64_t piece_end(const Call& c, int64_t p, int64_t ntiles) {
 }
 
 // Pre-tokens longer than SHORT_MAX bytes -> two work lists (medium: one warp
-// each, long: one CTA each), as (start, length) pairs.
+// each, long: one CTA each), as (start, length) pairs.  One thread per word of
+// the start bitmap: a start with another start later in the same word is
+// short; for the word's last start the next three words decide.
 __global__ void k_find_long(Call c) {
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
-  const int64_t nthreads = ntiles * (TILE / 16);
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < nthreads;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t x0 = t * 16;
-    if (x0 >= c.n) continue;
-    uint32_t bits = (c.W.pbits[x0 >> 5] >> (x0 & 31)) & 0xFFFFu;
-    if (x0 + 16 > c.n) bits &= (1u << (c.n - x0)) - 1u;
-    for (; bits; bits &= bits - 1) {
-      const int64_t p = x0 + __ffs(bits) - 1;
-      // quick reject: another start within SHORT_MAX bytes
-      const int64_t e = piece_end(c, p, ntiles);
-      if (e - p <= SHORT_MAX) continue;
-      if (c.T.n_spec && bit_get(c.W.sbits, p)) continue;  // specials are one id
-      if (e - p <= MEDIUM_MAX) {
-        const uint32_t k = atomicAdd(&c.W.status->n_medium, 1u);
-        c.W.long_list[2 * k] = (uint32_t)p;
-        c.W.long_list[2 * k + 1] = (uint32_t)(e - p);
-      } else {
-        const uint32_t k = atomicAdd(&c.W.status->n_biglong, 1u);
-        c.W.big_list[2 * k] = (uint32_t)p;
-        c.W.big_list[2 * k + 1] = (uint32_t)(e - p);
-      }
+  const int64_t nwords = (c.n + 31) >> 5;
+  for (int64_t wi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; wi < nwords;
+       wi += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t bits = c.W.pbits[wi];
+    if ((wi << 5) + 32 > c.n) bits &= (1u << (c.n - (wi << 5))) - 1u;
+    if (!bits) continue;
+    const int last = 31 - __clz(bits);
+    const int64_t p = (wi << 5) + last;
+    // next start within SHORT_MAX bytes after p?
+    bool short_piece = false;
+    for (int k = 1; k <= 3 && !short_piece; k++) {
+      const int64_t w2 = wi + k;
+      if ((w2 << 5) >= c.n) { short_piece = (c.n - p) <= SHORT_MAX; break; }
+      uint32_t b2 = c.W.pbits[w2];
+      if ((w2 << 5) + 32 > c.n) b2 |= ~((1u << (c.n - (w2 << 5))) - 1u);  // the text end ends the piece
+      if (b2) short_piece = (w2 << 5) + __ffs(b2) - 1 - p <= SHORT_MAX;
+      else if ((w2 << 5) + 32 - p > SHORT_MAX) break;
+    }
+    if (short_piece) continue;
+    if (c.T.n_spec && bit_get(c.W.sbits, p)) continue;  // specials are one id
+    const int64_t e = piece_end(c, p, ntiles);
+    if (e - p <= SHORT_MAX) continue;
+    if (e - p <= MEDIUM_MAX) {
+      const uint32_t k = atomicAdd(&c.W.status->n_medium, 1u);
+      c.W.long_list[2 * k] = (uint32_t)p;
+      c.W.long_list[2 * k + 1] = (uint32_t)(e - p);
+    } else {
+      const uint32_t k = atomicAdd(&c.W.status->n_biglong, 1u);
+      c.W.big_list[2 * k] = (uint32_t)p;
+      c.W.big_list[2 * k + 1] = (uint32_t)(e - p);
     }
   }
 }
 
-// Merges the listed pieces: each CTA first takes long pieces (all threads),
-// then each warp takes medium pieces.  ids -> arena[start ..], count -> cnt[start].
-__global__ void __launch_bounds__(ETHREADS) k_merge_global(Call c) {
-  __shared__ int64_t red64[ETHREADS / 32];
-  __shared__ uint32_t red32[ETHREADS / 32];
+// Word cache of the long pieces ("tokenizers v1 ...", "Key Technical
+// Improvements": a repeated word is merged only once).  One warp per listed
+// piece hashes its bytes, then claims a slot of the table or finds the slot
+// of an identical piece (same length, bytes compared one by one), so each
+// distinct long piece is merged once and its copies point at it.
+__device__ __forceinline__ uint64_t mix64(uint64_t x) {
+  x ^= x >> 33;
+  x *= 0xff51afd7ed558ccdull;
+  x ^= x >> 33;
+  x *= 0xc4ceb9fe1a85ec53ull;
+  x ^= x >> 33;
+  return x;
+}
+
+__global__ void k_dedup_global(Call c) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t n_med = c.W.status->n_medium, n_big = c.W.status->n_biglong;
+  const uint64_t mask = (1ull << c.W.dtab_log2) - 1;
+  for (int64_t k = gw; k < (int64_t)n_med + n_big; k += nw) {
+    const uint32_t* ent = k < n_med ? &c.W.long_list[2 * k] : &c.W.big_list[2 * (k - n_med)];
+    const int64_t p = ent[0], len = ent[1];
+    // position-dependent hash of the bytes, 8 per lane step
+    uint64_t h = 0;
+    for (int64_t q = 8 * lane; q < len; q += 256) {
+      uint64_t v = 0;
+      for (int j = 0; j < 8 && q + j < len; j++) v |= (uint64_t)gbyte(c, p + q + j) << (8 * j);
+      h += mix64(v ^ (0x9E3779B97F4A7C15ull * (uint64_t)(q + 1)));
+    }
+    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+    const uint64_t key = mix64(h ^ (uint64_t)len) | 1ull;
+    int64_t src = p;
+    uint64_t slot = key & mask;
+    for (int probe = 0; probe < 64; probe++, slot = (slot + 1) & mask) {
+      unsigned long long old = 0;
+      if (lane == 0) old = atomicCAS(&c.W.dtab[2 * slot], 0ull, (unsigned long long)key);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if (old == 0) {  // claimed: this piece owns the slot
+        if (lane == 0)
+          st_release_u64(reinterpret_cast<uint64_t*>(&c.W.dtab[2 * slot + 1]),
+                         (uint64_t)(p + 1) | ((uint64_t)len << 32));
+        break;
+      }
+      if (old != key) continue;
+      // same key: wait for the owner to publish itself, then compare bytes
+      uint64_t ow = 0;
+      if (lane == 0) {
+        for (uint32_t spins = 0; spins < SPIN_LIMIT; spins++) {
+          ow = ld_acquire_u64(reinterpret_cast<const uint64_t*>(&c.W.dtab[2 * slot + 1]));
+          if (ow) break;
+          __nanosleep(32);
+        }
+      }
+      ow = __shfl_sync(0xffffffffu, ow, 0);
+      if (!ow) break;  // gave up waiting: merge this copy itself
+      const int64_t owner = (int64_t)(ow & 0xFFFFFFFFu) - 1;
+      if ((int64_t)(ow >> 32) != len) continue;
+      bool same = true;
+      for (int64_t q = lane; q < len && same; q += 32) same = gbyte(c, p + q) == gbyte(c, owner + q);
+      if (__all_sync(0xffffffffu, same)) {
+        src = owner;
+        break;
+      }
+    }
+    if (lane == 0) c.W.gsrc[p] = (uint32_t)src;
+  }
+}
+
+// Merges the listed pieces that are the first of their kind (see the word
+// cache above).  k_merge_big: one 1024-thread CTA per piece over MEDIUM_MAX
+// bytes; k_merge_medium: one warp per piece of SHORT_MAX+1..MEDIUM_MAX bytes.
+// ids -> arena[start ..], count -> cnt[start].
+constexpr int BIG_THREADS = 1024;
+__global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
+  __shared__ int64_t red64[BIG_THREADS / 32];
+  __shared__ uint32_t red32[BIG_THREADS / 32];
   __shared__ uint32_t s_idx;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const uint32_t n_big = c.W.status->n_biglong, n_med = c.W.status->n_medium;
+  const int tid = threadIdx.x;
+  const uint32_t n_big = c.W.status->n_biglong;
   for (;;) {
     if (tid == 0) s_idx = atomicAdd(&c.W.status->big_next, 1u);
     __syncthreads();
@@ -1517,15 +1739,22 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_global(Call c) {
     __syncthreads();
     if (k >= n_big) break;
     const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
+    if (c.W.gsrc[p] != (uint32_t)p) continue;  // a copy: uses its owner's ids
     const int64_t m = merge_rounds(c, BlockGroup{red64, red32}, p, len);
     if (tid == 0) c.W.cnt[p] = (uint32_t)m;
   }
+}
+
+__global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t n_med = c.W.status->n_medium;
   for (;;) {
     uint32_t k = 0;
     if (lane == 0) k = atomicAdd(&c.W.status->medium_next, 1u);
     k = __shfl_sync(0xffffffffu, k, 0);
     if (k >= n_med) break;
     const int64_t p = c.W.long_list[2 * k], len = c.W.long_list[2 * k + 1];
+    if (c.W.gsrc[p] != (uint32_t)p) continue;  // a copy: uses its owner's ids
     const int64_t m = merge_rounds(c, WarpGroup{}, p, len);
     if (lane == 0) c.W.cnt[p] = (uint32_t)m;
   }
@@ -1579,6 +1808,7 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
   Work& w = ws->w;
   w.max_bytes = max_bytes;
   w.max_segments = max_segments;
+  w.dtab_log2 = DTAB_LOG2;
   struct Req { void** p; size_t bytes; };
   Req reqs[] = {
       {(void**)&w.status, sizeof(Status)},
@@ -1602,6 +1832,8 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.tile_meta, sizeof(uint32_t) * (n_split_tiles + 1)},
       {(void**)&w.seg_rel, sizeof(uint32_t) * (max_segments + 2)},
       {(void**)&w.tile_segs, sizeof(uint32_t) * 4 * (n_split_tiles + 1)},
+      {(void**)&w.gsrc, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.dtab, sizeof(unsigned long long) * 2 * ((size_t)1 << DTAB_LOG2)},
       {(void**)&w.big_list, sizeof(uint32_t) * 2 * (nb / (MEDIUM_MAX + 1) + 2)},
       {(void**)&w.lrk, sizeof(uint32_t) * (nb + 2)},
       {(void**)&w.lids2, sizeof(uint32_t) * (nb + 2)},
@@ -1614,6 +1846,7 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&ws->d_stage_ids, sizeof(int32_t) * nb},
       {(void**)&ws->d_stage_offsets, sizeof(int64_t) * (max_segments + 1)},
   };
+  static_assert(sizeof(reqs) / sizeof(reqs[0]) <= tk_workspace::MAX_DEV, "workspace buffer table");
   for (auto& r : reqs) {
     cudaError_t e = cudaMalloc(r.p, r.bytes);
     if (e != cudaSuccess) {
@@ -1684,8 +1917,12 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     const int enc_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(per_sm, 1));
     tk_prof_mark(ws, "k_find_long", st);
     k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 16) + 255) / 256, (int64_t)sms * 16), 256, 0, st>>>(c);
-    tk_prof_mark(ws, "k_merge_global", st);
-    k_merge_global<<<sms * 4, ETHREADS, 0, st>>>(c);
+    tk_prof_mark(ws, "k_dedup_global", st);
+    k_dedup_global<<<sms * 8, 256, 0, st>>>(c);
+    tk_prof_mark(ws, "k_merge_big", st);
+    k_merge_big<<<sms, BIG_THREADS, 0, st>>>(c);
+    tk_prof_mark(ws, "k_merge_medium", st);
+    k_merge_medium<<<sms * 4, ETHREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_encode_tiles", st);
     k_encode_tiles<<<enc_grid, ETHREADS, sizeof(EncSmem), st>>>(c);
     tk_prof_mark(ws, "k_scan_u32", st);

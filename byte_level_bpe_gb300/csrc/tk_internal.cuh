@@ -99,6 +99,10 @@ struct Work {
   uint32_t* seg_rel;    // [max_segments + 1] ids before each segment start, within its tile
   uint32_t* tile_segs;  // per split tile: first segment index at or after t0 - HALO, t0,
                         // t0 + TILE, t0 + TILE + HALO
+  uint32_t* gsrc;       // [max_bytes] at each long piece's start: the start of the identical
+                        // piece whose merge it uses (itself for the first occurrence)
+  unsigned long long* dtab;  // dedup table of long pieces: pairs (hash key, owner+1 | len << 32)
+  uint32_t dtab_log2;
   uint32_t* lrk;        // [max_bytes] long merge: pair ranks
   uint32_t* lids2;      // [max_bytes] long merge: second id buffer
   uint32_t* lrk2;       // [max_bytes] long merge: second rank buffer
@@ -185,6 +189,28 @@ struct MergeTabs {
         pair_max_probe(T.pair_max_probe) {}
 };
 
+// Load that bypasses L1 allocation (streams and big random tables), keeping
+// L1 for the small tables the merge reads on every pre-token.
+__device__ __forceinline__ uint64_t ld_na_u64(const uint64_t* p) {
+  uint64_t v;
+  asm("ld.global.nc.L1::no_allocate.u64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_na_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// Rank of the two-byte token b0 b1, or RANK_MAX (the dense first-round table;
+// one L2-resident load measured faster than any compressed form).
+__device__ __forceinline__ uint32_t dense_rank(const MergeTabs& T, uint32_t b0, uint32_t b1) {
+  return __ldg(&T.dense[(b0 << 8) | b1]);
+}
+
 // Carry of an operator whose aggregate can "reset" (the number-run and the
 // segmented code-point counts): every tile publishes its aggregate first
 // (st_release of DESC_AGG | agg); this walk then combines
@@ -249,7 +275,8 @@ __device__ __forceinline__ uint32_t pair_rank(const TT& T, uint32_t a, uint32_t 
 
 struct tk_tokenizer {
   tk::Tables t;
-  void* dev_mem[16];
+  static constexpr int MAX_DEV = 32;
+  void* dev_mem[MAX_DEV];
   int n_dev;
   int64_t n_ranks;
   int device;
@@ -272,7 +299,8 @@ struct tk_workspace {
   tk::Work w;
   tk_profile prof;
   const tk_tokenizer* tok;
-  void* dev_mem[32];
+  static constexpr int MAX_DEV = 64;
+  void* dev_mem[MAX_DEV];
   int n_dev;
   tk::Status* h_status;     // pinned host copy of the status block
   uint8_t* d_stage_text;    // staging for tk_encode_segments_host

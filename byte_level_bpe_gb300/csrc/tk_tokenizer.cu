@@ -84,6 +84,11 @@ static int upload(tk_tokenizer* tk_, const T* src, size_t count, const T** dst) 
     tk_set_error("tk_load: cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
     return TK_E_NOMEM;
   }
+  if (tk_->n_dev >= tk_tokenizer::MAX_DEV) {
+    cudaFree(p);
+    tk_set_error("tk_load: too many device tables");
+    return TK_E_NOMEM;
+  }
   tk_->dev_mem[tk_->n_dev++] = p;
   if (count) {
     e = cudaMemcpy(p, src, sizeof(T) * count, cudaMemcpyHostToDevice);
