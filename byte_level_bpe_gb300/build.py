@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD_DIR, "libtk.so")
-SOURCES = ["tk_encode.cu", "tk_scan.cu", "tk_tokenizer.cu"]
+SOURCES = ["tk_encode.cu", "tk_scan.cu", "tk_tokenizer.cu", "tk_noalloc.cu"]
 HEADERS = ["tk_internal.cuh", "tk_unicode_table.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]

@@ -36,6 +36,7 @@ SIGNATURES = {
     "tk_encode_segments_host": (_INT, [_P, _P, _P, _I64, _P, _P, _I64, _INT, _P, _I64, _P,
                                        ctypes.POINTER(_I64), _P]),
     "tk_decode": (_INT, [_P, _P, _P, _I64, _P, _I64, ctypes.POINTER(_I64), _P]),
+    "tk_decode_noalloc": (_INT, [_P, _P, _I64, _P, _I64, ctypes.POINTER(_I64), _P]),
     "tk_n_ranks": (_I64, [_P]),
     "tk_n_specials": (_I64, [_P]),
     "tk_max_id": (_I64, [_P]),
@@ -166,3 +167,12 @@ def tk_last_stats(ws):
     check(load().tk_last_stats(ws, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
           "tk_last_stats")
     return a.value, b.value, c.value
+
+
+def tk_decode_noalloc(tok, d_ids, n, d_out, cap, stream, raise_on_error=True):
+    """Device pointers (ints); no workspace, no allocation. Returns (status, n_bytes)."""
+    m = _I64(0)
+    rc = load().tk_decode_noalloc(tok, d_ids, n, d_out, cap, ctypes.byref(m), stream)
+    if raise_on_error:
+        check(rc, "tk_decode_noalloc")
+    return rc, m.value

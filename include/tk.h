@@ -150,6 +150,30 @@ int tk_decode(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, i
               uint8_t* d_out, int64_t cap, int64_t* h_len, void* cuda_stream);
 
 /*
+ * tk_decode_noalloc -- tk_decode for callers that cannot allocate device
+ * memory (a server whose memory pool already holds the device's memory, or a
+ * latency-critical path that must not enter the allocator or the device
+ * synchronisation cudaFree may imply).  The pages have no counterpart: this
+ * is an engineering entry point of this library.
+ *
+ *   Same arguments and results as tk_decode, without a workspace: d_ids[n]
+ *   (n <= 1,048,576, else TK_E_LIMIT), d_out[cap], *h_len = total bytes
+ *   (TK_E_CAPACITY when it exceeds cap), TK_E_BADID for an unknown id.
+ *   Allocates nothing: its scratch (about 4 KiB of look-back descriptors and
+ *   a status block) is a fixed array compiled into the library, held by every
+ *   GPU that loads it until the process exits.
+ *
+ *   The first call on a device looks up that array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls on a device share the array: calls that overlap on the GPU race,
+ *   so serialise them (for example on one stream).  Each call clears the part
+ *   of the array it uses before its kernel runs, and returns after reading its
+ *   32-byte status back (the call synchronises cuda_stream).
+ */
+int tk_decode_noalloc(const tk_tokenizer* tok, const int32_t* d_ids, int64_t n, uint8_t* d_out,
+                      int64_t cap, int64_t* h_len, void* cuda_stream);
+
+/*
  * Per-kernel timing of encodes on a workspace, for benchmarks.  With
  * profiling on, every kernel launch of tk_encode_segments /
  * tk_encode_segments_host / tk_decode is bracketed by CUDA events recorded on
