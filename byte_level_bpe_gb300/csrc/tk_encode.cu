@@ -416,6 +416,31 @@ __device__ int win_special(const Call& c, const SplitSmem& sm, int x, int64_t po
   return best;
 }
 
+// The rest of a white-space run from byte q, past the shared-memory window:
+// true iff the run holds no CR/LF and ends at a code point that is not white
+// space inside the same piece (the clause 5-7 question).  A byte scan: the
+// segment's end is looked up once; every position is first tested for a piece
+// start (a chunk cut, or a special that starts there), then classified.
+// check_q: whether q itself must be tested for a piece start.
+__device__ bool g_ws_rest_ends_in_piece(const Call& c, int64_t q, bool check_q) {
+  const int64_t seg_end = c.seg_off[seg_of(c, q) + 1];
+  for (bool first = true;; first = false) {
+    if (q >= c.n || q >= seg_end) return false;
+    if (!first || check_q) {
+      if (g_chunk_cut(c, q)) return false;
+      if (c.T.n_spec && g_special_at(c, q, nullptr)) return false;
+    }
+    const uint32_t b = gbyte(c, q);
+    if (b == 0x0A || b == 0x0D) return false;
+    if (b == 0x20 || b == 0x09 || b == 0x0B || b == 0x0C) { q++; continue; }
+    if (b < 0x80) return true;
+    int len;
+    const uint8_t k = g_kc(c, q, &len) & 7;
+    if (k != K_SP && k != K_WSO && k != K_NL) return true;
+    q += len;
+  }
+}
+
 // Accessors that read the window when the position is trusted, else global.
 struct Win {
   const Call& c;
@@ -509,12 +534,16 @@ __device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) 
         if (absorbed) return true;
         // else a start iff the rest of the run has no CR/LF and does not reach the piece end
         int64_t q = x;
+        bool check_q = false;
         for (;;) {
+          if (!w.trusted(q) || !w.trusted(q + 4)) return g_ws_rest_ends_in_piece(w.c, q, check_q);
           const uint8_t kq = w.kc(q) & 7;
           if (kq == K_NL) return false;
           if (kq != K_SP && kq != K_WSO) return true;
           q = w.next(q);
-          if (q >= w.c.n || w.pst(q)) return false;
+          if (q >= w.c.n) return false;
+          if (!w.trusted(q)) { check_q = true; continue; }
+          if (w.pst(q)) return false;
         }
       }
       // P is white space but not CR/LF: a start iff the next code point is in

@@ -239,3 +239,22 @@ def test_two_calls_in_a_row_reuse_workspace(full_gpu, full_enc, full_table):
     b = workloads.prose_text(full_table, 30000, seed=9)
     for t in (a, b, a):
         _compare(full_gpu, full_enc, [(t, False)], False)
+
+
+def test_long_white_space_walks(full_gpu, full_enc):
+    """CR/LF followed by white space whose run leaves the tile's window: the
+    run may end in text, at a special (a piece start), at a chunk cut or at
+    the text end."""
+    tails = ["<|endoftext|>", "x", "", "  y", "\n\n z"]
+    segs = []
+    for pad in (3, 4000, 4090, 8150):
+        for run in (70, 200, 1000, 5000):
+            for tail in tails:
+                body = "a" * pad + "\n" + " " * run + "\n " + " \t" * (run // 4) + tail
+                segs.append((body, True))
+                segs.append((body, False))
+    _compare(full_gpu, full_enc, segs, False)
+    _compare(full_gpu, full_enc, segs, True)
+    long_run = "q\n" + " " * 60_000 + "<|endoftext|>" + "\n" + " " * 30_000 + "w"
+    _compare(full_gpu, full_enc, [(long_run, True)], True)
+    _compare(full_gpu, full_enc, [(long_run, True)], False)
