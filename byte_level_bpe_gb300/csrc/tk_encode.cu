@@ -1018,122 +1018,67 @@ __device__ __noinline__ int merge_scratch(const MergeTabs T, const uint8_t* b, i
   return m;
 }
 
-// Four pair lookups at once: the first probe of each is issued before any is
-// examined (independent loads in flight), the rare longer probes after.
-__device__ __forceinline__ void pair_rank4(const Tables& T, const uint32_t a[4], const uint32_t b[4],
-                                           uint32_t r[4]) {
-  const uint64_t mask = (1ull << T.pair_log2) - 1;
-  uint64_t key[4], h[4], sl[4];
-#pragma unroll
-  for (int k = 0; k < 4; k++) {
-    key[k] = ((uint64_t)a[k] << 20) | b[k];
-    h[k] = (key[k] * 0x9E3779B97F4A7C15ull) >> (64 - T.pair_log2);
-    sl[k] = __ldg(&T.pair_slots[h[k]]);
+// The group that runs one round merge: NW warps (NW = 1: one warp, no block
+// barriers; else the whole CTA).  s64 / s32 are shared scratch of NW entries.
+template <int NW>
+struct RGroup {
+  int64_t* s64;
+  uint32_t* s32;
+  __device__ int warp() const { return NW == 1 ? 0 : (int)(threadIdx.x >> 5); }
+  __device__ void sync() const {
+    if (NW == 1) __syncwarp();
+    else __syncthreads();
   }
-#pragma unroll
-  for (int k = 0; k < 4; k++) {
-    if (sl[k] == ~0ull) { r[k] = RANK_MAX; continue; }
-    if ((sl[k] >> 20) == key[k]) { r[k] = (uint32_t)(sl[k] & 0xFFFFF); continue; }
-    r[k] = RANK_MAX;
-    uint64_t hh = (h[k] + 1) & mask;
-    for (uint32_t probe = 1; probe <= T.pair_max_probe; probe++) {
-      const uint64_t v = __ldg(&T.pair_slots[hh]);
-      if (v == ~0ull) break;
-      if ((v >> 20) == key[k]) { r[k] = (uint32_t)(v & 0xFFFFF); break; }
-      hh = (hh + 1) & mask;
-    }
-  }
-}
-
-// Cooperative groups for the round merge: a warp (no block barriers) or the
-// whole CTA.
-struct WarpGroup {
-  __device__ int rank() const { return threadIdx.x & 31; }
-  __device__ int size() const { return 32; }
-  __device__ void sync() const { __syncwarp(); }
-  __device__ uint32_t min_u32(uint32_t v) const {
+  __device__ uint32_t gmin(uint32_t v) const {
     for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-  }
-  // exclusive scan (op 0 = sum, 1 = max) with the group total in *tot
-  __device__ int64_t excl(int64_t v, int op, int64_t* tot) const {
-    const int l = threadIdx.x & 31;
-    int64_t x = v;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (l >= o) x = op ? max(x, y) : x + y;
-    }
-    *tot = __shfl_sync(0xffffffffu, x, 31);
-    const int64_t e = __shfl_up_sync(0xffffffffu, x, 1);
-    return l == 0 ? (op ? INT64_MIN : 0) : e;
-  }
-};
-
-struct BlockGroup {
-  int64_t* red64;  // [blockDim / 32]
-  uint32_t* red32;
-  __device__ int rank() const { return threadIdx.x; }
-  __device__ int size() const { return blockDim.x; }
-  __device__ void sync() const { __syncthreads(); }
-  __device__ uint32_t min_u32(uint32_t v) const {
-    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (NW == 1) return v;
     __syncthreads();
-    if (l == 0) red32[w] = v;
+    if ((threadIdx.x & 31) == 0) s32[warp()] = v;
     __syncthreads();
-    if (w == 0) {
-      v = (l < (int)(blockDim.x >> 5)) ? red32[l] : RANK_MAX;
-      for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-      if (l == 0) red32[0] = v;
-    }
-    __syncthreads();
-    const uint32_t r = red32[0];
+    uint32_t r = s32[0];
+    for (int k = 1; k < NW; k++) r = min(r, s32[k]);
     __syncthreads();
     return r;
   }
-  __device__ int64_t excl(int64_t v, int op, int64_t* tot) const {
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  // exclusive max (op 1) or sum (op 0) over the warps of one value per warp
+  __device__ int64_t warp_excl(int64_t wv, int op, int64_t* total) const {
     const int64_t idv = op ? INT64_MIN : 0;
-    int64_t x = v;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (l >= o) x = op ? max(x, y) : x + y;
+    if (NW == 1) {
+      *total = wv;
+      return idv;
     }
     __syncthreads();
-    if (l == 31) red64[w] = x;
+    if ((threadIdx.x & 31) == 0) s64[warp()] = wv;
     __syncthreads();
-    if (w == 0) {
-      int64_t y = (l < nw) ? red64[l] : idv;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t z = __shfl_up_sync(0xffffffffu, y, o);
-        if (l >= o) y = op ? max(y, z) : y + z;
-      }
-      if (l < nw) red64[l] = y;
+    int64_t e = idv, t = idv;
+    for (int k = 0; k < NW; k++) {
+      const int64_t v = s64[k];
+      if (k < warp()) e = op ? max(e, v) : e + v;
+      t = op ? max(t, v) : t + v;
     }
     __syncthreads();
-    const int64_t we = w ? red64[w - 1] : idv;
-    const int64_t le = __shfl_up_sync(0xffffffffu, x, 1);
-    const int64_t e = (l == 0) ? we : (op ? max(we, le) : we + le);
-    *tot = red64[nw - 1];
-    __syncthreads();
+    *total = t;
     return e;
   }
 };
 
 // Exact round merge of the pre-token text[s .. s+n) by a group (see the file
-// header).  Works in the workspace at the piece's byte offset; the ids end in
-// arena[s ..].  Returns the number of ids.
-template <class G>
-__device__ int64_t merge_rounds(const Call& c, const G& g, int64_t s, int64_t n) {
+// header).  Each warp owns a contiguous chunk of the parts and its lanes take
+// consecutive parts, so every pass reads and writes coalesced.  Works in the
+// workspace at the piece's byte offset; the ids end in arena[s ..].  Returns
+// the number of ids.
+template <int NW>
+__device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, int64_t n) {
   uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + s);
   uint32_t* A_rk = c.W.lrk + s;
   uint32_t* B_ids = c.W.lids2 + s;
   uint32_t* B_rk = c.W.lrk2 + s;
   uint8_t* sel = c.W.lsel + s;
   uint8_t* chg = c.W.lchg + s;
-  const int T = g.size(), tid = g.rank();
+  const int lane = threadIdx.x & 31, w = g.warp();
+  const uint32_t lt = (1u << lane) - 1u;  // lanes below this one
   const int64_t n0 = n;
-  for (int64_t i = tid; i < n; i += T) {
+  for (int64_t i = (int64_t)w * 32 + lane; i < n; i += NW * 32) {
     const uint32_t b = gbyte(c, s + i);
     A_ids[i] = __ldg(&c.T.byte_id[b]);
     A_rk[i] = (i + 1 < n) ? __ldg(&c.T.dense[(b << 8) | gbyte(c, s + i + 1)]) : RANK_MAX;
@@ -1141,83 +1086,78 @@ __device__ int64_t merge_rounds(const Call& c, const G& g, int64_t s, int64_t n)
   g.sync();
   bool in_b = false;
   for (int64_t round = 0;; round++) {
-    const int64_t C = (n + T - 1) / T;
-    const int64_t lo = min(n, tid * C), hi = min(n, lo + C);
+    const int64_t cw = (((n + NW - 1) / NW) + 31) & ~(int64_t)31;
+    const int64_t wlo = min(n, (int64_t)w * cw), whi = min(n, wlo + cw);
     // (1) the minimum pair rank
     uint32_t m = RANK_MAX;
-    for (int64_t i = lo; i < hi; i++) m = min(m, A_rk[i]);
-    const uint32_t rs = g.min_u32(m);
+    for (int64_t i = wlo + lane; i < whi; i += 32) m = min(m, A_rk[i]);
+    const uint32_t rs = g.gmin(m);
     if (rs == RANK_MAX) break;
-    // (2) chains of rs-pairs: every other pair from each chain's start
-    int64_t last_non = -1;
-    for (int64_t i = lo; i < hi; i++)
-      if (A_rk[i] != rs) last_non = i;
+    // (2) chains of rs-pairs: every other pair from each chain's start.  The
+    //     last non-candidate before each part comes from ballots and a carry.
+    int64_t ln_w = -1;
+    for (int64_t b = wlo; b < whi; b += 32) {
+      const int64_t i = b + lane;
+      const uint32_t nm = __ballot_sync(0xffffffffu, i < whi && A_rk[i] != rs);
+      if (nm) ln_w = b + 31 - __clz(nm);
+    }
     int64_t tot;
-    const int64_t before = g.excl(last_non, 1, &tot);
-    int64_t ln = before < -1 ? -1 : before;
-    for (int64_t i = lo; i < hi; i++) {
-      if (A_rk[i] != rs) { ln = i; sel[i] = 0; }
-      else sel[i] = ((i - ln - 1) & 1) == 0;
+    int64_t carry = g.warp_excl(ln_w, 1, &tot);
+    if (carry < -1) carry = -1;
+    for (int64_t b = wlo; b < whi; b += 32) {
+      const int64_t i = b + lane;
+      const bool in = i < whi;
+      const bool cand = in && A_rk[i] == rs;
+      const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
+      const uint32_t before = nm & lt;
+      const int64_t ln = before ? b + 31 - __clz(before) : carry;
+      if (in) sel[i] = cand && (((i - ln - 1) & 1) == 0);
+      if (nm) carry = b + 31 - __clz(nm);
     }
     g.sync();
     // (3) the first selected merge that creates a neighbour pair of lower rank
-    //     (its left and right pairs looked up four selected merges at a time)
-    uint32_t first_bad = 0xFFFFFFFFu;
-    for (int64_t i = lo; i < hi && first_bad == 0xFFFFFFFFu;) {
-      int64_t at[4];
-      uint32_t la[4], lb[4], ra[4], rb[4], lr[4], rr[4];
-      int k = 0;
-      for (; i < hi && k < 4; i++) {
-        if (!sel[i]) continue;
-        at[k] = i;
-        la[k] = (i >= 1) ? ((i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1]) : 0u;
-        lb[k] = rs;
-        ra[k] = rs;
-        rb[k] = (i + 2 < n) ? A_ids[i + 2] : 0u;
-        k++;
+    uint32_t fb = 0xFFFFFFFFu;
+    for (int64_t b = wlo; b < whi && fb == 0xFFFFFFFFu; b += 32) {
+      const int64_t i = b + lane;
+      bool bad = false;
+      if (i < whi && sel[i]) {
+        if (i >= 1) {
+          const uint32_t left = (i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1];
+          bad = pair_rank(c.T, left, rs) < rs;
+        }
+        if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, A_ids[i + 2]) < rs;
       }
-      for (int q = k; q < 4; q++) { at[q] = -1; la[q] = lb[q] = ra[q] = rb[q] = 0u; }
-      pair_rank4(c.T, la, lb, lr);
-      pair_rank4(c.T, ra, rb, rr);
-      for (int q = 0; q < k; q++) {
-        const bool bad = (at[q] >= 1 && lr[q] < rs) || (at[q] + 2 < n && rr[q] < rs);
-        if (bad) { first_bad = (uint32_t)at[q]; break; }
-      }
+      const uint32_t bm = __ballot_sync(0xffffffffu, bad);
+      if (bm) fb = (uint32_t)(b + __ffs(bm) - 1);
     }
-    const uint32_t limit = g.min_u32(first_bad);
+    const uint32_t limit = g.gmin(fb);
     // (4) merge the selected pairs up to limit, compacting into B
-    int64_t keep = 0;
-    for (int64_t i = lo; i < hi; i++)
-      keep += !(i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit);
-    int64_t dst = g.excl(keep, 0, &tot);
+    int64_t keep_w = 0;
+    for (int64_t b = wlo; b < whi; b += 32) {
+      const int64_t i = b + lane;
+      const bool kp = i < whi && !(i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit);
+      keep_w += __popc(__ballot_sync(0xffffffffu, kp));
+    }
+    int64_t dst = g.warp_excl(keep_w, 0, &tot);
     const int64_t n2 = tot;
-    for (int64_t i = lo; i < hi; i++) {
-      if (i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit) continue;
-      const bool merged = sel[i] && (uint64_t)i <= (uint64_t)limit;
-      B_ids[dst] = merged ? rs : A_ids[i];
-      B_rk[dst] = A_rk[i];
-      chg[dst] = merged;
-      dst++;
+    for (int64_t b = wlo; b < whi; b += 32) {
+      const int64_t i = b + lane;
+      const bool kp = i < whi && !(i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit);
+      const uint32_t km = __ballot_sync(0xffffffffu, kp);
+      if (kp) {
+        const int64_t pos = dst + __popc(km & lt);
+        const bool merged = sel[i] && (uint64_t)i <= (uint64_t)limit;
+        B_ids[pos] = merged ? rs : A_ids[i];
+        B_rk[pos] = A_rk[i];
+        chg[pos] = merged;
+      }
+      dst += __popc(km);
     }
     g.sync();
     // (5) re-rank the pairs next to merged pieces
-    const int64_t C2 = (n2 + T - 1) / T;
-    const int64_t lo2 = min(n2, tid * C2), hi2 = min(n2, lo2 + C2);
-    for (int64_t q = lo2; q < hi2;) {
-      int64_t at[4];
-      uint32_t a4[4], b4[4], r4[4];
-      int k = 0;
-      for (; q < hi2 && k < 4; q++) {
-        if (q + 1 >= n2) { B_rk[q] = RANK_MAX; continue; }
-        if (!(chg[q] || chg[q + 1])) continue;
-        at[k] = q;
-        a4[k] = B_ids[q];
-        b4[k] = B_ids[q + 1];
-        k++;
-      }
-      for (int j = k; j < 4; j++) { at[j] = -1; a4[j] = b4[j] = 0u; }
-      pair_rank4(c.T, a4, b4, r4);
-      for (int j = 0; j < k; j++) B_rk[at[j]] = r4[j];
+    for (int64_t q = (int64_t)w * 32 + lane; q < n2; q += NW * 32) {
+      if (q + 1 >= n2) B_rk[q] = RANK_MAX;
+      else if (chg[q] || chg[q + 1]) B_rk[q] = pair_rank(c.T, B_ids[q], B_ids[q + 1]);
     }
     g.sync();
     uint32_t* t1 = A_ids; A_ids = B_ids; B_ids = t1;
@@ -1225,11 +1165,14 @@ __device__ int64_t merge_rounds(const Call& c, const G& g, int64_t s, int64_t n)
     in_b = !in_b;
     n = n2;
     // every round merges at least one pair, so n0 rounds always suffice
-    if (round > n0) { if (tid == 0) set_error(c.W.status, TK_E_LIMIT, 6); break; }
+    if (round > n0) {
+      if (threadIdx.x == 0) set_error(c.W.status, TK_E_LIMIT, 6);
+      break;
+    }
   }
   if (in_b) {
     uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + s);
-    for (int64_t i = tid; i < n; i += T) dst[i] = A_ids[i];
+    for (int64_t i = (int64_t)w * 32 + lane; i < n; i += NW * 32) dst[i] = A_ids[i];
     g.sync();
   }
   return n;
@@ -1695,58 +1638,116 @@ __device__ __forceinline__ uint64_t mix64(uint64_t x) {
   return x;
 }
 
-__global__ void k_dedup_global(Call c) {
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const uint32_t n_med = c.W.status->n_medium, n_big = c.W.status->n_biglong;
+// Order-free hash of the bytes text[p .. p+len): a sum over 8-byte groups,
+// each mixed with its position, so any split of the groups among threads
+// gives the same value.  Returns this thread's partial sum over groups
+// first, first + step, ...
+__device__ __forceinline__ uint64_t hash_part(const Call& c, int64_t p, int64_t len, int64_t first,
+                                              int64_t step) {
+  uint64_t h = 0;
+  for (int64_t g = first; 8 * g < len; g += step) {
+    const int64_t q = 8 * g;
+    uint64_t v = 0;
+    for (int j = 0; j < 8 && q + j < len; j++) v |= (uint64_t)gbyte(c, p + q + j) << (8 * j);
+    h += mix64(v ^ (0x9E3779B97F4A7C15ull * (uint64_t)(q + 1)));
+  }
+  return h;
+}
+
+// Claims a slot for (key, p, len) or finds the slot of an identical piece.
+// Run by all lanes of a warp (medium pieces) or all threads of a CTA (big);
+// `eq` compares the bytes with a candidate owner across the group.  Returns
+// the start of the piece whose merge p uses.
+template <class Eq>
+__device__ int64_t dedup_claim(const Call& c, uint64_t key, int64_t p, int64_t len, bool leader,
+                               uint64_t* shared_word, Eq eq, bool cta) {
   const uint64_t mask = (1ull << c.W.dtab_log2) - 1;
-  for (int64_t k = gw; k < (int64_t)n_med + n_big; k += nw) {
-    const uint32_t* ent = k < n_med ? &c.W.long_list[2 * k] : &c.W.big_list[2 * (k - n_med)];
-    const int64_t p = ent[0], len = ent[1];
-    // position-dependent hash of the bytes, 8 per lane step
-    uint64_t h = 0;
-    for (int64_t q = 8 * lane; q < len; q += 256) {
-      uint64_t v = 0;
-      for (int j = 0; j < 8 && q + j < len; j++) v |= (uint64_t)gbyte(c, p + q + j) << (8 * j);
-      h += mix64(v ^ (0x9E3779B97F4A7C15ull * (uint64_t)(q + 1)));
-    }
-    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
-    const uint64_t key = mix64(h ^ (uint64_t)len) | 1ull;
-    int64_t src = p;
-    uint64_t slot = key & mask;
-    for (int probe = 0; probe < 64; probe++, slot = (slot + 1) & mask) {
-      unsigned long long old = 0;
-      if (lane == 0) old = atomicCAS(&c.W.dtab[2 * slot], 0ull, (unsigned long long)key);
-      old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == 0) {  // claimed: this piece owns the slot
-        if (lane == 0)
-          st_release_u64(reinterpret_cast<uint64_t*>(&c.W.dtab[2 * slot + 1]),
-                         (uint64_t)(p + 1) | ((uint64_t)len << 32));
-        break;
-      }
-      if (old != key) continue;
-      // same key: wait for the owner to publish itself, then compare bytes
-      uint64_t ow = 0;
-      if (lane == 0) {
+  uint64_t slot = key & mask;
+  for (int probe = 0; probe < 64; probe++, slot = (slot + 1) & mask) {
+    // one thread claims or reads the slot, then the owner word; all share it
+    if (leader) {
+      const unsigned long long old = atomicCAS(&c.W.dtab[2 * slot], 0ull, (unsigned long long)key);
+      uint64_t r;
+      if (old == 0) {
+        st_release_u64(reinterpret_cast<uint64_t*>(&c.W.dtab[2 * slot + 1]),
+                       (uint64_t)(p + 1) | ((uint64_t)len << 32));
+        r = 1;  // claimed
+      } else if (old != key) {
+        r = 2;  // another key: next slot
+      } else {
+        uint64_t ow = 0;
         for (uint32_t spins = 0; spins < SPIN_LIMIT; spins++) {
           ow = ld_acquire_u64(reinterpret_cast<const uint64_t*>(&c.W.dtab[2 * slot + 1]));
           if (ow) break;
           __nanosleep(32);
         }
+        r = ow ? ow : 3;  // 3: gave up waiting
       }
-      ow = __shfl_sync(0xffffffffu, ow, 0);
-      if (!ow) break;  // gave up waiting: merge this copy itself
-      const int64_t owner = (int64_t)(ow & 0xFFFFFFFFu) - 1;
-      if ((int64_t)(ow >> 32) != len) continue;
+      *shared_word = r;
+    }
+    if (cta) __syncthreads();
+    else __syncwarp();
+    const uint64_t r = *shared_word;
+    if (cta) __syncthreads();
+    else __syncwarp();
+    if (r == 1 || r == 3) return p;  // owner (or give up: merge this copy itself)
+    if (r == 2) continue;
+    const int64_t owner = (int64_t)(r & 0xFFFFFFFFu) - 1;
+    if ((int64_t)(r >> 32) != len) continue;
+    if (eq(owner)) return owner;
+  }
+  return p;
+}
+
+__global__ void k_dedup_medium(Call c) {
+  __shared__ uint64_t s_word[ETHREADS / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t n_med = c.W.status->n_medium;
+  for (int64_t k = gw; k < n_med; k += nw) {
+    const int64_t p = c.W.long_list[2 * k], len = c.W.long_list[2 * k + 1];
+    uint64_t h = hash_part(c, p, len, lane, 32);
+    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+    const uint64_t key = mix64(h ^ (uint64_t)len) | 1ull;
+    auto eq = [&](int64_t owner) {
       bool same = true;
       for (int64_t q = lane; q < len && same; q += 32) same = gbyte(c, p + q) == gbyte(c, owner + q);
-      if (__all_sync(0xffffffffu, same)) {
-        src = owner;
-        break;
-      }
-    }
+      return (bool)__all_sync(0xffffffffu, same);
+    };
+    const int64_t src = dedup_claim(c, key, p, len, lane == 0, &s_word[warp], eq, false);
     if (lane == 0) c.W.gsrc[p] = (uint32_t)src;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_dedup_big(Call c) {
+  __shared__ uint64_t s_red[32];
+  __shared__ uint64_t s_word;
+  __shared__ uint32_t s_idx;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t n_big = c.W.status->n_biglong;
+  for (;;) {
+    if (tid == 0) s_idx = atomicAdd(&c.W.status->dedup_big_next, 1u);
+    __syncthreads();
+    const uint32_t k = s_idx;
+    __syncthreads();
+    if (k >= n_big) break;
+    const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
+    uint64_t h = hash_part(c, p, len, tid, blockDim.x);
+    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+    if (lane == 0) s_red[warp] = h;
+    __syncthreads();
+    h = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) h += s_red[w];
+    __syncthreads();
+    const uint64_t key = mix64(h ^ (uint64_t)len) | 1ull;
+    auto eq = [&](int64_t owner) {
+      bool same = true;
+      for (int64_t q = tid; q < len && same; q += blockDim.x) same = gbyte(c, p + q) == gbyte(c, owner + q);
+      return (bool)__syncthreads_and(same);
+    };
+    const int64_t src = dedup_claim(c, key, p, len, tid == 0, &s_word, eq, true);
+    if (tid == 0) c.W.gsrc[p] = (uint32_t)src;
   }
 }
 
@@ -1769,7 +1770,7 @@ __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
     if (k >= n_big) break;
     const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
     if (c.W.gsrc[p] != (uint32_t)p) continue;  // a copy: uses its owner's ids
-    const int64_t m = merge_rounds(c, BlockGroup{red64, red32}, p, len);
+    const int64_t m = merge_rounds(c, RGroup<BIG_THREADS / 32>{red64, red32}, p, len);
     if (tid == 0) c.W.cnt[p] = (uint32_t)m;
   }
 }
@@ -1784,7 +1785,7 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
     if (k >= n_med) break;
     const int64_t p = c.W.long_list[2 * k], len = c.W.long_list[2 * k + 1];
     if (c.W.gsrc[p] != (uint32_t)p) continue;  // a copy: uses its owner's ids
-    const int64_t m = merge_rounds(c, WarpGroup{}, p, len);
+    const int64_t m = merge_rounds(c, RGroup<1>{nullptr, nullptr}, p, len);
     if (lane == 0) c.W.cnt[p] = (uint32_t)m;
   }
 }
@@ -1946,8 +1947,10 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     const int enc_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(per_sm, 1));
     tk_prof_mark(ws, "k_find_long", st);
     k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 16) + 255) / 256, (int64_t)sms * 16), 256, 0, st>>>(c);
-    tk_prof_mark(ws, "k_dedup_global", st);
-    k_dedup_global<<<sms * 8, 256, 0, st>>>(c);
+    tk_prof_mark(ws, "k_dedup_medium", st);
+    k_dedup_medium<<<sms * 8, ETHREADS, 0, st>>>(c);
+    tk_prof_mark(ws, "k_dedup_big", st);
+    k_dedup_big<<<sms, 1024, 0, st>>>(c);
     tk_prof_mark(ws, "k_merge_big", st);
     k_merge_big<<<sms, BIG_THREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_merge_medium", st);

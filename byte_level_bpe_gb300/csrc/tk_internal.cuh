@@ -52,6 +52,7 @@ struct Status {
   uint32_t n_biglong;
   uint32_t medium_next;
   uint32_t big_next;
+  uint32_t dedup_big_next;
   uint32_t tile_ctr[8];  // dynamic tile counters of the persistent kernels
   int64_t n_tiles;       // split tiles of this call (element count of the tile scan)
 };
