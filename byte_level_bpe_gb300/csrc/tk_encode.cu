@@ -112,6 +112,11 @@ __device__ __forceinline__ bool bit_get(const uint32_t* b, int64_t i) { return (
 struct Call {
   const uint8_t* text;
   int64_t n;
+  // Long pieces are indexed in the workspace by their global position
+  // gb + p: a pipelined host call places batch k's text at gb inside one
+  // staging buffer (text - gb), so a long piece of a later batch can use the
+  // ids merged for an identical piece of an earlier one.  0 otherwise.
+  int64_t gb;
   const int64_t* seg_off;
   const uint8_t* allow;
   int64_t S;
@@ -146,6 +151,10 @@ __device__ int64_t seg_lower(const Call& c, int64_t pos) {
 __device__ __forceinline__ uint8_t gbyte(const Call& c, int64_t p) {
   return (p >= 0 && p < c.n) ? __ldg(&c.text[p]) : 0;
 }
+
+// The byte at global position G (a long piece's bytes, possibly in an earlier
+// batch of the same pipelined call).
+__device__ __forceinline__ uint8_t text_at(const Call& c, int64_t G) { return __ldg(c.text - c.gb + G); }
 
 __device__ bool g_chunk_cut(const Call& c, int64_t pos) {
   if (!c.safe) return false;
@@ -234,7 +243,7 @@ struct SegCountOp {
 // Kernel: zero the status block and the look-back descriptors of one call.
 
 __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int safe,
-                        int64_t n_cut_words, int64_t n_tiles) {
+                        int64_t n_cut_words, int64_t n_tiles, int clear_dtab) {
   const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (tid == 0) {
@@ -251,7 +260,8 @@ __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int s
   for (int64_t i = tid; i < n_desc_scan; i += stride) W.desc_c[i] = 0;
   if (safe)
     for (int64_t i = tid; i < n_cut_words; i += stride) { W.win_cut[i] = 0; W.run_cut[i] = 0; }
-  for (int64_t i = tid; i < (2ll << W.dtab_log2); i += stride) W.dtab[i] = 0ull;
+  if (clear_dtab)
+    for (int64_t i = tid; i < (2ll << W.dtab_log2); i += stride) W.dtab[i] = 0ull;
 }
 
 // Segment table check: seg_off[0] = 0, non-decreasing, seg_off[S] = n.
@@ -1069,12 +1079,13 @@ struct RGroup {
 // the number of ids.
 template <int NW>
 __device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, int64_t n) {
-  uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + s);
-  uint32_t* A_rk = c.W.lrk + s;
-  uint32_t* B_ids = c.W.lids2 + s;
-  uint32_t* B_rk = c.W.lrk2 + s;
-  uint8_t* sel = c.W.lsel + s;
-  uint8_t* chg = c.W.lchg + s;
+  const int64_t G = c.gb + s;
+  uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + G);
+  uint32_t* A_rk = c.W.lrk + G;
+  uint32_t* B_ids = c.W.lids2 + G;
+  uint32_t* B_rk = c.W.lrk2 + G;
+  uint8_t* sel = c.W.lsel + G;
+  uint8_t* chg = c.W.lchg + G;
   const int lane = threadIdx.x & 31, w = g.warp();
   const uint32_t lt = (1u << lane) - 1u;  // lanes below this one
   const int64_t n0 = n;
@@ -1171,7 +1182,7 @@ __device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, i
     }
   }
   if (in_b) {
-    uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + s);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + G);
     for (int64_t i = (int64_t)w * 32 + lane; i < n; i += NW * 32) dst[i] = A_ids[i];
     g.sync();
   }
@@ -1330,7 +1341,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       } else {
         // merged earlier by k_merge_big / k_merge_medium: ids in the arena, count in cnt[]
         const int g = atomicAdd(&sm.n_gp, 1);
-        const uint32_t src = c.W.gsrc[t0 + x];
+        const uint32_t src = c.W.gsrc[c.gb + t0 + x];
         sm.gp[g] = GPiece{(uint32_t)x, src, c.W.cnt[src], 0u, 0u};
         atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
         sm.cnt[x] = 0;
@@ -1523,47 +1534,117 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
 }
 
 // Ordered output: each tile's staged ids go to out[tile_base + ...], with the
-// ids of its long pieces inserted from the arena.
+// ids of its long pieces inserted from the arena.  A tile without long pieces
+// is one straight copy, 16 ids per thread in flight.  Long pieces of more than
+// HUGE_IDS ids are listed for k_copy_huge, which spreads them over the grid.
+constexpr uint32_t HUGE_IDS = 8192;
+constexpr int COPY_UNROLL = 16;
+static_assert((STG * sizeof(uint32_t)) % 16 == 0, "staging slots stay 16-byte aligned");
+
 __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int64_t cap) {
   __shared__ uint32_t s_gp[MAX_GP * 4];
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  const int tid = threadIdx.x;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const uint64_t base = c.W.tile_base[tile];
     const uint32_t meta = c.W.tile_meta[tile];
     const uint32_t n_short = meta & 0xFFFFFFu;
     const int ngp = (int)(meta >> 24);
     const uint32_t* slot = c.W.staging + tile * STG;
-    for (int i = threadIdx.x; i < 4 * ngp; i += blockDim.x) s_gp[i] = slot[STG - 4 * ngp + i];
+    if (ngp == 0) {
+      for (uint32_t q0 = 0; q0 < n_short; q0 += COPY_UNROLL * ETHREADS) {
+        uint32_t v[COPY_UNROLL];
+#pragma unroll
+        for (int k = 0; k < COPY_UNROLL; k++) {
+          const uint32_t q = q0 + k * ETHREADS + tid;
+          v[k] = q < n_short ? __ldcs(slot + q) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < COPY_UNROLL; k++) {
+          const uint32_t q = q0 + k * ETHREADS + tid;
+          if (q < n_short && base + q < (uint64_t)cap) out[base + q] = (int32_t)v[k];
+        }
+      }
+      continue;
+    }
+    for (int i = tid; i < 4 * ngp; i += blockDim.x) s_gp[i] = slot[STG - 4 * ngp + i];
     __syncthreads();
-    for (uint32_t q = threadIdx.x; q < n_short; q += blockDim.x) {
+    for (uint32_t q = tid; q < n_short; q += blockDim.x) {
       uint64_t pos = base + q;
       for (int g = 0; g < ngp; g++) {
         const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
         if (e[0] <= q) pos += e[3];
       }
-      if (pos < (uint64_t)cap) out[pos] = (int32_t)slot[q];
+      if (pos < (uint64_t)cap) out[pos] = (int32_t)__ldcs(slot + q);
     }
     for (int g = 0; g < ngp; g++) {
       const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
       const uint64_t o = base + e[1];
+      if (e[3] > HUGE_IDS) {
+        if (tid == 0) {
+          const uint32_t k = atomicAdd(&c.W.status->n_huge, 1u);
+          c.W.huge_list[3 * (uint64_t)k] = o;
+          c.W.huge_list[3 * (uint64_t)k + 1] = e[2];
+          c.W.huge_list[3 * (uint64_t)k + 2] = e[3];
+        }
+        continue;
+      }
       const int32_t* src = c.W.arena + e[2];
-      for (uint32_t j = threadIdx.x; j < e[3]; j += blockDim.x)
+      for (uint32_t j = tid; j < e[3]; j += blockDim.x)
         if (o + j < (uint64_t)cap) out[o + j] = src[j];
     }
     __syncthreads();
   }
 }
 
+// The listed long pieces, each copied by every thread of the grid.
+__global__ void __launch_bounds__(ETHREADS) k_copy_huge(Call c, int32_t* out, int64_t cap) {
+  const uint32_t n_huge = c.W.status->n_huge;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  const uint64_t me = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (uint32_t k = 0; k < n_huge; k++) {
+    const uint64_t o = c.W.huge_list[3 * (uint64_t)k];
+    const int32_t* src = c.W.arena + c.W.huge_list[3 * (uint64_t)k + 1];
+    const uint64_t cnt = c.W.huge_list[3 * (uint64_t)k + 2];
+    for (uint64_t j0 = 0; j0 < cnt; j0 += 4 * stride) {
+      int32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const uint64_t j = j0 + u * stride + me;
+        v[u] = j < cnt ? __ldcs(src + j) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const uint64_t j = j0 + u * stride + me;
+        if (j < cnt && o + j < (uint64_t)cap) out[o + j] = v[u];
+      }
+    }
+  }
+}
+
 // out_offsets[s] = the tile base of the tile that holds segment s's start plus
 // the ids before it in that tile; n_ids = total.
-__global__ void k_seg_offsets(Call c, int64_t* out_offsets) {
+// With id_base (a batch of a pipelined call) every offset is shifted by
+// *id_base, and id_base[1] = *id_base + n_ids.
+__global__ void k_seg_offsets(Call c, int64_t* out_offsets, int64_t* id_base) {
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  const int64_t b = id_base ? id_base[0] : 0;
   for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s <= c.S;
        s += (int64_t)gridDim.x * blockDim.x) {
     const int64_t tile = min(c.seg_off[s] / TILE, ntiles - 1);
-    out_offsets[s] = (int64_t)c.W.tile_base[tile] + c.W.seg_rel[s];
+    out_offsets[s] = b + (int64_t)c.W.tile_base[tile] + c.W.seg_rel[s];
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) c.W.status->n_ids = c.W.tile_base[ntiles];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    c.W.status->n_ids = c.W.tile_base[ntiles];
+    if (id_base) id_base[1] = b + c.W.tile_base[ntiles];
+  }
+}
+
+// off[i] = raw[i] - raw[0]: a batch's segment offsets made relative to its text.
+__global__ void k_rebase(const int64_t* raw, int64_t* off, int64_t cnt) {
+  const int64_t r0 = raw[0];
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < cnt; i += (int64_t)gridDim.x * blockDim.x)
+    off[i] = raw[i] - r0;
 }
 
 // End of the pre-token that starts at byte p: the next start bit, else the
@@ -1670,7 +1751,7 @@ __device__ int64_t dedup_claim(const Call& c, uint64_t key, int64_t p, int64_t l
       uint64_t r;
       if (old == 0) {
         st_release_u64(reinterpret_cast<uint64_t*>(&c.W.dtab[2 * slot + 1]),
-                       (uint64_t)(p + 1) | ((uint64_t)len << 32));
+                       (uint64_t)(c.gb + p + 1) | ((uint64_t)len << 32));
         r = 1;  // claimed
       } else if (old != key) {
         r = 2;  // another key: next slot
@@ -1690,13 +1771,13 @@ __device__ int64_t dedup_claim(const Call& c, uint64_t key, int64_t p, int64_t l
     const uint64_t r = *shared_word;
     if (cta) __syncthreads();
     else __syncwarp();
-    if (r == 1 || r == 3) return p;  // owner (or give up: merge this copy itself)
+    if (r == 1 || r == 3) return c.gb + p;  // owner (or give up: merge this copy itself)
     if (r == 2) continue;
     const int64_t owner = (int64_t)(r & 0xFFFFFFFFu) - 1;
     if ((int64_t)(r >> 32) != len) continue;
     if (eq(owner)) return owner;
   }
-  return p;
+  return c.gb + p;
 }
 
 __global__ void k_dedup_medium(Call c) {
@@ -1712,11 +1793,11 @@ __global__ void k_dedup_medium(Call c) {
     const uint64_t key = mix64(h ^ (uint64_t)len) | 1ull;
     auto eq = [&](int64_t owner) {
       bool same = true;
-      for (int64_t q = lane; q < len && same; q += 32) same = gbyte(c, p + q) == gbyte(c, owner + q);
+      for (int64_t q = lane; q < len && same; q += 32) same = gbyte(c, p + q) == text_at(c, owner + q);
       return (bool)__all_sync(0xffffffffu, same);
     };
     const int64_t src = dedup_claim(c, key, p, len, lane == 0, &s_word[warp], eq, false);
-    if (lane == 0) c.W.gsrc[p] = (uint32_t)src;
+    if (lane == 0) c.W.gsrc[c.gb + p] = (uint32_t)src;
   }
 }
 
@@ -1743,11 +1824,11 @@ __global__ void __launch_bounds__(1024) k_dedup_big(Call c) {
     const uint64_t key = mix64(h ^ (uint64_t)len) | 1ull;
     auto eq = [&](int64_t owner) {
       bool same = true;
-      for (int64_t q = tid; q < len && same; q += blockDim.x) same = gbyte(c, p + q) == gbyte(c, owner + q);
+      for (int64_t q = tid; q < len && same; q += blockDim.x) same = gbyte(c, p + q) == text_at(c, owner + q);
       return (bool)__syncthreads_and(same);
     };
     const int64_t src = dedup_claim(c, key, p, len, tid == 0, &s_word, eq, true);
-    if (tid == 0) c.W.gsrc[p] = (uint32_t)src;
+    if (tid == 0) c.W.gsrc[c.gb + p] = (uint32_t)src;
   }
 }
 
@@ -1769,9 +1850,9 @@ __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
     __syncthreads();
     if (k >= n_big) break;
     const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
-    if (c.W.gsrc[p] != (uint32_t)p) continue;  // a copy: uses its owner's ids
+    if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
     const int64_t m = merge_rounds(c, RGroup<BIG_THREADS / 32>{red64, red32}, p, len);
-    if (tid == 0) c.W.cnt[p] = (uint32_t)m;
+    if (tid == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
   }
 }
 
@@ -1784,16 +1865,18 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
     k = __shfl_sync(0xffffffffu, k, 0);
     if (k >= n_med) break;
     const int64_t p = c.W.long_list[2 * k], len = c.W.long_list[2 * k + 1];
-    if (c.W.gsrc[p] != (uint32_t)p) continue;  // a copy: uses its owner's ids
+    if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
     const int64_t m = merge_rounds(c, RGroup<1>{nullptr, nullptr}, p, len);
-    if (lane == 0) c.W.cnt[p] = (uint32_t)m;
+    if (lane == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
   }
 }
 
 // Offsets of an encode with no text: every segment is empty.
-__global__ void k_empty_offsets(Call c, int64_t* out_offsets) {
+__global__ void k_empty_offsets(Call c, int64_t* out_offsets, int64_t* id_base) {
+  const int64_t b = id_base ? id_base[0] : 0;
   for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s <= c.S; s += (int64_t)gridDim.x * blockDim.x)
-    out_offsets[s] = 0;
+    out_offsets[s] = b;
+  if (id_base && blockIdx.x == 0 && threadIdx.x == 0) id_base[1] = b;
 }
 
 }  // namespace tk
@@ -1832,6 +1915,9 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
   ws->num_sms = tok->num_sms;
   cudaSetDevice(tok->device);
   const int64_t nb = std::max<int64_t>(max_bytes, 1);
+  // arrays indexed by global position: a pipelined call's batches sit up to
+  // 16 bytes per batch (plus alignment) past their offset in the text
+  const int64_t nbp = nb + 16 * (tk_workspace::PIPE_MAX + 2) + 2;
   const int64_t n_split_tiles = (nb + TILE - 1) / TILE + 1;
   const int64_t n_scan_tiles = (nb + 1 + SCAN_TILE - 1) / SCAN_TILE + 1;
   const int64_t cut_words = (nb + 64) / 32 + 1;
@@ -1852,9 +1938,9 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.pbits, sizeof(uint32_t) * cut_words},
       {(void**)&w.sbits, sizeof(uint32_t) * cut_words},
       {(void**)&w.tile_first, sizeof(uint32_t) * n_split_tiles},
-      {(void**)&w.cnt, sizeof(uint32_t) * (nb + 2)},
-      {(void**)&w.offs, sizeof(uint32_t) * (nb + 2)},
-      {(void**)&w.arena, sizeof(int32_t) * (nb + 2)},
+      {(void**)&w.cnt, sizeof(uint32_t) * nbp},
+      {(void**)&w.offs, sizeof(uint32_t) * nbp},
+      {(void**)&w.arena, sizeof(int32_t) * nbp},
       {(void**)&w.long_list, sizeof(uint32_t) * 2 * (nb / (SHORT_MAX + 1) + 2)},
       {(void**)&w.staging, sizeof(uint32_t) * (size_t)(n_split_tiles * STG)},
       {(void**)&w.tile_count, sizeof(uint32_t) * (n_split_tiles + 1)},
@@ -1862,19 +1948,22 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.tile_meta, sizeof(uint32_t) * (n_split_tiles + 1)},
       {(void**)&w.seg_rel, sizeof(uint32_t) * (max_segments + 2)},
       {(void**)&w.tile_segs, sizeof(uint32_t) * 4 * (n_split_tiles + 1)},
-      {(void**)&w.gsrc, sizeof(uint32_t) * (nb + 2)},
+      {(void**)&w.gsrc, sizeof(uint32_t) * nbp},
       {(void**)&w.dtab, sizeof(unsigned long long) * 2 * ((size_t)1 << DTAB_LOG2)},
       {(void**)&w.big_list, sizeof(uint32_t) * 2 * (nb / (MEDIUM_MAX + 1) + 2)},
-      {(void**)&w.lrk, sizeof(uint32_t) * (nb + 2)},
-      {(void**)&w.lids2, sizeof(uint32_t) * (nb + 2)},
-      {(void**)&w.lrk2, sizeof(uint32_t) * (nb + 2)},
-      {(void**)&w.lsel, (size_t)nb + 2},
-      {(void**)&w.lchg, (size_t)nb + 2},
-      {(void**)&ws->d_stage_text, (size_t)nb + 16},
-      {(void**)&ws->d_stage_off, sizeof(int64_t) * (max_segments + 1)},
+      {(void**)&w.lrk, sizeof(uint32_t) * nbp},
+      {(void**)&w.lids2, sizeof(uint32_t) * nbp},
+      {(void**)&w.lrk2, sizeof(uint32_t) * nbp},
+      {(void**)&w.lsel, (size_t)nbp},
+      {(void**)&w.lchg, (size_t)nbp},
+      {(void**)&w.huge_list, sizeof(uint64_t) * 3 * (nb / HUGE_IDS + 2)},
+      {(void**)&ws->d_stage_text, (size_t)nb + 16 * (tk_workspace::PIPE_MAX + 2)},
+      {(void**)&ws->d_stage_off, sizeof(int64_t) * (max_segments + 1 + tk_workspace::PIPE_MAX)},
       {(void**)&ws->d_stage_allow, (size_t)max_segments + 1},
       {(void**)&ws->d_stage_ids, sizeof(int32_t) * nb},
-      {(void**)&ws->d_stage_offsets, sizeof(int64_t) * (max_segments + 1)},
+      {(void**)&ws->d_stage_offsets, sizeof(int64_t) * (max_segments + 1 + tk_workspace::PIPE_MAX)},
+      {(void**)&ws->d_stage_raw, sizeof(int64_t) * (max_segments + 1 + tk_workspace::PIPE_MAX)},
+      {(void**)&ws->d_pipe_base, sizeof(int64_t) * (tk_workspace::PIPE_MAX + 1)},
   };
   static_assert(sizeof(reqs) / sizeof(reqs[0]) <= tk_workspace::MAX_DEV, "workspace buffer table");
   for (auto& r : reqs) {
@@ -1886,10 +1975,29 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
     }
     ws->dev_mem[ws->n_dev++] = *r.p;
   }
-  if (cudaMallocHost((void**)&ws->h_status, sizeof(Status)) != cudaSuccess) {
+  if (cudaMallocHost((void**)&ws->h_status, sizeof(Status)) != cudaSuccess ||
+      cudaMallocHost((void**)&ws->h_pipe_status, sizeof(Status) * tk_workspace::PIPE_MAX) != cudaSuccess) {
     tk_workspace_free(ws);
     tk_set_error("tk_workspace_create: cudaMallocHost failed");
     return TK_E_NOMEM;
+  }
+  bool ok = cudaStreamCreateWithFlags(&ws->s_h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&ws->s_d2h, cudaStreamNonBlocking) == cudaSuccess;
+  cudaEvent_t* evs[2 * tk_workspace::PIPE_MAX + 1];
+  int ne = 0;
+  evs[ne++] = &ws->ev_start;
+  for (int k = 0; k < tk_workspace::PIPE_MAX; k++) {
+    evs[ne++] = &ws->ev_h2d[k];
+    evs[ne++] = &ws->ev_done[k];
+  }
+  for (int k = 0; k < ne && ok; k++) {
+    ok = cudaEventCreateWithFlags(evs[k], cudaEventDisableTiming) == cudaSuccess;
+    if (ok) ws->n_events = k + 1;
+  }
+  if (!ok) {
+    tk_workspace_free(ws);
+    tk_set_error("tk_workspace_create: stream or event creation failed");
+    return TK_E_CUDA;
   }
   *out = ws;
   return TK_OK;
@@ -1897,19 +2005,29 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
 
 extern "C" void tk_workspace_free(tk_workspace* ws) {
   if (!ws) return;
+  if (ws->s_h2d) cudaStreamSynchronize(ws->s_h2d);
+  if (ws->s_d2h) cudaStreamSynchronize(ws->s_d2h);
   for (int i = 0; i < ws->n_dev; i++) cudaFree(ws->dev_mem[i]);
   if (ws->h_status) cudaFreeHost(ws->h_status);
+  if (ws->h_pipe_status) cudaFreeHost(ws->h_pipe_status);
+  // events in creation order: ev_start, then (ev_h2d[k], ev_done[k]) per batch
+  for (int k = 0; k < ws->n_events; k++)
+    cudaEventDestroy(k == 0 ? ws->ev_start : ((k - 1) % 2 == 0 ? ws->ev_h2d[(k - 1) / 2] : ws->ev_done[(k - 1) / 2]));
+  if (ws->s_h2d) cudaStreamDestroy(ws->s_h2d);
+  if (ws->s_d2h) cudaStreamDestroy(ws->s_d2h);
   delete ws;
 }
 
-// Launches the whole encode on `st` and reads back the status (one sync).
-static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_t* d_text, int64_t n,
+// Launches the whole encode on `st`; the status block stays on the device.
+// id_base: null, or a pipelined batch's slot (see k_seg_offsets).
+static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_t* d_text, int64_t n,
                          const int64_t* d_seg_off, const uint8_t* d_allow, int64_t S, int safe,
-                         int32_t* d_out, int64_t cap, int64_t* d_out_offsets, int64_t* h_n_ids,
-                         cudaStream_t st) {
+                         int32_t* d_out, int64_t cap, int64_t* d_out_offsets, int64_t* id_base,
+                         int64_t gb, cudaStream_t st) {
   Call c;
   c.text = d_text;
   c.n = n;
+  c.gb = gb;
   c.seg_off = d_seg_off;
   c.allow = d_allow;
   c.S = S;
@@ -1923,7 +2041,7 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   const int seg_grid = (int)std::max<int64_t>(1, std::min<int64_t>((S + 256) / 256, (int64_t)sms * 4));
   tk_prof_mark(ws, "k_reset", st);
   k_reset<<<sms * 2, 256, 0, st>>>(ws->w, n_split_tiles + 1, n_scan_tiles, c.safe, cut_words,
-                                   n_split_tiles);
+                                   n_split_tiles, gb == 0 ? 1 : 0);
   tk_prof_mark(ws, "k_check_segments", st);
   k_check_segments<<<seg_grid, 256, 0, st>>>(c);
   if (n > 0) {
@@ -1962,21 +2080,23 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     if (rc) return rc;
     tk_prof_mark(ws, "k_copy_out", st);
     k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * 8), ETHREADS, 0, st>>>(c, d_out, cap);
+    tk_prof_mark(ws, "k_copy_huge", st);
+    k_copy_huge<<<sms * 4, ETHREADS, 0, st>>>(c, d_out, cap);
     tk_prof_mark(ws, "k_seg_offsets", st);
-    k_seg_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets);
+    k_seg_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets, id_base);
   } else {
     tk_prof_mark(ws, "k_empty_offsets", st);
-    k_empty_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets);
+    k_empty_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets, id_base);
   }
   TK_CUDA(cudaGetLastError(), "encode launch");
-  TK_CUDA(cudaMemcpyAsync(ws->h_status, ws->w.status, sizeof(Status), cudaMemcpyDeviceToHost, st),
-          "status copy");
-  TK_CUDA(cudaStreamSynchronize(st), "encode");
-  tk_prof_finish(ws, st);
-  const Status& hs = *ws->h_status;
-  if (h_n_ids) *h_n_ids = hs.n_ids;
+  return TK_OK;
+}
+
+// The outcome recorded in a status block; pos_base shifts error positions
+// (a pipelined batch's first byte).
+static int encode_result(const Status& hs, int64_t cap, int64_t pos_base) {
   if (hs.code == TK_E_UTF8) {
-    tk_set_error("invalid UTF-8 at byte %lld", (long long)hs.err_pos);
+    tk_set_error("invalid UTF-8 at byte %lld", (long long)(hs.err_pos + pos_base));
     return TK_E_UTF8;
   }
   if (hs.code) {
@@ -1988,6 +2108,22 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     return TK_E_CAPACITY;
   }
   return TK_OK;
+}
+
+// Launches the whole encode on `st` and reads back the status (one sync).
+static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_t* d_text, int64_t n,
+                         const int64_t* d_seg_off, const uint8_t* d_allow, int64_t S, int safe,
+                         int32_t* d_out, int64_t cap, int64_t* d_out_offsets, int64_t* h_n_ids,
+                         cudaStream_t st) {
+  int rc = encode_launch(tok, ws, d_text, n, d_seg_off, d_allow, S, safe, d_out, cap, d_out_offsets,
+                         nullptr, 0, st);
+  if (rc) return rc;
+  TK_CUDA(cudaMemcpyAsync(ws->h_status, ws->w.status, sizeof(Status), cudaMemcpyDeviceToHost, st),
+          "status copy");
+  TK_CUDA(cudaStreamSynchronize(st), "encode");
+  tk_prof_finish(ws, st);
+  if (h_n_ids) *h_n_ids = ws->h_status->n_ids;
+  return encode_result(*ws->h_status, cap, 0);
 }
 
 extern "C" int tk_last_stats(const tk_workspace* ws, int64_t* n_pretokens, int64_t* n_ids,
@@ -2032,6 +2168,32 @@ extern "C" int tk_encode_segments(const tk_tokenizer* tok, tk_workspace* ws, con
                        d_out_ids, out_capacity, d_out_offsets, h_n_ids, (cudaStream_t)cuda_stream);
 }
 
+// Batches of a pipelined host call: consecutive segments, about PIPE_TARGET
+// bytes each (at least PIPE_MIN_BYTES), at most PIPE_MAX batches.  Returns
+// the batch count (1: no pipelining) and fills first[k] = the first segment
+// of batch k, first[count] = S.  Offsets that are not a valid table give 1:
+// the one-batch call then reports the error from the device check.
+constexpr int64_t PIPE_MIN_BYTES = 16ll << 20;
+// Start of batch k's text in the staging buffer: 16-byte aligned, after the
+// end of batch k - 1's (which ends below b0 + 16 k).
+static int64_t pipe_text_at(int64_t b0, int k) { return (b0 + 16 * (int64_t)k + 15) & ~(int64_t)15; }
+constexpr int PIPE_TARGET = 6;
+static int plan_batches(const int64_t* seg_off, int64_t S, int64_t n, int64_t* first) {
+  if (S < 2 || n < 2 * PIPE_MIN_BYTES || seg_off[0] != 0 || seg_off[S] != n) return 1;
+  for (int64_t s = 0; s < S; s++)
+    if (seg_off[s + 1] < seg_off[s]) return 1;
+  const int64_t target = std::max<int64_t>(PIPE_MIN_BYTES, (n + PIPE_TARGET - 1) / PIPE_TARGET);
+  int k = 0;
+  first[0] = 0;
+  for (int64_t s = 0; s < S; s++) {
+    // close the batch before segment s when it already holds `target` bytes
+    if (s > first[k] && seg_off[s] - seg_off[first[k]] >= target && k + 1 < tk_workspace::PIPE_MAX)
+      first[++k] = s;
+  }
+  first[k + 1] = S;
+  return k + 1;
+}
+
 extern "C" int tk_encode_segments_host(const tk_tokenizer* tok, tk_workspace* ws, const uint8_t* h_text,
                                        int64_t n_bytes, const int64_t* h_seg_off,
                                        const uint8_t* h_allow_special, int64_t S, int tiktoken_safe,
@@ -2042,20 +2204,98 @@ extern "C" int tk_encode_segments_host(const tk_tokenizer* tok, tk_workspace* ws
   if (rc) return rc;
   cudaSetDevice(ws->device);
   cudaStream_t st = (cudaStream_t)cuda_stream;
-  if (n_bytes) TK_CUDA(cudaMemcpyAsync(ws->d_stage_text, h_text, n_bytes, cudaMemcpyHostToDevice, st), "h2d text");
-  TK_CUDA(cudaMemcpyAsync(ws->d_stage_off, h_seg_off, sizeof(int64_t) * (S + 1), cudaMemcpyHostToDevice, st),
-          "h2d offsets");
-  if (S) TK_CUDA(cudaMemcpyAsync(ws->d_stage_allow, h_allow_special, S, cudaMemcpyHostToDevice, st), "h2d allow");
-  const int64_t dcap = std::min<int64_t>(out_capacity, std::max<int64_t>(ws->w.max_bytes, 1));
-  int64_t n_ids = 0;
-  rc = encode_device(tok, ws, ws->d_stage_text, n_bytes, ws->d_stage_off, ws->d_stage_allow, S,
-                     tiktoken_safe, ws->d_stage_ids, dcap, ws->d_stage_offsets, &n_ids, st);
-  if (h_n_ids) *h_n_ids = n_ids;
-  if (rc) return rc;
-  if (n_ids) TK_CUDA(cudaMemcpyAsync(h_out_ids, ws->d_stage_ids, sizeof(int32_t) * n_ids, cudaMemcpyDeviceToHost, st),
-                     "d2h ids");
-  TK_CUDA(cudaMemcpyAsync(h_out_offsets, ws->d_stage_offsets, sizeof(int64_t) * (S + 1), cudaMemcpyDeviceToHost, st),
-          "d2h offsets");
+  int64_t first[tk_workspace::PIPE_MAX + 1];
+  const int nbat = ws->prof.on ? 1 : plan_batches(h_seg_off, S, n_bytes, first);
+  if (nbat == 1) {
+    if (n_bytes) TK_CUDA(cudaMemcpyAsync(ws->d_stage_text, h_text, n_bytes, cudaMemcpyHostToDevice, st), "h2d text");
+    TK_CUDA(cudaMemcpyAsync(ws->d_stage_off, h_seg_off, sizeof(int64_t) * (S + 1), cudaMemcpyHostToDevice, st),
+            "h2d offsets");
+    if (S) TK_CUDA(cudaMemcpyAsync(ws->d_stage_allow, h_allow_special, S, cudaMemcpyHostToDevice, st), "h2d allow");
+    const int64_t dcap = std::min<int64_t>(out_capacity, std::max<int64_t>(ws->w.max_bytes, 1));
+    int64_t n_ids = 0;
+    rc = encode_device(tok, ws, ws->d_stage_text, n_bytes, ws->d_stage_off, ws->d_stage_allow, S,
+                       tiktoken_safe, ws->d_stage_ids, dcap, ws->d_stage_offsets, &n_ids, st);
+    if (h_n_ids) *h_n_ids = n_ids;
+    if (rc) return rc;
+    if (n_ids) TK_CUDA(cudaMemcpyAsync(h_out_ids, ws->d_stage_ids, sizeof(int32_t) * n_ids, cudaMemcpyDeviceToHost, st),
+                       "d2h ids");
+    TK_CUDA(cudaMemcpyAsync(h_out_offsets, ws->d_stage_offsets, sizeof(int64_t) * (S + 1), cudaMemcpyDeviceToHost, st),
+            "d2h offsets");
+    TK_CUDA(cudaStreamSynchronize(st), "encode (host buffers)");
+    return TK_OK;
+  }
+  // Pipelined: batch k's bytes, segment offsets, flags and ids sit in
+  // disjoint parts of the staging buffers (text and ids at the batch's byte
+  // offset, offsets at first[k] + k).  All copies in go first on s_h2d; the
+  // encodes run in order on st; batch k's ids go out on s_d2h while batch
+  // k + 1 encodes.  The workspace's other buffers serve one batch at a time,
+  // in stream order.
+  TK_CUDA(cudaEventRecord(ws->ev_start, st), "pipeline start");
+  TK_CUDA(cudaStreamWaitEvent(ws->s_h2d, ws->ev_start, 0), "pipeline start");
+  TK_CUDA(cudaStreamWaitEvent(ws->s_d2h, ws->ev_start, 0), "pipeline start");
+  TK_CUDA(cudaMemsetAsync(ws->d_pipe_base, 0, sizeof(int64_t), st), "pipeline base");
+  for (int k = 0; k < nbat; k++) {
+    const int64_t s0 = first[k], s1 = first[k + 1], b0 = h_seg_off[s0], b1 = h_seg_off[s1];
+    if (b1 > b0)
+      TK_CUDA(cudaMemcpyAsync(ws->d_stage_text + pipe_text_at(b0, k), h_text + b0, b1 - b0,
+                              cudaMemcpyHostToDevice, ws->s_h2d), "h2d text");
+    TK_CUDA(cudaMemcpyAsync(ws->d_stage_raw + s0 + k, h_seg_off + s0, sizeof(int64_t) * (s1 - s0 + 1),
+                            cudaMemcpyHostToDevice, ws->s_h2d), "h2d offsets");
+    TK_CUDA(cudaMemcpyAsync(ws->d_stage_allow + s0, h_allow_special + s0, s1 - s0, cudaMemcpyHostToDevice,
+                            ws->s_h2d), "h2d allow");
+    TK_CUDA(cudaEventRecord(ws->ev_h2d[k], ws->s_h2d), "h2d event");
+  }
+  for (int k = 0; k < nbat; k++) {
+    const int64_t s0 = first[k], s1 = first[k + 1], b0 = h_seg_off[s0], b1 = h_seg_off[s1];
+    TK_CUDA(cudaStreamWaitEvent(st, ws->ev_h2d[k], 0), "h2d wait");
+    k_rebase<<<(int)std::min<int64_t>((s1 - s0 + 256) / 256, 64), 256, 0, st>>>(
+        ws->d_stage_raw + s0 + k, ws->d_stage_off + s0 + k, s1 - s0 + 1);
+    rc = encode_launch(tok, ws, ws->d_stage_text + pipe_text_at(b0, k), b1 - b0, ws->d_stage_off + s0 + k,
+                       ws->d_stage_allow + s0, s1 - s0, tiktoken_safe, ws->d_stage_ids + b0,
+                       std::max<int64_t>(b1 - b0, 0), ws->d_stage_offsets + s0 + k, ws->d_pipe_base + k,
+                       pipe_text_at(b0, k), st);
+    if (rc) {
+      cudaStreamSynchronize(st);
+      cudaStreamSynchronize(ws->s_h2d);
+      cudaStreamSynchronize(ws->s_d2h);
+      return rc;
+    }
+    TK_CUDA(cudaMemcpyAsync(&ws->h_pipe_status[k], ws->w.status, sizeof(Status), cudaMemcpyDeviceToHost, st),
+            "status copy");
+    TK_CUDA(cudaEventRecord(ws->ev_done[k], st), "batch event");
+  }
+  // Copies out, batch by batch as each ends (the ids' count is known once the
+  // batch's status arrives).  Everything on s_d2h is enqueued here, after the
+  // host saw the batch end, so no copy waits behind a later batch.
+  int first_rc = TK_OK;
+  int64_t total = 0;
+  Status sum = {};
+  for (int k = 0; k < nbat; k++) {
+    TK_CUDA(cudaEventSynchronize(ws->ev_done[k]), "batch");
+    const Status& hs = ws->h_pipe_status[k];
+    const int64_t s0 = first[k], s1 = first[k + 1];
+    const int64_t b0 = h_seg_off[s0], b1 = h_seg_off[s1];
+    TK_CUDA(cudaMemcpyAsync(h_out_offsets + s0, ws->d_stage_offsets + s0 + k,
+                            sizeof(int64_t) * (s1 - s0 + (k == nbat - 1 ? 1 : 0)), cudaMemcpyDeviceToHost,
+                            ws->s_d2h), "d2h offsets");
+    const int brc = encode_result(hs, std::max<int64_t>(b1 - b0, 0), b0);
+    if (brc && !first_rc) first_rc = brc;
+    sum.n_ptok += hs.n_ptok;
+    sum.n_long += hs.n_long;
+    if (!first_rc && hs.n_ids && total + hs.n_ids <= out_capacity)
+      TK_CUDA(cudaMemcpyAsync(h_out_ids + total, ws->d_stage_ids + b0, sizeof(int32_t) * hs.n_ids,
+                              cudaMemcpyDeviceToHost, ws->s_d2h), "d2h ids");
+    total += hs.n_ids;
+  }
+  TK_CUDA(cudaStreamSynchronize(ws->s_d2h), "encode (host buffers)");
   TK_CUDA(cudaStreamSynchronize(st), "encode (host buffers)");
+  sum.n_ids = total;
+  *ws->h_status = sum;
+  if (h_n_ids) *h_n_ids = total;
+  if (first_rc) return first_rc;
+  if (total > out_capacity) {
+    tk_set_error("output capacity %lld < %lld ids", (long long)out_capacity, (long long)total);
+    return TK_E_CAPACITY;
+  }
   return TK_OK;
 }

@@ -53,6 +53,7 @@ struct Status {
   uint32_t medium_next;
   uint32_t big_next;
   uint32_t dedup_big_next;
+  uint32_t n_huge;       // entries of huge_list
   uint32_t tile_ctr[8];  // dynamic tile counters of the persistent kernels
   int64_t n_tiles;       // split tiles of this call (element count of the tile scan)
 };
@@ -109,6 +110,8 @@ struct Work {
   uint32_t* lrk2;       // [max_bytes] long merge: second rank buffer
   uint8_t* lsel;        // [max_bytes] long merge: selection flags
   uint8_t* lchg;        // [max_bytes] long merge: changed flags
+  uint64_t* huge_list;  // (output position, arena start, id count) of the long pieces
+                        // whose ids the whole grid copies
   int64_t max_bytes;
   int64_t max_segments;
 };
@@ -309,6 +312,15 @@ struct tk_workspace {
   uint8_t* d_stage_allow;
   int32_t* d_stage_ids;
   int64_t* d_stage_offsets;
+  // pipelined host calls: the text is cut at segment boundaries into batches
+  // whose copies in and out overlap the encode of their neighbours
+  static constexpr int PIPE_MAX = 16;
+  cudaStream_t s_h2d, s_d2h;
+  cudaEvent_t ev_start, ev_h2d[PIPE_MAX], ev_done[PIPE_MAX];
+  int n_events;
+  tk::Status* h_pipe_status;  // [PIPE_MAX] pinned
+  int64_t* d_stage_raw;       // segment offsets as copied in, before rebasing
+  int64_t* d_pipe_base;       // [PIPE_MAX + 1] ids before each batch
   int device;
   int num_sms;
 };

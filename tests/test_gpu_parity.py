@@ -258,3 +258,47 @@ def test_long_white_space_walks(full_gpu, full_enc):
     long_run = "q\n" + " " * 60_000 + "<|endoftext|>" + "\n" + " " * 30_000 + "w"
     _compare(full_gpu, full_enc, [(long_run, True)], True)
     _compare(full_gpu, full_enc, [(long_run, True)], False)
+
+
+def test_host_buffer_pipelined(full_table, full_enc):
+    """A host call large enough to be cut into batches at segment boundaries:
+    ids and offsets equal the one-shot device call's, sampled segments equal
+    the oracle's, and errors keep their whole-call meaning."""
+    import byte_level_bpe_gb300 as tk
+    text, off = workloads.serving_batch(full_table, seed=11, total=40 << 20, n_req=600)
+    segs = []
+    for r in range(len(off) - 1):
+        body = text[off[r]:off[r + 1]].tobytes()
+        if r % 7 == 0:
+            body = b"<|endoftext|>" + body
+        segs.append((body, r % 2 == 0))
+    h_text, h_off, h_allow = workloads.pack_segments(segs)
+    gpu = tk.Tokenizer(full_table, workloads.SPECIALS, max_bytes=len(h_text), max_segments=len(segs))
+    ids_h, off_h = gpu.encode_host(np.ascontiguousarray(h_text), h_off, h_allow, tiktoken_safe=True)
+    ids_d, off_d = gpu.encode_device(torch.from_numpy(h_text).cuda(), torch.from_numpy(h_off).cuda(),
+                                     torch.from_numpy(h_allow).cuda(), tiktoken_safe=True)
+    assert np.array_equal(off_h, off_d.cpu().numpy())
+    assert np.array_equal(ids_h, ids_d.cpu().numpy())
+    rng = np.random.default_rng(1)
+    for r in sorted(set(rng.choice(len(segs), size=12, replace=False).tolist()) | {0, len(segs) - 1}):
+        o_ids, _ = full_enc.encode_segments([segs[r]], tiktoken_safe=True)
+        assert np.array_equal(ids_h[off_h[r]:off_h[r + 1]], o_ids), r
+    # an invalid byte late in the text: reported at its position in the whole call
+    bad = h_text.copy()
+    pos = int(h_off[len(segs) - 3]) + 5
+    bad[pos] = 0xFF
+    with pytest.raises(tk.TkError) as ei:
+        gpu.encode_host(bad, h_off, h_allow, tiktoken_safe=True)
+    assert ei.value.code == tk.native.TK_E_UTF8 and f"byte {pos}" in str(ei.value)
+    # too small an output: the capacity error carries the full count
+    out = np.empty(len(ids_h) - 1, np.int32)
+    out_off = np.empty(len(segs) + 1, np.int64)
+    rc, n = tk.native.tk_encode_segments_host(
+        gpu.handle, gpu.workspace, h_text.ctypes.data, len(h_text), h_off.ctypes.data,
+        h_allow.ctypes.data, len(segs), 1, out.ctypes.data, out.size, out_off.ctypes.data,
+        torch.cuda.current_stream().cuda_stream, raise_on_error=False)
+    assert rc == tk.native.TK_E_CAPACITY and n == len(ids_h)
+    # and the workspace still encodes correctly afterwards
+    ids2, off2 = gpu.encode_host(np.ascontiguousarray(h_text), h_off, h_allow, tiktoken_safe=True)
+    assert np.array_equal(ids2, ids_h) and np.array_equal(off2, off_h)
+    gpu.close()
