@@ -845,38 +845,6 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
 // token r (rank = id), so the parts loop never touches bytes after its first
 // round ("Inside encode: a parts vector and a linear scan").
 
-// The parts loop of one pre-token of n <= SHORT_MAX bytes in one thread: the
-// first round reads the dense two-byte table, later rounds the pair table;
-// the leftmost minimum merges and only its two neighbours are re-ranked.
-// Returns the number of ids written to out.
-__device__ __forceinline__ int merge_thread(const Tables& T, const uint8_t* b, int n, int32_t* out) {
-  uint32_t ids[SHORT_MAX], rk[SHORT_MAX];
-  uint32_t prevb = b[0];
-  ids[0] = __ldg(&T.byte_id[prevb]);
-  for (int i = 1; i < n; i++) {
-    const uint32_t x = b[i];
-    ids[i] = __ldg(&T.byte_id[x]);
-    rk[i - 1] = __ldg(&T.dense[(prevb << 8) | x]);
-    prevb = x;
-  }
-  rk[n - 1] = RANK_MAX;
-  int m = n;
-  while (m > 1) {
-    uint32_t best = RANK_MAX;
-    int bi = -1;
-    for (int i = 0; i + 1 < m; i++)
-      if (rk[i] < best) { best = rk[i]; bi = i; }
-    if (best == RANK_MAX) break;
-    ids[bi] = best;
-    for (int i = bi + 1; i + 1 < m; i++) { ids[i] = ids[i + 1]; rk[i] = rk[i + 1]; }
-    m--;
-    rk[bi] = (bi + 1 < m) ? pair_rank(T, ids[bi], ids[bi + 1]) : RANK_MAX;
-    if (bi > 0) rk[bi - 1] = pair_rank(T, ids[bi - 1], ids[bi]);
-  }
-  for (int i = 0; i < m; i++) out[i] = (int32_t)ids[i];
-  return m;
-}
-
 // The same loop for a pre-token of n <= W bytes with every array in
 // registers: fully unrolled, dynamic positions handled by predicated selects.
 // b must have W readable bytes.
@@ -991,49 +959,21 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
 
 // Length class of a pre-token for the tile's work list (warps then run
 // pieces of one class together).
-constexpr int N_CLASSES = 7;  // 1, 2, 3, 4, 5-8, 9-16, 17-64 bytes
+constexpr int N_CLASSES = 6;  // 1, 2, 3, 4, 5-8, 9-16 bytes
 __device__ __forceinline__ int len_class(int n) {
-  return n <= 4 ? n - 1 : n <= 8 ? 4 : n <= 16 ? 5 : 6;
-}
-
-// The loop for one pre-token of up to SHORT_MAX bytes on caller-provided
-// shared scratch (ids, rk of SHORT_MAX entries each).
-__device__ __noinline__ int merge_scratch(const MergeTabs T, const uint8_t* b, int n, uint32_t* ids, uint32_t* rk,
-                             int32_t* out) {
-  uint32_t prevb = b[0];
-  ids[0] = __ldg(&T.byte_id[prevb]);
-  for (int i = 1; i < n; i++) {
-    const uint32_t x = b[i];
-    ids[i] = __ldg(&T.byte_id[x]);
-    rk[i - 1] = dense_rank(T, prevb, x);
-    prevb = x;
-  }
-  rk[n - 1] = RANK_MAX;
-  int m = n;
-  while (m > 1) {
-    uint32_t best = RANK_MAX;
-    int bi = -1;
-    for (int i = 0; i + 1 < m; i++) {
-      const uint32_t r = rk[i];
-      if (r < best) { best = r; bi = i; }
-    }
-    if (best == RANK_MAX) break;
-    ids[bi] = best;
-    for (int i = bi + 1; i + 1 < m; i++) { ids[i] = ids[i + 1]; rk[i] = rk[i + 1]; }
-    m--;
-    rk[bi] = (bi + 1 < m) ? pair_rank(T, ids[bi], ids[bi + 1]) : RANK_MAX;
-    if (bi > 0) rk[bi - 1] = pair_rank(T, ids[bi - 1], ids[bi]);
-  }
-  for (int i = 0; i < m; i++) out[i] = (int32_t)ids[i];
-  return m;
+  return n <= 4 ? n - 1 : n <= 8 ? 4 : 5;
 }
 
 // The group that runs one round merge: NW warps (NW = 1: one warp, no block
 // barriers; else the whole CTA).  s64 / s32 are shared scratch of NW entries.
 template <int NW>
 struct RGroup {
+  static constexpr int kWarps = NW;
   int64_t* s64;
   uint32_t* s32;
+  // the group's threads share one L1: plain loads see each other's stores
+  template <class T>
+  __device__ T ld(const T* p) const { return *p; }
   __device__ int warp() const { return NW == 1 ? 0 : (int)(threadIdx.x >> 5); }
   __device__ void sync() const {
     if (NW == 1) __syncwarp();
@@ -1072,13 +1012,95 @@ struct RGroup {
   }
 };
 
+// Thread-block cluster primitives (inline PTX): rank in the cluster, the
+// cluster-wide barrier (release / acquire at cluster scope), and loads from
+// another CTA's shared memory.
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cl_map(const void* p, uint32_t rank) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_ld32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int64_t cl_ld64(uint32_t a) {
+  int64_t v;
+  asm volatile("ld.shared::cluster.s64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// The round-merge group of a whole cluster of CL 1024-thread CTAs (one piece
+// spread over CL SMs).  Reductions go through each CTA's shared memory and
+// distributed shared memory; the merge buffers are read through L2 (.cg),
+// since the CTAs sit on different SMs.  s64 / s32: 33 entries per CTA.
+template <int CL>
+struct CGroup {
+  static constexpr int kWarps = CL * 32;
+  int64_t* s64;
+  uint32_t* s32;
+  uint32_t rank;
+  __device__ int warp() const { return (int)(rank * 32 + (threadIdx.x >> 5)); }
+  __device__ void sync() const { cl_sync(); }
+  template <class T>
+  __device__ T ld(const T* p) const { return __ldcg(p); }
+  __device__ uint32_t gmin(uint32_t v) const {
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) s32[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      uint32_t u = s32[threadIdx.x];
+      for (int o = 16; o > 0; o >>= 1) u = min(u, __shfl_xor_sync(0xffffffffu, u, o));
+      if (threadIdx.x == 0) s32[32] = u;
+    }
+    cl_sync();
+    uint32_t r = 0xFFFFFFFFu;
+    for (int k = 0; k < CL; k++) r = min(r, cl_ld32(cl_map(&s32[32], (uint32_t)k)));
+    cl_sync();
+    return r;
+  }
+  __device__ int64_t warp_excl(int64_t wv, int op, int64_t* total) const {
+    const int64_t idv = op ? INT64_MIN : 0;
+    const int wl = (int)(threadIdx.x >> 5);
+    if ((threadIdx.x & 31) == 0) s64[wl] = wv;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int64_t t = idv;
+      for (int k = 0; k < 32; k++) t = op ? max(t, s64[k]) : t + s64[k];
+      s64[32] = t;
+    }
+    cl_sync();
+    int64_t e = idv, t = idv;
+    for (int k = 0; k < wl; k++) e = op ? max(e, s64[k]) : e + s64[k];
+    for (int r = 0; r < CL; r++) {
+      const int64_t v = cl_ld64(cl_map(&s64[32], (uint32_t)r));
+      if (r < (int)rank) e = op ? max(e, v) : e + v;
+      t = op ? max(t, v) : t + v;
+    }
+    cl_sync();
+    *total = t;
+    return e;
+  }
+};
+
 // Exact round merge of the pre-token text[s .. s+n) by a group (see the file
 // header).  Each warp owns a contiguous chunk of the parts and its lanes take
 // consecutive parts, so every pass reads and writes coalesced.  Works in the
 // workspace at the piece's byte offset; the ids end in arena[s ..].  Returns
 // the number of ids.
-template <int NW>
-__device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, int64_t n) {
+template <class Grp>
+__device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t n) {
+  constexpr int NW = Grp::kWarps;
   const int64_t G = c.gb + s;
   uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + G);
   uint32_t* A_rk = c.W.lrk + G;
@@ -1101,24 +1123,27 @@ __device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, i
     const int64_t wlo = min(n, (int64_t)w * cw), whi = min(n, wlo + cw);
     // (1) the minimum pair rank
     uint32_t m = RANK_MAX;
-    for (int64_t i = wlo + lane; i < whi; i += 32) m = min(m, A_rk[i]);
+#pragma unroll 4
+    for (int64_t i = wlo + lane; i < whi; i += 32) m = min(m, g.ld(&A_rk[i]));
     const uint32_t rs = g.gmin(m);
     if (rs == RANK_MAX) break;
     // (2) chains of rs-pairs: every other pair from each chain's start.  The
     //     last non-candidate before each part comes from ballots and a carry.
     int64_t ln_w = -1;
+#pragma unroll 4
     for (int64_t b = wlo; b < whi; b += 32) {
       const int64_t i = b + lane;
-      const uint32_t nm = __ballot_sync(0xffffffffu, i < whi && A_rk[i] != rs);
+      const uint32_t nm = __ballot_sync(0xffffffffu, i < whi && g.ld(&A_rk[i]) != rs);
       if (nm) ln_w = b + 31 - __clz(nm);
     }
     int64_t tot;
     int64_t carry = g.warp_excl(ln_w, 1, &tot);
     if (carry < -1) carry = -1;
+#pragma unroll 4
     for (int64_t b = wlo; b < whi; b += 32) {
       const int64_t i = b + lane;
       const bool in = i < whi;
-      const bool cand = in && A_rk[i] == rs;
+      const bool cand = in && g.ld(&A_rk[i]) == rs;
       const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
       const uint32_t before = nm & lt;
       const int64_t ln = before ? b + 31 - __clz(before) : carry;
@@ -1131,12 +1156,12 @@ __device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, i
     for (int64_t b = wlo; b < whi && fb == 0xFFFFFFFFu; b += 32) {
       const int64_t i = b + lane;
       bool bad = false;
-      if (i < whi && sel[i]) {
+      if (i < whi && g.ld(&sel[i])) {
         if (i >= 1) {
-          const uint32_t left = (i >= 2 && sel[i - 2]) ? rs : A_ids[i - 1];
+          const uint32_t left = (i >= 2 && g.ld(&sel[i - 2])) ? rs : g.ld(&A_ids[i - 1]);
           bad = pair_rank(c.T, left, rs) < rs;
         }
-        if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, A_ids[i + 2]) < rs;
+        if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, g.ld(&A_ids[i + 2])) < rs;
       }
       const uint32_t bm = __ballot_sync(0xffffffffu, bad);
       if (bm) fb = (uint32_t)(b + __ffs(bm) - 1);
@@ -1144,31 +1169,34 @@ __device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, i
     const uint32_t limit = g.gmin(fb);
     // (4) merge the selected pairs up to limit, compacting into B
     int64_t keep_w = 0;
+#pragma unroll 4
     for (int64_t b = wlo; b < whi; b += 32) {
       const int64_t i = b + lane;
-      const bool kp = i < whi && !(i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit);
+      const bool kp = i < whi && !(i >= 1 && g.ld(&sel[i - 1]) && (uint64_t)(i - 1) <= (uint64_t)limit);
       keep_w += __popc(__ballot_sync(0xffffffffu, kp));
     }
     int64_t dst = g.warp_excl(keep_w, 0, &tot);
     const int64_t n2 = tot;
+#pragma unroll 4
     for (int64_t b = wlo; b < whi; b += 32) {
       const int64_t i = b + lane;
-      const bool kp = i < whi && !(i >= 1 && sel[i - 1] && (uint64_t)(i - 1) <= (uint64_t)limit);
+      const bool kp = i < whi && !(i >= 1 && g.ld(&sel[i - 1]) && (uint64_t)(i - 1) <= (uint64_t)limit);
       const uint32_t km = __ballot_sync(0xffffffffu, kp);
       if (kp) {
         const int64_t pos = dst + __popc(km & lt);
-        const bool merged = sel[i] && (uint64_t)i <= (uint64_t)limit;
-        B_ids[pos] = merged ? rs : A_ids[i];
-        B_rk[pos] = A_rk[i];
+        const bool merged = g.ld(&sel[i]) && (uint64_t)i <= (uint64_t)limit;
+        B_ids[pos] = merged ? rs : g.ld(&A_ids[i]);
+        B_rk[pos] = g.ld(&A_rk[i]);
         chg[pos] = merged;
       }
       dst += __popc(km);
     }
     g.sync();
     // (5) re-rank the pairs next to merged pieces
+#pragma unroll 4
     for (int64_t q = (int64_t)w * 32 + lane; q < n2; q += NW * 32) {
       if (q + 1 >= n2) B_rk[q] = RANK_MAX;
-      else if (chg[q] || chg[q + 1]) B_rk[q] = pair_rank(c.T, B_ids[q], B_ids[q + 1]);
+      else if (g.ld(&chg[q]) || g.ld(&chg[q + 1])) B_rk[q] = pair_rank(c.T, g.ld(&B_ids[q]), g.ld(&B_ids[q + 1]));
     }
     g.sync();
     uint32_t* t1 = A_ids; A_ids = B_ids; B_ids = t1;
@@ -1183,7 +1211,7 @@ __device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, i
   }
   if (in_b) {
     uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + G);
-    for (int64_t i = (int64_t)w * 32 + lane; i < n; i += NW * 32) dst[i] = A_ids[i];
+    for (int64_t i = (int64_t)w * 32 + lane; i < n; i += NW * 32) dst[i] = g.ld(&A_ids[i]);
     g.sync();
   }
   return n;
@@ -1198,11 +1226,13 @@ __device__ int64_t merge_rounds(const Call& c, const RGroup<NW>& g, int64_t s, i
 constexpr int ETHREADS = 256;
 constexpr int EPAD = 96;                 // bytes loaded past the tile (short pieces, specials)
 constexpr int MEDIUM_MAX = 1024;
+constexpr int64_t CLUSTER_MIN = 32768;   // longer pieces merge on a CTA cluster
+constexpr int MERGE_CL = 8;              // CTAs per cluster (portable size)
 constexpr int MAX_GP = TILE / (SHORT_MAX + 1) + 2;  // pieces merged through global memory
 constexpr int REG_MAX = 16;  // pieces up to this length merge in registers
 constexpr uint32_t NO_START = 0xFFFFFFFFu;
 constexpr int64_t STG = TILE + SHORT_MAX + 8;       // staging slot per tile (u32 entries)
-constexpr uint32_t DTAB_LOG2 = 18;                  // dedup table of long pieces: 2^18 slots
+constexpr uint32_t DTAB_LOG2 = 20;                  // dedup table of long pieces: 2^20 slots
 
 struct GPiece {
   uint32_t rel;  // start in the tile
@@ -1220,8 +1250,6 @@ struct EncSmem {
   uint32_t cls_cnt[16];                 // work list: class starts [0..N], then fill cursors
   int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
   int32_t outs[TILE + SHORT_MAX];       // work list (x | len << 16), then compacted ids
-  uint32_t scr_ids[ETHREADS / 32][SHORT_MAX];  // per-warp scratch for 17..64-byte pieces
-  uint32_t scr_rk[ETHREADS / 32][SHORT_MAX];
   GPiece gp[MAX_GP];
   uint32_t th_full[ETHREADS];
   uint32_t th_short[ETHREADS];
@@ -1339,7 +1367,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
         sm.plen[x] = (uint8_t)len;
         atomicAdd(&sm.cls_cnt[len_class((int)len)], 1u);
       } else {
-        // merged earlier by k_merge_big / k_merge_medium: ids in the arena, count in cnt[]
+        // merged earlier (k_merge_medium / _big / _cluster): ids in the arena, count in cnt[]
         const int g = atomicAdd(&sm.n_gp, 1);
         const uint32_t src = c.W.gsrc[c.gb + t0 + x];
         sm.gp[g] = GPiece{(uint32_t)x, src, c.W.cnt[src], 0u, 0u};
@@ -1369,14 +1397,12 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     }
     __syncthreads();
     // 2b. the list, class by class (class k is list[cls_cnt[k] .. cls_cnt[k + 1])).
-    //     One and two bytes: four
-    //     pieces per thread at a time; three bytes: two at a time; up to 16
-    //     bytes: the register loop; 17..64 bytes: one warp each (its first
-    //     lane, on the warp's shared scratch).
+    //     One and two bytes: four pieces per thread at a time; three bytes:
+    //     two at a time; 4..16 bytes: the register loop.
     {
       const MergeTabs MT(c.T);
       const uint32_t e0 = sm.cls_cnt[1], e1 = sm.cls_cnt[2], e2 = sm.cls_cnt[3];
-      const uint32_t e5 = sm.cls_cnt[6], e6 = sm.cls_cnt[7];
+      const uint32_t e5 = sm.cls_cnt[N_CLASSES];
       for (uint32_t i = tid; i < e0; i += 4 * ETHREADS) {
         uint32_t x[4], v[4];
 #pragma unroll
@@ -1430,15 +1456,6 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
         const uint32_t ent = list[i];
         const int x = ent & 0xFFFF, len = ent >> 16;
         sm.cnt[x] = (uint8_t)merge_small(MT, &sm.text[x], len, &sm.stage[x]);
-      }
-      for (uint32_t i = e5 + warp; i < e6; i += ETHREADS / 32) {
-        if (lane == 0) {
-          const uint32_t ent = list[i];
-          const int x = ent & 0xFFFF, len = ent >> 16;
-          sm.cnt[x] = (uint8_t)merge_scratch(MT, &sm.text[x], len, sm.scr_ids[warp], sm.scr_rk[warp],
-                                             &sm.stage[x]);
-        }
-        __syncwarp();
       }
     }
     __syncthreads();
@@ -1569,13 +1586,23 @@ __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int
     }
     for (int i = tid; i < 4 * ngp; i += blockDim.x) s_gp[i] = slot[STG - 4 * ngp + i];
     __syncthreads();
-    for (uint32_t q = tid; q < n_short; q += blockDim.x) {
-      uint64_t pos = base + q;
-      for (int g = 0; g < ngp; g++) {
-        const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
-        if (e[0] <= q) pos += e[3];
+    for (uint32_t q0 = 0; q0 < n_short; q0 += COPY_UNROLL * ETHREADS) {
+      uint32_t v[COPY_UNROLL];
+#pragma unroll
+      for (int k = 0; k < COPY_UNROLL; k++) {
+        const uint32_t q = q0 + k * ETHREADS + tid;
+        v[k] = q < n_short ? __ldcs(slot + q) : 0u;
       }
-      if (pos < (uint64_t)cap) out[pos] = (int32_t)__ldcs(slot + q);
+#pragma unroll
+      for (int k = 0; k < COPY_UNROLL; k++) {
+        const uint32_t q = q0 + k * ETHREADS + tid;
+        if (q >= n_short) continue;
+        // short id q follows every long piece whose short prefix is <= q
+        uint64_t pos = base + q;
+        for (int g = 0; g < ngp; g++)
+          if (s_gp[4 * g] <= q) pos += s_gp[4 * g + 3];
+        if (pos < (uint64_t)cap) out[pos] = (int32_t)v[k];
+      }
     }
     for (int g = 0; g < ngp; g++) {
       const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
@@ -1665,10 +1692,28 @@ __device__ int64_t piece_end(const Call& c, int64_t p, int64_t ntiles) {
   return c.n;
 }
 
-// Pre-tokens longer than SHORT_MAX bytes -> two work lists (medium: one warp
-// each, long: one CTA each), as (start, length) pairs.  One thread per word of
-// the start bitmap: a start with another start later in the same word is
-// short; for the word's last start the next three words decide.
+// Pre-tokens longer than SHORT_MAX bytes -> three work lists (medium: one warp
+// each, big: one CTA each, longest: one CTA cluster each), as (start, length)
+// pairs.  One thread per word of the start bitmap: a start's length is the
+// distance to the next start in the word; for the word's last start the next
+// words decide.
+__device__ __forceinline__ void list_long(const Call& c, int64_t p, int64_t len) {
+  if (c.T.n_spec && bit_get(c.W.sbits, p)) return;  // specials are one id
+  if (len <= MEDIUM_MAX) {
+    const uint32_t k = atomicAdd(&c.W.status->n_medium, 1u);
+    c.W.long_list[2 * k] = (uint32_t)p;
+    c.W.long_list[2 * k + 1] = (uint32_t)len;
+  } else if (len <= CLUSTER_MIN) {
+    const uint32_t k = atomicAdd(&c.W.status->n_biglong, 1u);
+    c.W.big_list[2 * k] = (uint32_t)p;
+    c.W.big_list[2 * k + 1] = (uint32_t)len;
+  } else {
+    const uint32_t k = atomicAdd(&c.W.status->n_cl, 1u);
+    c.W.cl_list[2 * k] = (uint32_t)p;
+    c.W.cl_list[2 * k + 1] = (uint32_t)len;
+  }
+}
+
 __global__ void k_find_long(Call c) {
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const int64_t nwords = (c.n + 31) >> 5;
@@ -1678,8 +1723,29 @@ __global__ void k_find_long(Call c) {
     if ((wi << 5) + 32 > c.n) bits &= (1u << (c.n - (wi << 5))) - 1u;
     if (!bits) continue;
     const int last = 31 - __clz(bits);
+    // starts followed by another start within SHORT_MAX (= 16) bytes, from
+    // this word and the next (the text end counts as a start)
+    uint64_t w = bits;
+    if ((wi << 5) + 32 < c.n) {
+      uint32_t nx = c.W.pbits[wi + 1];
+      if ((wi << 5) + 64 > c.n) nx |= ~((1u << (c.n - (wi << 5) - 32)) - 1u);
+      w |= (uint64_t)nx << 32;
+    } else {
+      w |= ~0ull << (c.n - (wi << 5));
+    }
+    static_assert(SHORT_MAX == 16, "the shift ladder below covers 16 positions");
+    uint64_t near = w >> 1;  // near = OR of w >> d for d = 1 .. 16
+    near |= near >> 1;
+    near |= near >> 2;
+    near |= near >> 4;
+    near |= near >> 8;
+    for (uint32_t bb = bits & ~(1u << last) & ~(uint32_t)near; bb; bb &= bb - 1) {
+      const int x = __ffs(bb) - 1;
+      const uint32_t later = bits & ~((2u << x) - 1u);
+      list_long(c, (wi << 5) + x, __ffs(later) - 1 - x);
+    }
     const int64_t p = (wi << 5) + last;
-    // next start within SHORT_MAX bytes after p?
+    // the last start: is there another start within SHORT_MAX bytes?
     bool short_piece = false;
     for (int k = 1; k <= 3 && !short_piece; k++) {
       const int64_t w2 = wi + k;
@@ -1690,18 +1756,8 @@ __global__ void k_find_long(Call c) {
       else if ((w2 << 5) + 32 - p > SHORT_MAX) break;
     }
     if (short_piece) continue;
-    if (c.T.n_spec && bit_get(c.W.sbits, p)) continue;  // specials are one id
     const int64_t e = piece_end(c, p, ntiles);
-    if (e - p <= SHORT_MAX) continue;
-    if (e - p <= MEDIUM_MAX) {
-      const uint32_t k = atomicAdd(&c.W.status->n_medium, 1u);
-      c.W.long_list[2 * k] = (uint32_t)p;
-      c.W.long_list[2 * k + 1] = (uint32_t)(e - p);
-    } else {
-      const uint32_t k = atomicAdd(&c.W.status->n_biglong, 1u);
-      c.W.big_list[2 * k] = (uint32_t)p;
-      c.W.big_list[2 * k + 1] = (uint32_t)(e - p);
-    }
+    if (e - p > SHORT_MAX) list_long(c, p, e - p);
   }
 }
 
@@ -1806,14 +1862,15 @@ __global__ void __launch_bounds__(1024) k_dedup_big(Call c) {
   __shared__ uint64_t s_word;
   __shared__ uint32_t s_idx;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t n_big = c.W.status->n_biglong;
+  const uint32_t n_big = c.W.status->n_biglong, n_cl = c.W.status->n_cl;
   for (;;) {
     if (tid == 0) s_idx = atomicAdd(&c.W.status->dedup_big_next, 1u);
     __syncthreads();
     const uint32_t k = s_idx;
     __syncthreads();
-    if (k >= n_big) break;
-    const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
+    if (k >= n_big + n_cl) break;
+    const uint32_t* ent = k < n_big ? &c.W.big_list[2 * k] : &c.W.cl_list[2 * (k - n_big)];
+    const int64_t p = ent[0], len = ent[1];
     uint64_t h = hash_part(c, p, len, tid, blockDim.x);
     for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
     if (lane == 0) s_red[warp] = h;
@@ -1832,9 +1889,81 @@ __global__ void __launch_bounds__(1024) k_dedup_big(Call c) {
   }
 }
 
+// The parts loop of one pre-token of SMALL_WARP_MAX bytes or fewer on one
+// warp, in registers: element i sits in lane i % 32, slot i / 32 (K slots).
+// Each step takes the leftmost pair of least rank by a warp reduction of
+// (rank << 6 | position), merges it, shifts the later elements down one
+// place, and looks up the two new neighbour pairs in two lanes at once.
+// ids -> dst[0 ..]; returns the count.
+constexpr int SMALL_WARP_MAX = 64;
+template <int K>
+__device__ int merge_warp(const Call& c, int64_t s, int n, uint32_t* dst) {
+  static_assert(K == 1 || K == 2, "one or two elements per lane");
+  const int lane = threadIdx.x & 31;
+  constexpr uint32_t NOKEY = 0xFFFFFFFFu;
+  uint32_t id[K], rk[K];
+#pragma unroll
+  for (int k = 0; k < K; k++) {
+    const int i = 32 * k + lane;
+    const uint32_t b = gbyte(c, s + i);
+    id[k] = i < n ? __ldg(&c.T.byte_id[b]) : 0u;
+    rk[k] = (i + 1 < n) ? __ldg(&c.T.dense[(b << 8) | gbyte(c, s + i + 1)]) : RANK_MAX;
+  }
+  int m = n;
+  for (int step = 0; step < n; step++) {
+    uint32_t key = NOKEY;
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+      const int i = 32 * k + lane;
+      if (i + 1 < m && rk[k] != RANK_MAX) key = min(key, (rk[k] << 6) | (uint32_t)i);
+    }
+    for (int o = 16; o > 0; o >>= 1) key = min(key, __shfl_xor_sync(0xffffffffu, key, o));
+    if (key == NOKEY) break;
+    const uint32_t rs = key >> 6;
+    const int j = (int)(key & 63);
+    // element j becomes rs; elements after j move down one place
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+      const uint32_t nid = __shfl_down_sync(0xffffffffu, id[k], 1);
+      const uint32_t nrk = __shfl_down_sync(0xffffffffu, rk[k], 1);
+      const uint32_t wid = (k + 1 < K) ? __shfl_sync(0xffffffffu, id[(k + 1) % K], 0) : 0u;
+      const uint32_t wrk = (k + 1 < K) ? __shfl_sync(0xffffffffu, rk[(k + 1) % K], 0) : RANK_MAX;
+      const int i = 32 * k + lane;
+      if (i > j) {
+        id[k] = lane == 31 ? wid : nid;
+        rk[k] = lane == 31 ? wrk : nrk;
+      } else if (i == j) {
+        id[k] = rs;
+      }
+    }
+    m--;
+    // neighbours of the new element: j - 1 and j + 1 (after the shift)
+    const int jl = j - 1, jr = j + 1;
+    const uint32_t idl = jl >= 0 ? __shfl_sync(0xffffffffu, (K == 2 && jl >= 32) ? id[K - 1] : id[0], jl & 31) : 0u;
+    const uint32_t idr = jr < m ? __shfl_sync(0xffffffffu, (K == 2 && jr >= 32) ? id[K - 1] : id[0], jr & 31) : 0u;
+    const bool do_l = jl >= 0 && lane == (jl & 31);
+    const bool do_r = lane == (j & 31);
+    // one call site, so the two lanes' lookups run together (ranks < 2^20)
+    uint32_t r = RANK_MAX;
+    if (do_l || (do_r && jr < m)) r = pair_rank(c.T, do_l ? idl : rs, do_l ? rs : idr);
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+      if (do_l && 32 * k + lane == jl) rk[k] = r;
+      if (do_r && 32 * k + lane == j) rk[k] = r;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < K; k++) {
+    const int i = 32 * k + lane;
+    if (i < m) dst[i] = id[k];
+  }
+  return m;
+}
+
 // Merges the listed pieces that are the first of their kind (see the word
 // cache above).  k_merge_big: one 1024-thread CTA per piece over MEDIUM_MAX
-// bytes; k_merge_medium: one warp per piece of SHORT_MAX+1..MEDIUM_MAX bytes.
+// bytes; k_merge_medium: one warp per piece of SHORT_MAX+1..MEDIUM_MAX bytes
+// (in registers up to SMALL_WARP_MAX bytes, else the round merge).
 // ids -> arena[start ..], count -> cnt[start].
 constexpr int BIG_THREADS = 1024;
 __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
@@ -1856,6 +1985,28 @@ __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
   }
 }
 
+// k_merge_cluster: one cluster of MERGE_CL 1024-thread CTAs per piece over
+// CLUSTER_MIN bytes; rank 0 takes the next piece and shares it through
+// distributed shared memory.
+__global__ void __cluster_dims__(MERGE_CL, 1, 1) __launch_bounds__(BIG_THREADS, 1) k_merge_cluster(Call c) {
+  __shared__ int64_t s64[33];
+  __shared__ uint32_t s32[33];
+  __shared__ uint32_t s_idx;
+  const uint32_t rank = cl_rank();
+  const uint32_t n_cl = c.W.status->n_cl;
+  for (;;) {
+    if (rank == 0 && threadIdx.x == 0) s_idx = atomicAdd(&c.W.status->cl_next, 1u);
+    cl_sync();
+    const uint32_t k = cl_ld32(cl_map(&s_idx, 0));
+    cl_sync();
+    if (k >= n_cl) break;
+    const int64_t p = c.W.cl_list[2 * k], len = c.W.cl_list[2 * k + 1];
+    if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
+    const int64_t m = merge_rounds(c, CGroup<MERGE_CL>{s64, s32, rank}, p, len);
+    if (rank == 0 && threadIdx.x == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
+  }
+}
+
 __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
   const int lane = threadIdx.x & 31;
   const uint32_t n_med = c.W.status->n_medium;
@@ -1866,7 +2017,11 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
     if (k >= n_med) break;
     const int64_t p = c.W.long_list[2 * k], len = c.W.long_list[2 * k + 1];
     if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
-    const int64_t m = merge_rounds(c, RGroup<1>{nullptr, nullptr}, p, len);
+    int64_t m;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + c.gb + p);
+    if (len <= 32) m = merge_warp<1>(c, p, (int)len, dst);
+    else if (len <= SMALL_WARP_MAX) m = merge_warp<2>(c, p, (int)len, dst);
+    else m = merge_rounds(c, RGroup<1>{nullptr, nullptr}, p, len);
     if (lane == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
   }
 }
@@ -1951,6 +2106,7 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.gsrc, sizeof(uint32_t) * nbp},
       {(void**)&w.dtab, sizeof(unsigned long long) * 2 * ((size_t)1 << DTAB_LOG2)},
       {(void**)&w.big_list, sizeof(uint32_t) * 2 * (nb / (MEDIUM_MAX + 1) + 2)},
+      {(void**)&w.cl_list, sizeof(uint32_t) * 2 * (nb / (CLUSTER_MIN + 1) + 2)},
       {(void**)&w.lrk, sizeof(uint32_t) * nbp},
       {(void**)&w.lids2, sizeof(uint32_t) * nbp},
       {(void**)&w.lrk2, sizeof(uint32_t) * nbp},
@@ -2071,6 +2227,8 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     k_dedup_big<<<sms, 1024, 0, st>>>(c);
     tk_prof_mark(ws, "k_merge_big", st);
     k_merge_big<<<sms, BIG_THREADS, 0, st>>>(c);
+    tk_prof_mark(ws, "k_merge_cluster", st);
+    k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), BIG_THREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_merge_medium", st);
     k_merge_medium<<<sms * 4, ETHREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_encode_tiles", st);

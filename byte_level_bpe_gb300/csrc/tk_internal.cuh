@@ -22,7 +22,7 @@ constexpr int HALO = 128;
 constexpr int TRUST = 64;
 constexpr int WIN = TILE + 2 * HALO;
 
-constexpr int SHORT_MAX = 64;   // pre-tokens up to this length merge in one thread
+constexpr int SHORT_MAX = 16;   // pre-tokens up to this length merge inside the tile kernel
 constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_ITEMS = 8;    // u32 counts per scan thread
 constexpr int SCAN_TILE = SCAN_THREADS * SCAN_ITEMS;
@@ -54,6 +54,8 @@ struct Status {
   uint32_t big_next;
   uint32_t dedup_big_next;
   uint32_t n_huge;       // entries of huge_list
+  uint32_t n_cl;         // entries of cl_list
+  uint32_t cl_next;
   uint32_t tile_ctr[8];  // dynamic tile counters of the persistent kernels
   int64_t n_tiles;       // split tiles of this call (element count of the tile scan)
 };
@@ -93,7 +95,8 @@ struct Work {
   uint32_t* offs;       // [max_bytes + 1] decode: exclusive scan of cnt
   int32_t* arena;       // [max_bytes] ids of pieces merged through global memory, at their byte offset
   uint32_t* long_list;  // (start, length) of pre-tokens of SHORT_MAX+1 .. MEDIUM_MAX bytes
-  uint32_t* big_list;   // (start, length) of pre-tokens longer than MEDIUM_MAX bytes
+  uint32_t* big_list;   // (start, length) of pre-tokens of MEDIUM_MAX+1 .. CLUSTER_MIN bytes
+  uint32_t* cl_list;    // (start, length) of pre-tokens longer than CLUSTER_MIN bytes
   uint32_t* staging;    // per split tile: compacted short ids, long-piece table at the end
   uint32_t* tile_count; // per split tile: ids (then: exclusive scan -> tile_base)
   uint32_t* tile_base;  // [n_tiles + 1]

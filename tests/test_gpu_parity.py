@@ -302,3 +302,31 @@ def test_host_buffer_pipelined(full_table, full_enc):
     ids2, off2 = gpu.encode_host(np.ascontiguousarray(h_text), h_off, h_allow, tiktoken_safe=True)
     assert np.array_equal(ids2, ids_h) and np.array_equal(off2, off_h)
     gpu.close()
+
+
+def test_cluster_merged_pieces(full_gpu, full_enc):
+    """Pre-tokens long enough for the CTA-cluster merge (over 16 KiB), with
+    small alphabets so that many ranks and long merge chains occur; one piece
+    appears twice (the copy takes the first one's ids)."""
+    rng = np.random.default_rng(12)
+    pieces = [("".join(rng.choice(list(a), n))).encode() for n, a in
+              [(16385, "ab"), (20000, "abc"), (30000, "etaoin"), (80000, "esr"), (17000, "a")]]
+    segs = [(p, False) for p in pieces] + [(b" " + pieces[2], False), (pieces[1], False)]
+    _compare(full_gpu, full_enc, segs, False)
+    _compare(full_gpu, full_enc, segs, True)
+
+
+def test_mid_length_pieces(full_gpu, full_enc):
+    """Pre-tokens of 17..1024 bytes (merged per warp outside the tile kernel),
+    around the one- and two-slot register limits (32 and 64 bytes), repeated
+    so that copies take their owner's ids, mixed with short words."""
+    rng = np.random.default_rng(21)
+    parts = []
+    for n in [17, 18, 31, 32, 33, 47, 63, 64, 65, 100, 513, 1024]:
+        for alpha in ["ab", "etaoinshr", "abcdefghijklmnopqrstuvwxyz"]:
+            w = "".join(rng.choice(list(alpha), n))
+            parts += [" " + w[1:], w, " " + w[1:]]
+    rng.shuffle(parts)
+    text = " ".join(parts).encode()
+    segs = [(text[i:i + 5000], False) for i in range(0, len(text), 5000)]
+    _compare(full_gpu, full_enc, segs, False)
