@@ -330,3 +330,20 @@ def test_mid_length_pieces(full_gpu, full_enc):
     text = " ".join(parts).encode()
     segs = [(text[i:i + 5000], False) for i in range(0, len(text), 5000)]
     _compare(full_gpu, full_enc, segs, False)
+
+
+def test_token_that_does_not_encode_to_itself():
+    """A table may hold a token that the merge loop never builds from its own
+    bytes: with bc < ab < cd < abcd, "abcd" merges bc first and stops at
+    [a, bc, d].  Such a token must not be used as a whole-piece shortcut."""
+    import byte_level_bpe_gb300 as tk
+    table = [bytes([i]) for i in range(256)] + [b"bc", b"ab", b"cd", b"abcd", b"wxyz", b"wx", b"yz"]
+    # wxyz (rank 260) is unreachable too: wx (261) and yz (262) come later
+    enc = oracle.Encoding(table, {})
+    gpu = tk.Tokenizer(table, {}, max_bytes=1 << 16, max_segments=4)
+    text = "abcd abcd wxyz abcdabcd wxyzwxyz ab cd bc"
+    g_ids, _ = gpu.encode_segments([(text, False)], tiktoken_safe=False)
+    o_ids = enc.encode(text.encode())
+    assert np.array_equal(g_ids.cpu().numpy(), o_ids)
+    assert list(enc.encode(b"abcd")) == [ord("a"), 256, ord("d")]
+    gpu.close()

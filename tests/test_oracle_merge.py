@@ -92,3 +92,13 @@ def test_table_validation():
         oracle.Encoding(floor + [b"ab", b"ab"])  # duplicate bytes
     with pytest.raises(oracle.OracleError):
         oracle.Encoding(floor, {"<|x|>": 65})  # special id collides with a rank
+
+
+def test_token_unreachable_from_its_own_bytes():
+    """Worked by hand: ranks bc=256 < ab=257 < cd=258 < abcd=259.  The loop
+    merges the least rank first (bc), after which no pair of [a, bc, d] is a
+    token, so "abcd" never becomes the token abcd."""
+    table = [bytes([i]) for i in range(256)] + [b"bc", b"ab", b"cd", b"abcd"]
+    enc = oracle.Encoding(table, {})
+    assert list(enc.bpe_piece(b"abcd")) == [ord("a"), 256, ord("d")]
+    assert list(enc.bpe_piece(b"abcdab")) == [ord("a"), 256, ord("d"), 257]
