@@ -606,7 +606,7 @@ __device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t
   return ((S_N | S_L | S_O | S_NL | S_W) & ~sl) >> 4 & 0xFFFFu;
 }
 
-__global__ void __launch_bounds__(SPLIT_THREADS) k_split(Call c) {
+__global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
   __shared__ SplitSmem sm;
   __shared__ uint8_t s_asc[128];
   __shared__ int s_any_allow;
@@ -1249,10 +1249,9 @@ struct EncSmem {
   uint8_t plen[TILE];                   // length of the short piece starting at each byte
   uint32_t cls_cnt[16];                 // work list: class starts [0..N], then fill cursors
   int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
-  int32_t outs[TILE + SHORT_MAX];       // work list (x | len << 16), then compacted ids
+  uint16_t list[TILE + SHORT_MAX];      // work list: x | (len - 1) << 12
   GPiece gp[MAX_GP];
   uint32_t th_full[ETHREADS];
-  uint32_t th_short[ETHREADS];
   uint32_t warp_tot[2 * ETHREADS / 32];
   int64_t red64[ETHREADS / 32];
   uint32_t red32[ETHREADS / 32];
@@ -1389,11 +1388,11 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       sm.cls_cnt[N_CLASSES] = run;
     }
     __syncthreads();
-    uint32_t* list = reinterpret_cast<uint32_t*>(sm.outs);
+    uint16_t* list = sm.list;
     for (uint32_t bits = my; bits; bits &= bits - 1) {
       const int x = xb + __ffs(bits) - 1;
       const int len = sm.plen[x];
-      if (len) list[atomicAdd(&sm.cls_cnt[N_CLASSES + 1 + len_class(len)], 1u)] = (uint32_t)x | ((uint32_t)len << 16);
+      if (len) list[atomicAdd(&sm.cls_cnt[N_CLASSES + 1 + len_class(len)], 1u)] = (uint16_t)(x | ((len - 1) << 12));
     }
     __syncthreads();
     // 2b. the list, class by class (class k is list[cls_cnt[k] .. cls_cnt[k + 1])).
@@ -1408,7 +1407,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
 #pragma unroll
         for (int k = 0; k < 4; k++) {
           const uint32_t ii = i + k * ETHREADS;
-          x[k] = ii < e0 ? (list[ii] & 0xFFFFu) : 0u;
+          x[k] = ii < e0 ? (list[ii] & 0xFFFu) : 0u;
           v[k] = __ldg(&MT.byte_id[sm.text[x[k]]]);
         }
 #pragma unroll
@@ -1423,7 +1422,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
 #pragma unroll
         for (int k = 0; k < 4; k++) {
           const uint32_t ii = i + k * ETHREADS;
-          x[k] = ii < e1 ? (list[ii] & 0xFFFFu) : 0u;
+          x[k] = ii < e1 ? (list[ii] & 0xFFFu) : 0u;
           r[k] = dense_rank(MT, sm.text[x[k]], sm.text[x[k] + 1]);
         }
 #pragma unroll
@@ -1441,8 +1440,8 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       }
       for (uint32_t i = e1 + tid; i < e2; i += 2 * ETHREADS) {
         const uint32_t i2 = i + ETHREADS;
-        const uint32_t xa = list[i] & 0xFFFFu;
-        const uint32_t xb2 = i2 < e2 ? (list[i2] & 0xFFFFu) : xa;
+        const uint32_t xa = list[i] & 0xFFFu;
+        const uint32_t xb2 = i2 < e2 ? (list[i2] & 0xFFFu) : xa;
         const Ids3 ma = merge3(MT, &sm.text[xa]);
         const Ids3 mb = merge3(MT, &sm.text[xb2]);
         put3(&sm.stage[xa], ma);
@@ -1454,7 +1453,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       }
       for (uint32_t i = e2 + tid; i < e5; i += ETHREADS) {
         const uint32_t ent = list[i];
-        const int x = ent & 0xFFFF, len = ent >> 16;
+        const int x = ent & 0xFFF, len = (int)(ent >> 12) + 1;
         sm.cnt[x] = (uint8_t)merge_small(MT, &sm.text[x], len, &sm.stage[x]);
       }
     }
@@ -1472,7 +1471,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       if (ngp) atomicAdd(&c.W.status->n_long, (uint32_t)ngp);
     }
     // 4. per-thread totals -> block scan -> tile total -> look-back
-    uint32_t my_full = my_short;
+    uint32_t my_full = my_short, th_short = 0;
     for (uint32_t bits = my; bits; bits &= bits - 1) {
       const int x = xb + __ffs(bits) - 1;
       if ((sm.gb[x >> 5] >> (x & 31)) & 1u)
@@ -1502,12 +1501,14 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       }
       __syncthreads();
       sm.th_full[tid] = sm.warp_tot[warp] + a - my_full;
-      sm.th_short[tid] = sm.warp_tot[ETHREADS / 32 + warp] + b - my_short;
+      th_short = sm.warp_tot[ETHREADS / 32 + warp] + b - my_short;
     }
     __syncthreads();
-    // 5. compaction of short ids; offsets of the global pieces
+    // 5. compaction of short ids into the tile's staging slot (in order);
+    //    offsets of the global pieces
+    uint32_t* slot = c.W.staging + tile * STG;
     {
-      uint32_t f = sm.th_full[tid], s = sm.th_short[tid];
+      uint32_t f = sm.th_full[tid], s = th_short;
       for (uint32_t bits = my; bits; bits &= bits - 1) {
         const int x = xb + __ffs(bits) - 1;
         if ((sm.gb[x >> 5] >> (x & 31)) & 1u) {
@@ -1520,17 +1521,14 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
           continue;
         }
         const uint32_t m = sm.cnt[x];
-        for (uint32_t j = 0; j < m; j++) sm.outs[s + j] = sm.stage[x + j];
+        for (uint32_t j = 0; j < m; j++) slot[s + j] = (uint32_t)sm.stage[x + j];
         s += m;
         f += m;
       }
     }
     __syncthreads();
-    // 6. the tile's output to its staging slot: short ids in order, the table
-    //    of pieces merged through global memory at the slot's end; the tile's
-    //    id count; segment offsets relative to the tile
-    uint32_t* slot = c.W.staging + tile * STG;
-    for (uint32_t q = tid; q < sm.tile_short; q += ETHREADS) slot[q] = (uint32_t)sm.outs[q];
+    // 6. the table of pieces merged through global memory at the slot's end;
+    //    the tile's id count; segment offsets relative to the tile
     for (int g = tid; g < ngp; g += ETHREADS) {
       uint32_t* e = slot + STG - 4 * (g + 1);
       e[0] = sm.gp[g].short_excl;
