@@ -850,6 +850,10 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
 // b must have W readable bytes.
 template <int W>
 __device__ __forceinline__ int merge_reg(const MergeTabs T, const uint8_t* b, int n, int32_t* out) {
+  static_assert(W <= 16, "positions are packed in four bits");
+  // rk[i]: rank of the pair (i, i + 1), NOPAIR if none; ranks are below 2^20,
+  // so (rank << 4 | i) orders by rank, then by position (the leftmost minimum)
+  constexpr uint32_t NOPAIR = 0x0FFFFFFFu;
   uint32_t ids[W], rk[W];
 #pragma unroll
   for (int i = 0; i < W; i++) {
@@ -859,43 +863,40 @@ __device__ __forceinline__ int merge_reg(const MergeTabs T, const uint8_t* b, in
   }
 #pragma unroll
   for (int i = 0; i < W - 1; i++) {
-    uint32_t v = RANK_MAX;
-    if (i + 1 < n) v = dense_rank(T, b[i], b[i + 1]);
+    uint32_t v = NOPAIR;
+    if (i + 1 < n) {
+      const uint32_t r = dense_rank(T, b[i], b[i + 1]);
+      v = r == RANK_MAX ? NOPAIR : r;
+    }
     rk[i] = v;
   }
-  rk[W - 1] = RANK_MAX;
+  rk[W - 1] = NOPAIR;
   int m = n;
   while (m > 1) {
-    // leftmost minimum (strict <)
-    uint32_t best = rk[0];
-    int bi = 0;
+    uint32_t key = 0xFFFFFFFFu;
 #pragma unroll
-    for (int i = 1; i < W - 1; i++) {
-      const bool lt = rk[i] < best;
-      best = lt ? rk[i] : best;
-      bi = lt ? i : bi;
-    }
-    if (best == RANK_MAX) break;
+    for (int i = 0; i < W - 1; i++) key = min(key, (rk[i] << 4) | (uint32_t)i);
+    if (key >= (NOPAIR << 4)) break;
+    const int bi = (int)(key & 15u);
+    const uint32_t best = key >> 4;
     // piece bi becomes the token `best`; pieces after bi + 1 move down one
+    uint32_t a_prev = 0, a_next = 0;
 #pragma unroll
     for (int i = 0; i < W - 1; i++) {
-      const uint32_t nid = (i == bi) ? best : ((i > bi) ? ids[i + 1] : ids[i]);
-      const uint32_t nrk = (i > bi) ? rk[i + 1] : rk[i];
+      const bool gt = i > bi;
+      const uint32_t nid = gt ? ids[i + 1] : (i == bi ? best : ids[i]);
+      rk[i] = gt ? rk[i + 1] : rk[i];
       ids[i] = nid;
-      rk[i] = nrk;
+      a_prev = (i == bi - 1) ? nid : a_prev;
+      a_next = (i == bi + 1) ? nid : a_next;
     }
-    rk[W - 1] = RANK_MAX;
+    rk[W - 1] = NOPAIR;
     m--;
     // re-rank the pairs at bi and bi - 1
-    uint32_t a_prev = 0, a = 0, a_next = 0;
-#pragma unroll
-    for (int i = 0; i < W; i++) {
-      a_prev = (i == bi - 1) ? ids[i] : a_prev;
-      a = (i == bi) ? ids[i] : a;
-      a_next = (i == bi + 1) ? ids[i] : a_next;
-    }
-    const uint32_t r0 = (bi + 1 < m) ? pair_rank(T, a, a_next) : RANK_MAX;
-    const uint32_t r1 = (bi > 0) ? pair_rank(T, a_prev, a) : RANK_MAX;
+    uint32_t r0 = (bi + 1 < m) ? pair_rank(T, best, a_next) : RANK_MAX;
+    uint32_t r1 = (bi > 0) ? pair_rank(T, a_prev, best) : RANK_MAX;
+    r0 = r0 == RANK_MAX ? NOPAIR : r0;
+    r1 = r1 == RANK_MAX ? NOPAIR : r1;
 #pragma unroll
     for (int i = 0; i < W; i++) rk[i] = (i == bi) ? r0 : ((i == bi - 1) ? r1 : rk[i]);
   }
@@ -954,15 +955,16 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
   }
   if (n <= 4) return merge_reg<4>(T, b, n, out);
   if (n <= 8) return merge_reg<8>(T, b, n, out);
+  if (n <= 12) return merge_reg<12>(T, b, n, out);
   return merge_reg<16>(T, b, n, out);
 }
 
 // Length class of a pre-token for the tile's work list (warps then run
 // pieces of one class together).
-constexpr int N_CLASSES = 6;  // 1, 2, 3, 4, 5-8, 9-16 bytes
-__device__ __forceinline__ int len_class(int n) {
-  return n <= 4 ? n - 1 : n <= 8 ? 4 : 5;
-}
+constexpr int N_CLASSES = SHORT_MAX;  // one class per length: a warp's lanes get
+                                     // pieces of one length (the same loop width
+                                     // and similar step counts)
+__device__ __forceinline__ int len_class(int n) { return n - 1; }
 
 // The group that runs one round merge: NW warps (NW = 1: one warp, no block
 // barriers; else the whole CTA).  s64 / s32 are shared scratch of NW entries.
@@ -1247,7 +1249,7 @@ struct EncSmem {
   uint32_t gb[TILE / 32];               // starts of pieces merged through global memory
   uint8_t cnt[TILE];                    // ids of the short piece starting at each byte
   uint8_t plen[TILE];                   // length of the short piece starting at each byte
-  uint32_t cls_cnt[16];                 // work list: class starts [0..N], then fill cursors
+  uint32_t cls_cnt[2 * N_CLASSES + 1];  // work list: class starts [0..N], then fill cursors
   int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
   uint16_t list[TILE + SHORT_MAX];      // work list: x | (len - 1) << 12
   GPiece gp[MAX_GP];
@@ -1324,7 +1326,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       sm.sb[i] = c.T.n_spec ? c.W.sbits[(t0 >> 5) + i] : 0u;
       sm.gb[i] = 0;
     }
-    if (tid < 16) sm.cls_cnt[tid] = 0;
+    if (tid < 2 * N_CLASSES + 1) sm.cls_cnt[tid] = 0;
     if (tid == 0) {
       sm.n_gp = 0;
       sm.n_starts = 0;
@@ -2333,7 +2335,7 @@ constexpr int64_t PIPE_MIN_BYTES = 16ll << 20;
 // Start of batch k's text in the staging buffer: 16-byte aligned, after the
 // end of batch k - 1's (which ends below b0 + 16 k).
 static int64_t pipe_text_at(int64_t b0, int k) { return (b0 + 16 * (int64_t)k + 15) & ~(int64_t)15; }
-constexpr int PIPE_TARGET = 6;
+constexpr int PIPE_TARGET = 8;
 static int plan_batches(const int64_t* seg_off, int64_t S, int64_t n, int64_t* first) {
   if (S < 2 || n < 2 * PIPE_MIN_BYTES || seg_off[0] != 0 || seg_off[S] != n) return 1;
   for (int64_t s = 0; s < S; s++)
