@@ -1258,6 +1258,7 @@ struct EncSmem {
   int64_t red64[ETHREADS / 32];
   uint32_t red32[ETHREADS / 32];
   int n_gp;
+  uint32_t mnext;  // merge work-list cursor
   uint32_t n_starts;
   int64_t tile;
   uint64_t base;
@@ -1329,6 +1330,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     if (tid < 2 * N_CLASSES + 1) sm.cls_cnt[tid] = 0;
     if (tid == 0) {
       sm.n_gp = 0;
+      sm.mnext = 0;
       sm.n_starts = 0;
       sm.seg[0] = c.W.tile_segs[4 * tile + 1];
       sm.seg[1] = (tile == ntiles - 1) ? c.S + 1 : c.W.tile_segs[4 * tile + 2];
@@ -1397,66 +1399,22 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       if (len) list[atomicAdd(&sm.cls_cnt[N_CLASSES + 1 + len_class(len)], 1u)] = (uint16_t)(x | ((len - 1) << 12));
     }
     __syncthreads();
-    // 2b. the list, class by class (class k is list[cls_cnt[k] .. cls_cnt[k + 1])).
-    //     One and two bytes: four pieces per thread at a time; three bytes:
-    //     two at a time; 4..16 bytes: the register loop.
+    // 2b. the list, longest pieces first: each warp takes the next 32 entries
+    //     (one length, or two at a class boundary) until none is left, so no
+    //     warp holds the tile back with a late long piece.
     {
       const MergeTabs MT(c.T);
-      const uint32_t e0 = sm.cls_cnt[1], e1 = sm.cls_cnt[2], e2 = sm.cls_cnt[3];
-      const uint32_t e5 = sm.cls_cnt[N_CLASSES];
-      for (uint32_t i = tid; i < e0; i += 4 * ETHREADS) {
-        uint32_t x[4], v[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const uint32_t ii = i + k * ETHREADS;
-          x[k] = ii < e0 ? (list[ii] & 0xFFFu) : 0u;
-          v[k] = __ldg(&MT.byte_id[sm.text[x[k]]]);
+      const uint32_t total = sm.cls_cnt[N_CLASSES];
+      for (;;) {
+        uint32_t pos = 0;
+        if (lane == 0) pos = atomicAdd(&sm.mnext, 32u);
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        if (pos >= total) break;
+        if (pos + lane < total) {
+          const uint32_t ent = list[total - 1 - (pos + lane)];
+          const int x = ent & 0xFFF, len = (int)(ent >> 12) + 1;
+          sm.cnt[x] = (uint8_t)merge_small(MT, &sm.text[x], len, &sm.stage[x]);
         }
-#pragma unroll
-        for (int k = 0; k < 4; k++)
-          if (i + k * ETHREADS < e0) {
-            sm.stage[x[k]] = (int32_t)v[k];
-            sm.cnt[x[k]] = 1;
-          }
-      }
-      for (uint32_t i = e0 + tid; i < e1; i += 4 * ETHREADS) {
-        uint32_t x[4], r[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const uint32_t ii = i + k * ETHREADS;
-          x[k] = ii < e1 ? (list[ii] & 0xFFFu) : 0u;
-          r[k] = dense_rank(MT, sm.text[x[k]], sm.text[x[k] + 1]);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          if (i + k * ETHREADS >= e1) continue;
-          if (r[k] != RANK_MAX) {
-            sm.stage[x[k]] = (int32_t)r[k];
-            sm.cnt[x[k]] = 1;
-          } else {
-            sm.stage[x[k]] = (int32_t)__ldg(&MT.byte_id[sm.text[x[k]]]);
-            sm.stage[x[k] + 1] = (int32_t)__ldg(&MT.byte_id[sm.text[x[k] + 1]]);
-            sm.cnt[x[k]] = 2;
-          }
-        }
-      }
-      for (uint32_t i = e1 + tid; i < e2; i += 2 * ETHREADS) {
-        const uint32_t i2 = i + ETHREADS;
-        const uint32_t xa = list[i] & 0xFFFu;
-        const uint32_t xb2 = i2 < e2 ? (list[i2] & 0xFFFu) : xa;
-        const Ids3 ma = merge3(MT, &sm.text[xa]);
-        const Ids3 mb = merge3(MT, &sm.text[xb2]);
-        put3(&sm.stage[xa], ma);
-        sm.cnt[xa] = (uint8_t)ma.n;
-        if (i2 < e2) {
-          put3(&sm.stage[xb2], mb);
-          sm.cnt[xb2] = (uint8_t)mb.n;
-        }
-      }
-      for (uint32_t i = e2 + tid; i < e5; i += ETHREADS) {
-        const uint32_t ent = list[i];
-        const int x = ent & 0xFFF, len = (int)(ent >> 12) + 1;
-        sm.cnt[x] = (uint8_t)merge_small(MT, &sm.text[x], len, &sm.stage[x]);
       }
     }
     __syncthreads();
