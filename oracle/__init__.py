@@ -70,6 +70,8 @@ def lib():
         _lib.orc_py_isspace.restype = ctypes.c_int
         _lib.orc_train.argtypes = [P, I64, I64, P, I64, P]
         _lib.orc_train.restype = I64
+        _lib.orc_utf8_holdback.argtypes = [P, I64]
+        _lib.orc_utf8_holdback.restype = ctypes.c_int
     return _lib
 
 
@@ -173,6 +175,33 @@ class Encoding:
         if rc != ORC_OK:
             raise OracleError(rc, "decode failed")
         return out[: n.value].tobytes()
+
+
+def utf8_holdback(b):
+    """How many trailing bytes of b form a proper prefix of a UTF-8 character."""
+    arr = _buf(bytes(b))
+    return int(lib().orc_utf8_holdback(_ptr(arr), len(arr)))
+
+
+class StreamDecoder:
+    """Streaming decode ("tiktoken Deep Dive", "Pitfalls that bite in
+    production"): each feed returns the held-back bytes of the previous feed
+    plus the bytes of the new ids, minus a trailing partial character, which
+    waits for the next feed; finish() returns what is still held."""
+
+    def __init__(self, enc):
+        self.enc = enc
+        self.pending = b""
+
+    def feed(self, ids):
+        out = self.pending + self.enc.decode(ids)
+        k = utf8_holdback(out)
+        self.pending = out[len(out) - k:] if k else b""
+        return out[:len(out) - k]
+
+    def finish(self):
+        out, self.pending = self.pending, b""
+        return out
 
 
 def split(text):

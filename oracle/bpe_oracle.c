@@ -584,6 +584,47 @@ int orc_decode(const orc_enc* E, const int32_t* ids, int64_t n, uint8_t* out, in
 }
 
 /* ------------------------------------------------------------------------- */
+/* Streaming decode ([TT] "Pitfalls that bite in production": tokens are not   */
+/* characters, so a token can end inside a character; accumulate the bytes    */
+/* and hold back any trailing partial sequence).  A trailing partial sequence */
+/* is a proper prefix of a well-formed UTF-8 character: a lead byte followed  */
+/* by fewer continuation bytes than it announces, each in its allowed range   */
+/* (Unicode's table of well-formed byte sequences: after E0 the next byte is  */
+/* A0..BF, after ED 80..9F, after F0 90..BF, after F4 80..8F, else 80..BF).   */
+/* Returns how many of the last bytes of b[0..n) form such a prefix (0..3).   */
+
+static int lead_len(uint8_t b) {
+  if (b >= 0xC2 && b <= 0xDF) return 2;
+  if (b >= 0xE0 && b <= 0xEF) return 3;
+  if (b >= 0xF0 && b <= 0xF4) return 4;
+  return 0; /* ASCII, a continuation byte, or a byte that never leads */
+}
+
+static int second_ok(uint8_t lead, uint8_t b) {
+  if (lead == 0xE0) return b >= 0xA0 && b <= 0xBF;
+  if (lead == 0xED) return b >= 0x80 && b <= 0x9F;
+  if (lead == 0xF0) return b >= 0x90 && b <= 0xBF;
+  if (lead == 0xF4) return b >= 0x80 && b <= 0x8F;
+  return b >= 0x80 && b <= 0xBF;
+}
+
+int orc_utf8_holdback(const uint8_t* b, int64_t n) {
+  /* try each possible start of the partial character: 1, 2, 3 bytes from the end */
+  for (int64_t k = 1; k <= 3 && k <= n; k++) {
+    const int64_t p = n - k;
+    const int need = lead_len(b[p]);
+    if (need == 0) continue;  /* not a lead byte: the start must be further back */
+    if (k >= need) return 0;   /* the character at p is complete (or too long) */
+    for (int64_t j = p + 1; j < n; j++) {
+      const int ok = (j == p + 1) ? second_ok(b[p], b[j]) : (b[j] >= 0x80 && b[j] <= 0xBF);
+      if (!ok) return 0;
+    }
+    return (int)k;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Plain BPE trainer for the tiny table: split the corpus with the pattern,   */
 /* count identical pre-tokens, then repeatedly merge the most frequent        */
 /* adjacent pair whose concatenation is not yet a token (ties: smallest       */
