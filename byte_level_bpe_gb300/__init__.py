@@ -176,9 +176,46 @@ class Tokenizer:
                                 out.data_ptr(), out.numel(), st.cuda_stream)
         return out[:m]
 
+    def stream_decoder(self, stream=None):
+        """Incremental decode: feed(ids) -> bytes that end on a character
+        boundary (a trailing partial character waits for the next feed);
+        finish() -> the bytes still held back."""
+        return _StreamDecoder(self, stream)
+
     def decode(self, ids):
         torch = _torch()
         if not torch.is_tensor(ids):
             ids = torch.as_tensor(np.asarray(ids, np.int32))
         d = ids.to(self.device, dtype=torch.int32).contiguous()
         return self.decode_device(d).cpu().numpy().tobytes()
+
+
+class _StreamDecoder:
+    def __init__(self, tok, stream):
+        self._tok = tok
+        self._stream = stream
+        self._state = native.DecodeState()
+
+    def _call(self, ids, final):
+        torch = _torch()
+        tok = self._tok
+        if not torch.is_tensor(ids):
+            ids = torch.as_tensor(np.asarray(ids, np.int32))
+        d = ids.to(tok.device, dtype=torch.int32).contiguous()
+        n = int(d.numel())
+        tok.ensure_workspace(max(n, 1), 1)
+        st = self._stream if self._stream is not None else torch.cuda.current_stream(tok.device)
+        rc, need = native.tk_decode_stream(tok._h, tok._ws, self._state, d.data_ptr() if n else None, n, final,
+                                           None, 0, st.cuda_stream, raise_on_error=False)
+        if rc not in (native.TK_OK, native.TK_E_CAPACITY):
+            native.check(rc, "tk_decode_stream")
+        out = torch.empty(max(need + 4, 1), dtype=torch.uint8, device=tok.device)
+        _, m = native.tk_decode_stream(tok._h, tok._ws, self._state, d.data_ptr() if n else None, n, final,
+                                       out.data_ptr(), out.numel(), st.cuda_stream)
+        return out[:m].cpu().numpy().tobytes()
+
+    def feed(self, ids):
+        return self._call(ids, False)
+
+    def finish(self):
+        return self._call([], True)

@@ -56,6 +56,8 @@ struct Status {
   uint32_t n_huge;       // entries of huge_list
   uint32_t n_cl;         // entries of cl_list
   uint32_t cl_next;
+  int32_t holdback;      // streaming decode: bytes held back at the end
+  uint32_t tail;         // ... and those bytes, little-endian
   uint32_t tile_ctr[8];  // dynamic tile counters of the persistent kernels
   int64_t n_tiles;       // split tiles of this call (element count of the tile scan)
 };

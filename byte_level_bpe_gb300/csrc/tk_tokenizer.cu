@@ -315,19 +315,11 @@ __global__ void k_dec_total(Work W, int64_t n) { W.status->n_ids = W.offs[n]; }
 
 }  // namespace tk
 
-extern "C" int tk_decode(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, int64_t n,
-                         uint8_t* d_out, int64_t cap, int64_t* h_len, void* cuda_stream) {
+// Enqueues a decode of d_ids[n] into d_out[cap] on st (no sync); the byte
+// total lands in the status block (n_ids).
+static int decode_enqueue(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, int64_t n,
+                          uint8_t* d_out, int64_t cap, cudaStream_t st) {
   using namespace tk;
-  if (!tok || !ws || n < 0 || cap < 0 || (n > 0 && !d_ids) || (cap > 0 && !d_out)) {
-    tk_set_error("tk_decode: bad argument");
-    return TK_E_ARG;
-  }
-  if (n > ws->w.max_bytes) {
-    tk_set_error("tk_decode: %lld ids above the workspace limit %lld", (long long)n, (long long)ws->w.max_bytes);
-    return TK_E_LIMIT;
-  }
-  cudaSetDevice(ws->device);
-  cudaStream_t st = (cudaStream_t)cuda_stream;
   const int64_t n_desc = (n + 1 + SCAN_TILE - 1) / SCAN_TILE + 1;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)ws->num_sms * 8));
   tk_prof_mark(ws, "k_dec_reset", st);
@@ -345,26 +337,139 @@ extern "C" int tk_decode(const tk_tokenizer* tok, tk_workspace* ws, const int32_
   }
   tk_prof_mark(ws, "k_dec_total", st);
   k_dec_total<<<1, 1, 0, st>>>(ws->w, n);
+  return TK_OK;
+}
+
+// Reads the status back and turns it into a return code (total = bytes needed).
+static int decode_finish(tk_workspace* ws, int64_t cap, int64_t extra, cudaStream_t st, const char* who) {
   cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = cudaMemcpyAsync(ws->h_status, ws->w.status, sizeof(Status), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ws->h_status, ws->w.status, sizeof(tk::Status), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
-    tk_set_error("tk_decode: %s", cudaGetErrorString(e));
+    tk_set_error("%s: %s", who, cudaGetErrorString(e));
     return TK_E_CUDA;
   }
   tk_prof_finish(ws, st);
-  if (h_len) *h_len = ws->h_status->n_ids;
   if (ws->h_status->code == TK_E_BADID) {
-    tk_set_error("tk_decode: unknown id at index %lld", (long long)ws->h_status->err_pos);
+    tk_set_error("%s: unknown id at index %lld", who, (long long)ws->h_status->err_pos);
     return TK_E_BADID;
   }
   if (ws->h_status->code) {
-    tk_set_error("tk_decode: device error %d", ws->h_status->code);
+    tk_set_error("%s: device error %d", who, ws->h_status->code);
     return ws->h_status->code;
   }
-  if (ws->h_status->n_ids > cap) {
-    tk_set_error("tk_decode: capacity %lld < %lld bytes", (long long)cap, (long long)ws->h_status->n_ids);
+  if (ws->h_status->n_ids + extra > cap) {
+    tk_set_error("%s: capacity %lld < %lld bytes", who, (long long)cap, (long long)(ws->h_status->n_ids + extra));
     return TK_E_CAPACITY;
   }
+  return TK_OK;
+}
+
+extern "C" int tk_decode(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, int64_t n,
+                         uint8_t* d_out, int64_t cap, int64_t* h_len, void* cuda_stream) {
+  using namespace tk;
+  if (!tok || !ws || n < 0 || cap < 0 || (n > 0 && !d_ids) || (cap > 0 && !d_out)) {
+    tk_set_error("tk_decode: bad argument");
+    return TK_E_ARG;
+  }
+  if (n > ws->w.max_bytes) {
+    tk_set_error("tk_decode: %lld ids above the workspace limit %lld", (long long)n, (long long)ws->w.max_bytes);
+    return TK_E_LIMIT;
+  }
+  cudaSetDevice(ws->device);
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  int rc = decode_enqueue(tok, ws, d_ids, n, d_out, cap, st);
+  if (rc) return rc;
+  rc = decode_finish(ws, cap, 0, st, "tk_decode");
+  if (h_len) *h_len = ws->h_status->n_ids;
+  return rc;
+}
+
+namespace tk {
+// How many bytes at the end of b[0..n) start a character that is not complete
+// yet: step back over at most three continuation bytes (10xxxxxx) to the
+// character's first byte; if that byte announces more bytes than are present
+// (C2..DF: 2, E0..EF: 3, F0..F4: 4) and the second byte, if present, is in its
+// well-formed range (E0: A0..BF, ED: 80..9F, F0: 90..BF, F4: 80..8F), all of
+// them wait for the next call.
+__device__ int utf8_partial_tail(const uint8_t* b, int64_t n) {
+  int64_t p = n - 1;
+  int back = 0;
+  while (p >= 0 && back < 3 && (b[p] & 0xC0u) == 0x80u) {
+    p--;
+    back++;
+  }
+  if (p < 0) return 0;
+  const uint32_t lead = b[p];
+  const int want = (lead >= 0xC2u && lead <= 0xDFu) ? 2 : (lead >= 0xE0u && lead <= 0xEFu) ? 3
+                 : (lead >= 0xF0u && lead <= 0xF4u) ? 4 : 0;
+  const int have = (int)(n - p);
+  if (want == 0 || have >= want) return 0;
+  if (have >= 2) {
+    const uint32_t s = b[p + 1];
+    const uint32_t lo = lead == 0xE0u ? 0xA0u : lead == 0xF0u ? 0x90u : 0x80u;
+    const uint32_t hi = lead == 0xEDu ? 0x9Fu : lead == 0xF4u ? 0x8Fu : 0xBFu;
+    if (s < lo || s > hi) return 0;
+  }
+  return have;
+}
+
+// One thread: the held-back count and bytes of a streaming decode whose
+// output holds np pending bytes followed by the decoded ones.
+__global__ void k_dec_holdback(Work W, const uint8_t* out, int64_t np, int64_t cap, int final) {
+  const int64_t total = np + W.status->n_ids;
+  int hb = 0;
+  uint32_t tail = 0;
+  if (!final && total <= cap && W.status->code == 0) {
+    hb = utf8_partial_tail(out, total);
+    for (int j = 0; j < hb; j++) tail |= (uint32_t)out[total - hb + j] << (8 * j);
+  }
+  W.status->holdback = hb;
+  W.status->tail = tail;
+}
+}  // namespace tk
+
+extern "C" int tk_decode_stream(const tk_tokenizer* tok, tk_workspace* ws, tk_decode_state* state,
+                                const int32_t* d_ids, int64_t n, int final, uint8_t* d_out, int64_t cap,
+                                int64_t* h_len, void* cuda_stream) {
+  using namespace tk;
+  if (!tok || !ws || !state || n < 0 || cap < 0 || (n > 0 && !d_ids) || (cap > 0 && !d_out) ||
+      state->n_pending < 0 || state->n_pending > 3) {
+    tk_set_error("tk_decode_stream: bad argument");
+    return TK_E_ARG;
+  }
+  if (n > ws->w.max_bytes) {
+    tk_set_error("tk_decode_stream: %lld ids above the workspace limit %lld", (long long)n,
+                 (long long)ws->w.max_bytes);
+    return TK_E_LIMIT;
+  }
+  cudaSetDevice(ws->device);
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  const int64_t np = state->n_pending;
+  const bool fits = cap >= np;  // else only the total is computed (TK_E_CAPACITY)
+  if (np && fits) {
+    // the held-back bytes go first (a copy from pageable memory: the runtime
+    // has taken the bytes when the call returns)
+    uint8_t pend[4];
+    memcpy(pend, state->pending, (size_t)np);
+    const cudaError_t e = cudaMemcpyAsync(d_out, pend, (size_t)np, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) {
+      tk_set_error("tk_decode_stream: pending bytes: %s", cudaGetErrorString(e));
+      return TK_E_CUDA;
+    }
+  }
+  int rc = decode_enqueue(tok, ws, d_ids, n, fits ? d_out + np : nullptr, fits ? cap - np : 0, st);
+  if (rc) return rc;
+  k_dec_holdback<<<1, 1, 0, st>>>(ws->w, d_out, np, cap, final ? 1 : 0);
+  rc = decode_finish(ws, cap, np, st, "tk_decode_stream");
+  const int64_t total = np + ws->h_status->n_ids;
+  if (rc) {
+    if (h_len) *h_len = total;
+    return rc;  // the state is unchanged: the call may be repeated
+  }
+  const int hb = ws->h_status->holdback;
+  for (int j = 0; j < 4; j++) state->pending[j] = j < hb ? (uint8_t)(ws->h_status->tail >> (8 * j)) : 0;
+  state->n_pending = hb;
+  if (h_len) *h_len = total - hb;
   return TK_OK;
 }

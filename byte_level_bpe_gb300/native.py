@@ -37,6 +37,7 @@ SIGNATURES = {
                                        ctypes.POINTER(_I64), _P]),
     "tk_decode": (_INT, [_P, _P, _P, _I64, _P, _I64, ctypes.POINTER(_I64), _P]),
     "tk_decode_noalloc": (_INT, [_P, _P, _I64, _P, _I64, ctypes.POINTER(_I64), _P]),
+    "tk_decode_stream": (_INT, [_P, _P, _P, _P, _I64, _INT, _P, _I64, ctypes.POINTER(_I64), _P]),
     "tk_n_ranks": (_I64, [_P]),
     "tk_n_specials": (_I64, [_P]),
     "tk_max_id": (_I64, [_P]),
@@ -175,4 +176,19 @@ def tk_decode_noalloc(tok, d_ids, n, d_out, cap, stream, raise_on_error=True):
     rc = load().tk_decode_noalloc(tok, d_ids, n, d_out, cap, ctypes.byref(m), stream)
     if raise_on_error:
         check(rc, "tk_decode_noalloc")
+    return rc, m.value
+
+
+class DecodeState(ctypes.Structure):
+    """tk_decode_state: the bytes a streaming decode holds back between calls."""
+    _fields_ = [("pending", ctypes.c_uint8 * 4), ("n_pending", ctypes.c_int32)]
+
+
+def tk_decode_stream(tok, ws, state, d_ids, n, final, d_out, cap, stream, raise_on_error=True):
+    """state: a DecodeState; device pointers (ints). Returns (status, n_bytes)."""
+    m = _I64(0)
+    rc = load().tk_decode_stream(tok, ws, ctypes.byref(state), d_ids, n, 1 if final else 0, d_out, cap,
+                                 ctypes.byref(m), stream)
+    if raise_on_error:
+        check(rc, "tk_decode_stream")
     return rc, m.value

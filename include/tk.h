@@ -150,6 +150,35 @@ int tk_decode(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, i
               uint8_t* d_out, int64_t cap, int64_t* h_len, void* cuda_stream);
 
 /*
+ * tk_decode_stream -- incremental decode of ids that arrive in pieces
+ * ("tiktoken Deep Dive", "Pitfalls that bite in production": tokens are not
+ * characters, so a token can end inside a character; accumulate the bytes and
+ * hold back any trailing partial sequence).
+ *
+ *   state: caller-owned, zeroed before the first call of a stream; holds the
+ *       0..3 bytes held back by the previous call.
+ *   d_ids[n]: the next ids.  final: nonzero on the last call of the stream
+ *       (nothing is held back then; n may be 0 to flush).
+ *   d_out[cap]: receives the held-back bytes of the previous call, then the
+ *       bytes of d_ids; *h_len = the bytes it may emit now: all of them except
+ *       a trailing proper prefix of a well-formed UTF-8 character (a lead byte
+ *       C2..F4 with fewer continuation bytes than it announces, the second in
+ *       its allowed range), which is kept in state for the next call.  A
+ *       surrogate prefix (ED A0..BF) is not held: no character completes it.
+ *   cap must hold state->n_pending + the bytes of d_ids; on TK_E_CAPACITY,
+ *   *h_len is that total and state is unchanged (the call may be repeated),
+ *   as for TK_E_BADID.  Uses the workspace for scratch (n <= max_bytes).
+ */
+typedef struct tk_decode_state {
+  uint8_t pending[4]; /* held-back bytes (n_pending of them) */
+  int32_t n_pending;  /* 0..3 */
+} tk_decode_state;
+
+int tk_decode_stream(const tk_tokenizer* tok, tk_workspace* ws, tk_decode_state* state,
+                     const int32_t* d_ids, int64_t n, int final, uint8_t* d_out, int64_t cap,
+                     int64_t* h_len, void* cuda_stream);
+
+/*
  * tk_decode_noalloc -- tk_decode for callers that cannot allocate device
  * memory (a server whose memory pool already holds the device's memory, or a
  * latency-critical path that must not enter the allocator or the device
