@@ -176,6 +176,22 @@ class Tokenizer:
                                 out.data_ptr(), out.numel(), st.cuda_stream)
         return out[:m]
 
+    def decode_segments(self, d_ids, d_id_off, stream=None):
+        """Device ids + id offsets[S+1] -> (device bytes, device byte offsets[S+1])."""
+        torch = _torch()
+        n = int(d_ids.numel())
+        S = int(d_id_off.numel()) - 1
+        self.ensure_workspace(max(n, 1), 1)
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        byte_off = torch.empty(S + 1, dtype=torch.int64, device=self.device)
+        _, m = native.tk_decode_segments(self._h, self._ws, d_ids.data_ptr() if n else None, n,
+                                         d_id_off.data_ptr(), S, None, 0, byte_off.data_ptr(),
+                                         st.cuda_stream, raise_on_error=False)
+        out = torch.empty(max(m, 1), dtype=torch.uint8, device=self.device)
+        native.tk_decode_segments(self._h, self._ws, d_ids.data_ptr() if n else None, n, d_id_off.data_ptr(),
+                                  S, out.data_ptr(), out.numel(), byte_off.data_ptr(), st.cuda_stream)
+        return out[:m], byte_off
+
     def stream_decoder(self, stream=None):
         """Incremental decode: feed(ids) -> bytes that end on a character
         boundary (a trailing partial character waits for the next feed);

@@ -386,6 +386,20 @@ extern "C" int tk_decode(const tk_tokenizer* tok, tk_workspace* ws, const int32_
 }
 
 namespace tk {
+// byte_off[s] = bytes before segment s's first id (the decode's exclusive scan
+// at id_off[s]); the id offsets must run 0 = id_off[0] <= ... <= id_off[S] = n.
+__global__ void k_dec_seg_offsets(Work W, const int64_t* id_off, int64_t S, int64_t n, int64_t* byte_off) {
+  for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s <= S; s += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t a = id_off[s];
+    const bool ok = a >= 0 && a <= n && (s > 0 || a == 0) && (s < S || a == n) && (s == S || id_off[s + 1] >= a);
+    if (!ok) {
+      set_error(W.status, TK_E_ARG, 21);
+      continue;
+    }
+    byte_off[s] = W.offs[a];
+  }
+}
+
 // How many bytes at the end of b[0..n) start a character that is not complete
 // yet: step back over at most three continuation bytes (10xxxxxx) to the
 // character's first byte; if that byte announces more bytes than are present
@@ -472,4 +486,31 @@ extern "C" int tk_decode_stream(const tk_tokenizer* tok, tk_workspace* ws, tk_de
   state->n_pending = hb;
   if (h_len) *h_len = total - hb;
   return TK_OK;
+}
+
+extern "C" int tk_decode_segments(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, int64_t n,
+                                  const int64_t* d_id_off, int64_t S, uint8_t* d_out, int64_t cap,
+                                  int64_t* d_byte_off, int64_t* h_len, void* cuda_stream) {
+  using namespace tk;
+  if (!tok || !ws || n < 0 || S < 0 || cap < 0 || (n > 0 && !d_ids) || (cap > 0 && !d_out) || !d_id_off ||
+      !d_byte_off) {
+    tk_set_error("tk_decode_segments: bad argument");
+    return TK_E_ARG;
+  }
+  if (n > ws->w.max_bytes) {
+    tk_set_error("tk_decode_segments: %lld ids above the workspace limit %lld", (long long)n,
+                 (long long)ws->w.max_bytes);
+    return TK_E_LIMIT;
+  }
+  cudaSetDevice(ws->device);
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  int rc = decode_enqueue(tok, ws, d_ids, n, d_out, cap, st);
+  if (rc) return rc;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((S + 256) / 256, (int64_t)ws->num_sms * 4));
+  tk_prof_mark(ws, "k_dec_seg_offsets", st);
+  k_dec_seg_offsets<<<grid, 256, 0, st>>>(ws->w, d_id_off, S, n, d_byte_off);
+  rc = decode_finish(ws, cap, 0, st, "tk_decode_segments");
+  if (h_len) *h_len = ws->h_status->n_ids;
+  if (rc == TK_E_ARG) tk_set_error("tk_decode_segments: id offsets must run 0 <= ... <= n");
+  return rc;
 }

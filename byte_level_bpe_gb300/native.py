@@ -38,6 +38,7 @@ SIGNATURES = {
     "tk_decode": (_INT, [_P, _P, _P, _I64, _P, _I64, ctypes.POINTER(_I64), _P]),
     "tk_decode_noalloc": (_INT, [_P, _P, _I64, _P, _I64, ctypes.POINTER(_I64), _P]),
     "tk_decode_stream": (_INT, [_P, _P, _P, _P, _I64, _INT, _P, _I64, ctypes.POINTER(_I64), _P]),
+    "tk_decode_segments": (_INT, [_P, _P, _P, _I64, _P, _I64, _P, _I64, _P, ctypes.POINTER(_I64), _P]),
     "tk_n_ranks": (_I64, [_P]),
     "tk_n_specials": (_I64, [_P]),
     "tk_max_id": (_I64, [_P]),
@@ -191,4 +192,14 @@ def tk_decode_stream(tok, ws, state, d_ids, n, final, d_out, cap, stream, raise_
                                  ctypes.byref(m), stream)
     if raise_on_error:
         check(rc, "tk_decode_stream")
+    return rc, m.value
+
+
+def tk_decode_segments(tok, ws, d_ids, n, d_id_off, S, d_out, cap, d_byte_off, stream, raise_on_error=True):
+    """Device pointers (ints). Returns (status, total bytes)."""
+    m = _I64(0)
+    rc = load().tk_decode_segments(tok, ws, d_ids, n, d_id_off, S, d_out, cap, d_byte_off, ctypes.byref(m),
+                                   stream)
+    if raise_on_error:
+        check(rc, "tk_decode_segments")
     return rc, m.value

@@ -150,6 +150,17 @@ int tk_decode(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, i
               uint8_t* d_out, int64_t cap, int64_t* h_len, void* cuda_stream);
 
 /*
+ * tk_decode_segments -- tk_decode of S sequences at once (the ids of an
+ * encode_segments call, say): d_ids[n] with d_id_off[S+1] (0 = d_id_off[0] <=
+ * ... <= d_id_off[S] = n, else TK_E_ARG) -> their bytes one after the other in
+ * d_out[cap] and d_byte_off[S+1], the byte offset of each sequence's first
+ * byte (d_byte_off[S] = *h_len, the total).  Errors as for tk_decode.
+ */
+int tk_decode_segments(const tk_tokenizer* tok, tk_workspace* ws, const int32_t* d_ids, int64_t n,
+                       const int64_t* d_id_off, int64_t S, uint8_t* d_out, int64_t cap,
+                       int64_t* d_byte_off, int64_t* h_len, void* cuda_stream);
+
+/*
  * tk_decode_stream -- incremental decode of ids that arrive in pieces
  * ("tiktoken Deep Dive", "Pitfalls that bite in production": tokens are not
  * characters, so a token can end inside a character; accumulate the bytes and

@@ -99,3 +99,29 @@ def test_errors_leave_the_state_unchanged(full_table):
     assert rc == 0 and out[:m].cpu().numpy().tobytes() == "\U0001F600A".encode()
     assert state.n_pending == 0
     gpu.close()
+
+
+def test_decode_segments_matches_oracle(full_table, full_enc):
+    import byte_level_bpe_gb300 as tk
+    from byte_level_bpe_gb300 import native
+    segs = workloads.agentic_segments(full_table, seed=7, scale=0.01)
+    ids, off = full_enc.encode_segments(segs, tiktoken_safe=True)
+    gpu = tk.Tokenizer(full_table, workloads.SPECIALS, max_bytes=1 << 20, max_segments=len(segs) + 1)
+    d_ids = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda()
+    d_off = torch.from_numpy(np.ascontiguousarray(off, np.int64)).cuda()
+    out, boff = gpu.decode_segments(d_ids, d_off)
+    parts = [full_enc.decode(ids[off[s]:off[s + 1]]) for s in range(len(segs))]
+    assert out.cpu().numpy().tobytes() == b"".join(parts)
+    assert boff.cpu().numpy().tolist() == np.r_[0, np.cumsum([len(p) for p in parts])].tolist()
+    text, seg_off, _ = workloads.pack_segments(segs)
+    assert out.cpu().numpy().tobytes() == text.tobytes()          # round trip of the encode
+    assert boff.cpu().numpy().tolist() == seg_off.tolist()
+    # offsets that do not run from 0 to n are refused
+    bad = d_off.clone()
+    bad[1] = bad[2] + 1
+    rc, _ = native.tk_decode_segments(gpu.handle, gpu.workspace, d_ids.data_ptr(), len(ids), bad.data_ptr(),
+                                      len(segs), out.data_ptr(), out.numel(),
+                                      torch.empty(len(segs) + 1, dtype=torch.int64, device="cuda").data_ptr(),
+                                      torch.cuda.current_stream().cuda_stream, raise_on_error=False)
+    assert rc == native.TK_E_ARG
+    gpu.close()
