@@ -60,7 +60,7 @@ def lib():
         _lib.orc_decode.restype = ctypes.c_int
         _lib.orc_bpe_piece.argtypes = [P, P, I64, P]
         _lib.orc_bpe_piece.restype = I64
-        _lib.orc_split_bytes.argtypes = [P, I64, P]
+        _lib.orc_split_bytes.argtypes = [P, I64, P, ctypes.c_int]
         _lib.orc_split_bytes.restype = I64
         _lib.orc_safe_chunks_bytes.argtypes = [P, I64, P]
         _lib.orc_safe_chunks_bytes.restype = I64
@@ -72,6 +72,8 @@ def lib():
         _lib.orc_train.restype = I64
         _lib.orc_utf8_holdback.argtypes = [P, I64]
         _lib.orc_utf8_holdback.restype = ctypes.c_int
+        _lib.orc_set_pattern.argtypes = [P, ctypes.c_int]
+        _lib.orc_set_pattern.restype = ctypes.c_int
     return _lib
 
 
@@ -94,7 +96,7 @@ class Encoding:
     """ranks: list of byte strings where index = rank = id (or (bytes, id) pairs);
     specials: dict str|bytes -> id."""
 
-    def __init__(self, ranks, specials=None):
+    def __init__(self, ranks, specials=None, pattern=None):
         if ranks and isinstance(ranks[0], tuple):
             toks = [t for t, _ in ranks]
             ids = [i for _, i in ranks]
@@ -120,6 +122,10 @@ class Encoding:
         if rc != ORC_OK:
             raise OracleError(rc, "table rejected")
         self._h = h
+        if pattern is not None:
+            rc = lib().orc_set_pattern(h, int(pattern))
+            if rc != ORC_OK:
+                raise OracleError(rc, "unknown pattern")
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -204,12 +210,16 @@ class StreamDecoder:
         return out
 
 
-def split(text):
+PATTERN_CL100K = 1       # the split pattern printed on the tiktoken page
+PATTERN_R50K_DIGITS = 2  # the same with r50k's digit clause " ?\p{N}++"
+
+
+def split(text, pattern=PATTERN_CL100K):
     """Pre-token byte strings of one ordinary piece (the pattern's clauses)."""
     b = text.encode("utf-8", "surrogatepass") if isinstance(text, str) else text
     arr = _buf(b)
     st = np.zeros(len(b) + 1, np.int64)
-    k = lib().orc_split_bytes(_ptr(arr), len(b), _ptr(st))
+    k = lib().orc_split_bytes(_ptr(arr), len(b), _ptr(st), int(pattern))
     if k < 0:
         raise OracleError(int(k), "split failed")
     starts = list(st[:k]) + [len(b)]

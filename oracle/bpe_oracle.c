@@ -40,6 +40,9 @@
 #define ORC_E_NOMEM (-6)
 #define ORC_E_BADID (-8)
 
+#define ORC_PATTERN_CL100K 1      /* the pattern printed on the tiktoken page */
+#define ORC_PATTERN_R50K_DIGITS 2 /* the same with r50k's digit clause */
+
 #define RANK_MAX 0xFFFFFFFFu
 #define CHUNK_CHARS 400000   /* [BT] "at most 400k characters" */
 #define RUN_CHARS 25000      /* [BT] "runs ... at 25k characters" */
@@ -129,6 +132,7 @@ typedef struct {
   int64_t* spec_off;
   int32_t* spec_ids;
   int64_t n_spec;
+  int pattern;         /* ORC_PATTERN_CL100K or ORC_PATTERN_R50K_DIGITS */
 } orc_enc;
 
 static int cmp_bytes(const uint8_t* a, int64_t la, const uint8_t* b, int64_t lb) {
@@ -186,6 +190,7 @@ int orc_new(const uint8_t* rank_bytes, const int64_t* rank_off, const uint32_t* 
   memcpy(E->rank_bytes, rank_bytes, (size_t)nb);
   E->n = n;
   E->max_id = -1;
+  E->pattern = ORC_PATTERN_CL100K;
   for (int64_t i = 0; i < n; i++) {
     int64_t len = rank_off[i + 1] - rank_off[i];
     if (len <= 0) { orc_free(E); return ORC_E_TABLE; }
@@ -285,6 +290,10 @@ int64_t orc_bpe_piece(const orc_enc* E, const uint8_t* b, int64_t m, int32_t* ou
 /*   C2 [^\r\n\p{L}\p{N}]?+\p{L}++   C6 \s*[\r\n]                             */
 /*   C3 \p{N}{1,3}+                  C7 \s+(?!\S)                             */
 /*   C4  ?[^\s\p{L}\p{N}]++[\r\n]*+  C8 \s                                    */
+/*                                                                            */
+/* ORC_PATTERN_R50K_DIGITS is the same alternation with r50k's digit clause   */
+/* in place of C3 ([TT] "r50k, cl100k, o200k": " ?\p{N}++", an unbounded      */
+/* digit run with an optional leading space).                                 */
 
 /* (?i:x) for the ASCII letters of clause 1: simple case folding adds U+017F
  * (LATIN SMALL LETTER LONG S) to s; the other letters fold only to their
@@ -295,7 +304,7 @@ static int fold_eq(uint32_t c, char x) {
   return x == 's' && c == 0x017F;
 }
 
-static int64_t match_clause(const uint32_t* c, int64_t n, int64_t p) {
+static int64_t match_clause(const uint32_t* c, int64_t n, int64_t p, int pattern) {
   /* C1: contractions */
   if (c[p] == 0x27 && p + 1 < n) {
     uint32_t a = c[p + 1];
@@ -316,8 +325,16 @@ static int64_t match_clause(const uint32_t* c, int64_t n, int64_t p) {
       return q - p;
     }
   }
-  /* C3: one to three numbers */
-  if (is_N(c[p])) {
+  if (pattern == ORC_PATTERN_R50K_DIGITS) {
+    /* C3 (r50k): an optional space, then every number that follows */
+    int64_t q = p;
+    if (c[p] == 0x20 && p + 1 < n && is_N(c[p + 1])) q = p + 1;
+    if (is_N(c[q])) {
+      while (q < n && is_N(c[q])) q++;
+      return q - p;
+    }
+  } else if (is_N(c[p])) {
+    /* C3: one to three numbers */
     int64_t q = p;
     while (q < n && q - p < 3 && is_N(c[q])) q++;
     return q - p;
@@ -353,10 +370,10 @@ static int64_t match_clause(const uint32_t* c, int64_t n, int64_t p) {
 
 /* Splits c[0..n) into pre-tokens; writes the start of each (code-point index)
  * to starts[] and returns how many there are. */
-int64_t orc_split_cps(const uint32_t* c, int64_t n, int64_t* starts) {
+int64_t orc_split_cps(const uint32_t* c, int64_t n, int64_t* starts, int pattern) {
   int64_t p = 0, k = 0;
   while (p < n) {
-    int64_t len = match_clause(c, n, p);
+    int64_t len = match_clause(c, n, p, pattern);
     if (len <= 0) return -1;
     starts[k++] = p;
     p += len;
@@ -420,7 +437,7 @@ static int encode_ordinary(const orc_enc* E, const uint8_t* seg, const uint32_t*
                            orc_sink* sink) {
   int64_t n = c1 - c0;
   if (n <= 0) return ORC_OK;
-  int64_t np = orc_split_cps(cps + c0, n, starts);
+  int64_t np = orc_split_cps(cps + c0, n, starts, E->pattern);
   if (np < 0) return ORC_E_ARG;
   for (int64_t t = 0; t < np; t++) {
     int64_t a = c0 + starts[t];
@@ -520,7 +537,7 @@ int orc_encode_segments(const orc_enc* E, const uint8_t* text, const int64_t* se
 
 /* Pre-token boundaries of one ordinary piece of UTF-8 text, as byte offsets
  * (for tests of the split alone).  Returns the count, or a negative error. */
-int64_t orc_split_bytes(const uint8_t* s, int64_t n, int64_t* byte_starts) {
+int64_t orc_split_bytes(const uint8_t* s, int64_t n, int64_t* byte_starts, int pattern) {
   uint32_t* cps = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(n + 1));
   int64_t* boff = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
   int64_t* st = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
@@ -528,7 +545,7 @@ int64_t orc_split_bytes(const uint8_t* s, int64_t n, int64_t* byte_starts) {
   int64_t ncp = 0, bad = -1;
   int64_t rc = utf8_decode(s, n, cps, boff, &ncp, &bad);
   if (rc == ORC_OK) {
-    rc = orc_split_cps(cps, ncp, st);
+    rc = orc_split_cps(cps, ncp, st, pattern);
     for (int64_t k = 0; k < rc; k++) byte_starts[k] = boff[st[k]];
   }
   free(cps); free(boff); free(st);
@@ -649,7 +666,7 @@ int64_t orc_train(const uint8_t* corpus, int64_t n, int64_t n_merges, uint8_t* t
                   int64_t tokens_cap, int64_t* tok_off) {
   int64_t* bst = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
   if (!bst) return ORC_E_NOMEM;
-  int64_t np = orc_split_bytes(corpus, n, bst);
+  int64_t np = orc_split_bytes(corpus, n, bst, ORC_PATTERN_CL100K);
   if (np < 0) { free(bst); return np; }
   orc_span* sp = (orc_span*)malloc(sizeof(orc_span) * (size_t)(np ? np : 1));
   for (int64_t i = 0; i < np; i++) {
@@ -760,4 +777,11 @@ int64_t orc_train(const uint8_t* corpus, int64_t n, int64_t n_merges, uint8_t* t
   free(tstart); free(tlen); free(tbytes);
   free(hkey); free(hcnt); free(hstamp); free(touched); free(excl);
   return made;
+}
+
+/* Selects the split pattern of an encoding (ORC_PATTERN_CL100K by default). */
+int orc_set_pattern(orc_enc* E, int pattern) {
+  if (!E || (pattern != ORC_PATTERN_CL100K && pattern != ORC_PATTERN_R50K_DIGITS)) return ORC_E_ARG;
+  E->pattern = pattern;
+  return ORC_OK;
 }

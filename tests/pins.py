@@ -12,16 +12,21 @@
 SPLIT_PATTERN = (r"""'(?i:[sdmt]|ll|ve|re)|[^\r\n\p{L}\p{N}]?+\p{L}++|\p{N}{1,3}+"""
                  r"""| ?[^\s\p{L}\p{N}]++[\r\n]*+|\s++$|\s*[\r\n]|\s+(?!\S)|\s""")
 
-_compiled = None
+# The same alternation with r50k's digit clause in place of cl100k's ("tiktoken
+# Deep Dive", "r50k, cl100k, o200k": r50k used " ?\p{N}++", an unbounded digit
+# run with an optional leading space).
+SPLIT_PATTERN_R50K_DIGITS = SPLIT_PATTERN.replace(r"\p{N}{1,3}+", r" ?\p{N}++")
+assert SPLIT_PATTERN_R50K_DIGITS != SPLIT_PATTERN
+
+_compiled = {}
 
 
-def regex_split(text):
-    global _compiled
+def regex_split(text, pattern=SPLIT_PATTERN):
     import regex
-    if _compiled is None:
-        _compiled = regex.compile(SPLIT_PATTERN)
+    if pattern not in _compiled:
+        _compiled[pattern] = regex.compile(pattern)
     s = text.decode("utf-8") if isinstance(text, bytes) else text
-    return [m.group(0).encode("utf-8") for m in _compiled.finditer(s)]
+    return [m.group(0).encode("utf-8") for m in _compiled[pattern].finditer(s)]
 
 
 def naive_bpe(piece, ranks):

@@ -75,3 +75,42 @@ def test_workload_texts_match_library(full_table):
     for text in [workloads.tiny_input(), workloads.prose_text(full_table, 256 * 1024, seed=9),
                  workloads.multilingual_text(full_table, 512 * 1024, seed=11)]:
         assert oracle.split(text) == regex_split(text)
+
+
+# --- the same alternation with r50k's digit clause (" ?\p{N}++") -------------
+
+def test_r50k_digits_printed_examples():
+    with open(os.path.join(HERE, "golden", "split_examples_r50k_digits.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        got = [p.decode() for p in oracle.split(c["text"], oracle.PATTERN_R50K_DIGITS)]
+        assert got == c["pretokens"], (c["text"], got, c["cite"])
+
+
+def _check_r50k(s):
+    from pins import SPLIT_PATTERN_R50K_DIGITS
+    exp = regex_split(s, SPLIT_PATTERN_R50K_DIGITS)
+    got = oracle.split(s, oracle.PATTERN_R50K_DIGITS)
+    assert got == exp, (s, got, exp)
+
+
+def test_r50k_digits_exhaustive_short_strings():
+    pytest.importorskip("regex")
+    alpha = ALPHABET[:15]
+    for L in range(1, 5):
+        for t in itertools.product(alpha, repeat=L):
+            _check_r50k("".join(t))
+
+
+def test_r50k_digits_random_strings_and_workloads(full_table):
+    pytest.importorskip("regex")
+    import workloads
+    rng = np.random.default_rng(17)
+    for _ in range(20000):
+        L = int(rng.integers(1, 65))
+        _check_r50k("".join(ALPHABET[i] for i in rng.integers(0, len(ALPHABET), size=L)))
+    from pins import SPLIT_PATTERN_R50K_DIGITS
+    agentic = workloads.pack_segments(workloads.agentic_segments(full_table, seed=3, scale=0.05))[0]
+    for text in [agentic, workloads.multilingual_text(full_table, 256 * 1024, seed=12)]:
+        text = text.tobytes() if isinstance(text, np.ndarray) else bytes(text)
+        assert oracle.split(text, oracle.PATTERN_R50K_DIGITS) == regex_split(text, SPLIT_PATTERN_R50K_DIGITS)
