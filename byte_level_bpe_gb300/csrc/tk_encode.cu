@@ -504,6 +504,8 @@ __device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) 
   const uint8_t P = kp & 7, C = kx & 7;
   switch (C) {
     case K_N:
+      // r50k's digit clause " ?\p{N}++": one run, a single space before it joins
+      if (w.c.T.pattern == TK_PATTERN_R50K_DIGITS) return P != K_N && P != K_SP;
       return P != K_N || nidx == 0;
     case K_L: {
       if (P == K_N || P == K_NL) return true;
@@ -577,23 +579,30 @@ __device__ __forceinline__ uint32_t gather_plane(uint32_t w, int i) {
 // index in its number run of the code point at x0.  Returns the start bits of
 // the 16 bytes; *slow receives the bytes whose test needs the white-space
 // walks (CR/LF followed by other white space).
-__device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t r, uint32_t* slow) {
+__device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t r, uint32_t* slow,
+                                                   bool r50k_digits) {
   const uint32_t p0 = P[0], p1 = P[1], p2 = P[2];
   const uint32_t L = ~p0 & ~p1 & ~p2, N = p0 & ~p1 & ~p2, O = ~p0 & p1 & ~p2, NL = p0 & p1 & ~p2;
   const uint32_t SP = ~p0 & ~p1 & p2, WSO = p0 & ~p1 & p2;
   const uint32_t APOS = P[3], C1 = P[4], LLf = P[5], VR = P[6], E = P[7];
   const uint32_t SPW = SP | WSO, WS = NL | SPW, OS = O | SP;
-  // numbers: group starts at run start + 3k
-  const uint32_t N1 = N << 1, N2 = N << 2;
-  uint32_t G = N & ~N1 & ~1u;
-  if ((N >> 4) & (N >> 3) & 1u) {  // the run at x0 began earlier: its index there is r
-    const int first = 4 + (int)((3u - r) % 3u);
-    const uint32_t span = ((2u << first) - 1u) & ~0xFu;  // bits 4..first
-    if ((N & span) == span) G |= 1u << first;
-  }
+  uint32_t S_N;
+  if (r50k_digits) {
+    // one start per digit run, on the space before it if there is one
+    S_N = N & ~(N << 1) & ~(SP << 1);
+  } else {
+    // numbers: group starts at run start + 3k
+    const uint32_t N1 = N << 1, N2 = N << 2;
+    uint32_t G = N & ~N1 & ~1u;
+    if ((N >> 4) & (N >> 3) & 1u) {  // the run at x0 began earlier: its index there is r
+      const int first = 4 + (int)((3u - r) % 3u);
+      const uint32_t span = ((2u << first) - 1u) & ~0xFu;  // bits 4..first
+      if ((N & span) == span) G |= 1u << first;
+    }
 #pragma unroll
-  for (int it = 0; it < 7; it++) G |= (G << 3) & N & N1 & N2;
-  const uint32_t S_N = G & N;
+    for (int it = 0; it < 7; it++) G |= (G << 3) & N & N1 & N2;
+    S_N = G & N;
+  }
   const uint32_t S_L =
       L & ((N << 1) | (NL << 1) | ((O << 1) & (OS << 2)) |
            ((L << 1) & (C1 << 1) & (APOS << 2) & ~(OS << 3)) |
@@ -790,7 +799,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       }
       if (fast) {
         uint32_t slow;
-        bits = starts_ascii16(P, r, &slow);
+        bits = starts_ascii16(P, r, &slow, c.T.pattern == TK_PATTERN_R50K_DIGITS);
         for (; slow; slow &= slow - 1) {
           const int j = __ffs(slow) - 1;
           if (starts_here(w, wlo + xb + j, sm.kc[xb + j], 0)) bits |= 1u << j;

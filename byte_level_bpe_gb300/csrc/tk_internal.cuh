@@ -78,6 +78,7 @@ struct Tables {
   const int32_t* tok_len;      // [max_id + 1] decode: length, -1 if the id is unused
   const uint8_t* tok_bytes;
   int64_t max_id;
+  int32_t pattern;             // TK_PATTERN_CL100K or TK_PATTERN_R50K_DIGITS
 };
 
 // Device scratch of one encode (all sized from max_bytes / max_segments).

@@ -118,7 +118,7 @@ extern "C" int tk_load(const uint8_t* rank_bytes, const int64_t* rank_off, const
   using namespace tk;
   if (!out) return TK_E_ARG;
   *out = nullptr;
-  if (pattern_id != TK_PATTERN_CL100K) {
+  if (pattern_id != TK_PATTERN_CL100K && pattern_id != TK_PATTERN_R50K_DIGITS) {
     tk_set_error("tk_load: unknown pattern_id %d", pattern_id);
     return TK_E_ARG;
   }
@@ -258,6 +258,7 @@ extern "C" int tk_load(const uint8_t* rank_bytes, const int64_t* rank_off, const
     tk_free(tok);
     return rc;
   }
+  t.pattern = pattern_id;
   t.pair_log2 = log2cap;
   t.pair_max_probe = max_probe;
   t.n_spec = (int32_t)n_spec;

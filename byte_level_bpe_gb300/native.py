@@ -21,6 +21,7 @@ TK_E_TIMEOUT = -7
 TK_E_BADID = -8
 TK_E_LIMIT = -9
 TK_PATTERN_CL100K = 1
+TK_PATTERN_R50K_DIGITS = 2
 
 # Every exported function of include/tk.h, with (restype, argtypes).
 _P = ctypes.c_void_p

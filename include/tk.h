@@ -45,7 +45,7 @@ enum {
   TK_E_LIMIT = -9     /* input exceeds the workspace's max_bytes / max_segments */
 };
 
-enum { TK_PATTERN_CL100K = 1 };
+enum { TK_PATTERN_CL100K = 1, TK_PATTERN_R50K_DIGITS = 2 };
 
 /*
  * tk_load -- build a tokenizer from host arrays (copied; the caller may free
@@ -59,7 +59,10 @@ enum { TK_PATTERN_CL100K = 1 };
  *       by exact string outside the merge loop ("Special tokens and the
  *       injection nobody plans for").  May be empty (n_spec = 0).
  *   pattern_id: TK_PATTERN_CL100K, the pattern printed in "tiktoken Deep
- *       Dive", "The split pattern".
+ *       Dive", "The split pattern"; or TK_PATTERN_R50K_DIGITS, the same
+ *       alternation with r50k's digit clause " ?\p{N}++" (an unbounded digit
+ *       run with an optional leading space; "r50k, cl100k, o200k") in place
+ *       of cl100k's \p{N}{1,3}+.
  *
  * Rejected with TK_E_TABLE: a missing single byte ("The byte floor": all 256
  * bytes must be tokens), duplicate token bytes, duplicate ids, ids >= 2^20 - 1,

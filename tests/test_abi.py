@@ -68,7 +68,7 @@ def test_table_validation_is_host_side():
     assert rc == native.TK_E_TABLE and "overlap" in msg
     rc, _ = _load(floor, {b"\xff": 300})  # not UTF-8
     assert rc == native.TK_E_TABLE
-    rc, _ = _load(floor, pattern=2)
+    rc, _ = _load(floor, pattern=3)  # patterns are 1 (cl100k) and 2 (cl100k with r50k digits)
     assert rc == native.TK_E_ARG
 
 

@@ -347,3 +347,28 @@ def test_token_that_does_not_encode_to_itself():
     assert np.array_equal(g_ids.cpu().numpy(), o_ids)
     assert list(enc.encode(b"abcd")) == [ord("a"), 256, ord("d")]
     gpu.close()
+
+
+def test_r50k_digit_clause(full_table):
+    """The split pattern with r50k's digit clause: the agentic prompt (JSON
+    numbers, hex ids), digit/space-heavy random segments, and digit runs that
+    cross tiles and exceed the long-piece thresholds."""
+    import byte_level_bpe_gb300 as tk
+    enc = oracle.Encoding(full_table, workloads.SPECIALS, pattern=oracle.PATTERN_R50K_DIGITS)
+    gpu = tk.Tokenizer(full_table, workloads.SPECIALS, pattern_id=tk.native.TK_PATTERN_R50K_DIGITS,
+                       max_bytes=1 << 24, max_segments=8192)
+    _compare(gpu, enc, workloads.agentic_segments(full_table, seed=3, scale=0.25), True)
+    rng = np.random.default_rng(23)
+    alpha = ["1", "9", "0", " ", "  ", "\t", "\n", "a", "x", "$", ".", "१", "٣", " 12", "'s", "\r\n"]
+    segs = []
+    for _ in range(1500):
+        L = int(rng.integers(0, 40))
+        segs.append(("".join(alpha[i] for i in rng.integers(0, len(alpha), size=L)), bool(rng.integers(0, 2))))
+    _compare(gpu, enc, segs, False)
+    _compare(gpu, enc, segs, True)
+    digits = "".join(str(d) for d in rng.integers(0, 10, size=70000))
+    long_segs = [(digits[:5000], False), (" " + digits[:40000], False), ("a " + digits, False),
+                 (("x " + digits[:3000]) * 5, False), (" " * 3 + digits[:100], False)]
+    _compare(gpu, enc, long_segs, False)
+    _compare(gpu, enc, long_segs, True)
+    gpu.close()
