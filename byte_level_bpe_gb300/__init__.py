@@ -73,6 +73,9 @@ class Tokenizer:
         if getattr(self, "_ws", None):
             native.tk_workspace_free(self._ws)
             self._ws = None
+        if getattr(self, "_cache", None):
+            native.tk_cache_free(self._cache)
+            self._cache = None
         if getattr(self, "_h", None):
             native.tk_free(self._h)
             self._h = None
@@ -91,6 +94,17 @@ class Tokenizer:
     def workspace(self):
         return self._ws
 
+    def attach_cache(self, max_bytes=256 << 20):
+        """A cross-call word cache for this tokenizer's encodes (None: detach)."""
+        if getattr(self, "_cache", None):
+            native.tk_workspace_set_cache(self._ws, None)
+            native.tk_cache_free(self._cache)
+            self._cache = None
+        if max_bytes:
+            self._cache = native.tk_cache_create(self._h, max_bytes)
+            native.tk_workspace_set_cache(self._ws, self._cache)
+        return self._cache
+
     def ensure_workspace(self, max_bytes, max_segments):
         """Grows the workspace (never inside an encode: allocation happens here)."""
         mb, ms = self._ws_cap
@@ -102,6 +116,8 @@ class Tokenizer:
             self._ws = None
         self._ws = native.tk_workspace_create(self._h, mb, ms)
         self._ws_cap = (mb, ms)
+        if getattr(self, "_cache", None):
+            native.tk_workspace_set_cache(self._ws, self._cache)
 
     # ------------------------------------------------------------------
     def pack(self, segments):

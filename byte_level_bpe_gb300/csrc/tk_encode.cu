@@ -1381,7 +1381,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       } else {
         // merged earlier (k_merge_medium / _big / _cluster): ids in the arena, count in cnt[]
         const int g = atomicAdd(&sm.n_gp, 1);
-        const uint32_t src = c.W.gsrc[c.gb + t0 + x];
+        const uint32_t src = c.W.gsrc[c.gb + t0 + x] & ~GSRC_CACHED;
         sm.gp[g] = GPiece{(uint32_t)x, src, c.W.cnt[src], 0u, 0u};
         atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
         sm.cnt[x] = 0;
@@ -1820,7 +1820,10 @@ __global__ void k_dedup_medium(Call c) {
       return (bool)__all_sync(0xffffffffu, same);
     };
     const int64_t src = dedup_claim(c, key, p, len, lane == 0, &s_word[warp], eq, false);
-    if (lane == 0) c.W.gsrc[c.gb + p] = (uint32_t)src;
+    if (lane == 0) {
+      c.W.gsrc[c.gb + p] = (uint32_t)src;
+      c.W.long_key[k] = key;
+    }
   }
 }
 
@@ -1852,7 +1855,144 @@ __global__ void __launch_bounds__(1024) k_dedup_big(Call c) {
       return (bool)__syncthreads_and(same);
     };
     const int64_t src = dedup_claim(c, key, p, len, tid == 0, &s_word, eq, true);
-    if (tid == 0) c.W.gsrc[c.gb + p] = (uint32_t)src;
+    if (tid == 0) {
+      c.W.gsrc[c.gb + p] = (uint32_t)src;
+      if (k < n_big) c.W.big_key[k] = key;
+      else c.W.cl_key[k - n_big] = key;
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// Cross-call word cache.  k_cache_lookup: every distinct listed piece of
+// this call (an owner) whose key, length and bytes match a cache entry takes
+// the entry's ids (gsrc gets GSRC_CACHED, so the merge kernels pass it by).
+// k_cache_insert: every owner merged in this call enters the cache while
+// its capacity lasts.  One warp per listed piece.
+__device__ __forceinline__ bool listed_piece(const Call& c, uint64_t k, int64_t* p, int64_t* len, uint64_t* key) {
+  const uint64_t n_med = c.W.status->n_medium, n_big = c.W.status->n_biglong, n_cl = c.W.status->n_cl;
+  if (k < n_med) {
+    *p = c.W.long_list[2 * k]; *len = c.W.long_list[2 * k + 1]; *key = c.W.long_key[k];
+  } else if (k < n_med + n_big) {
+    k -= n_med;
+    *p = c.W.big_list[2 * k]; *len = c.W.big_list[2 * k + 1]; *key = c.W.big_key[k];
+  } else if (k < n_med + n_big + n_cl) {
+    k -= n_med + n_big;
+    *p = c.W.cl_list[2 * k]; *len = c.W.cl_list[2 * k + 1]; *key = c.W.cl_key[k];
+  } else {
+    return false;
+  }
+  return true;
+}
+
+// Group-wide compare of a piece's bytes with a cache entry and copy of its
+// ids (a warp for pieces of up to MEDIUM_MAX bytes, a CTA beyond): no early
+// exit, so the loads of many positions are in flight at once.
+template <bool CTA>
+__device__ void cache_probe(const Call& c, int64_t G, int64_t len, uint64_t key, uint64_t* s_ref) {
+  const CacheDev& C = c.W.cache;
+  const uint64_t mask = (1ull << C.slot_log2) - 1;
+  const int t = CTA ? (int)threadIdx.x : (int)(threadIdx.x & 31);
+  const int nt = CTA ? (int)blockDim.x : 32;
+  uint64_t slot = key & mask;
+  for (int probe = 0; probe < 64; probe++, slot = (slot + 1) & mask) {
+    // one thread reads the slot; all share (entry + 1, or 0 to stop, or ~0 to go on)
+    if (t == 0) {
+      const uint64_t sk = C.slots[2 * slot];
+      uint64_t r = 0;
+      if (sk != 0) {
+        r = ~0ull;
+        const uint64_t ref = sk == key ? C.slots[2 * slot + 1] : 0;
+        if (ref && (int64_t)C.entries[ref - 1].len == len) r = ref;
+      }
+      *s_ref = r;
+    }
+    if (CTA) __syncthreads();
+    else __syncwarp();
+    const uint64_t ref = *s_ref;
+    if (CTA) __syncthreads();
+    else __syncwarp();
+    if (ref == 0) return;  // not cached
+    if (ref == ~0ull) continue;
+    const CacheEntry e = C.entries[ref - 1];
+    bool same = true;
+    for (int64_t q = t; q < len; q += nt) same &= C.bytes[e.byte_off + q] == text_at(c, G + q);
+    const bool all = CTA ? __syncthreads_and(same) : __all_sync(0xffffffffu, same);
+    if (!all) continue;
+    for (uint32_t j = t; j < e.n_ids; j += nt) c.W.arena[G + j] = C.ids[e.id_off + j];
+    if (t == 0) {
+      c.W.cnt[G] = e.n_ids;
+      c.W.gsrc[G] = (uint32_t)G | GSRC_CACHED;
+      atomicAdd(&c.W.status->n_cache_hits, 1u);
+    }
+    return;
+  }
+}
+
+// Pieces of up to MEDIUM_MAX bytes: one warp each.
+__global__ void k_cache_lookup(Call c) {
+  __shared__ uint64_t s_ref[ETHREADS / 32];
+  const uint64_t gw = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) >> 5;
+  const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+  const uint64_t n_med = c.W.status->n_medium;
+  for (uint64_t k = gw; k < n_med; k += nw) {
+    const int64_t p = c.W.long_list[2 * k], len = c.W.long_list[2 * k + 1];
+    const int64_t G = c.gb + p;
+    if (c.W.gsrc[G] != (uint32_t)G) continue;  // a copy of another piece of this call
+    cache_probe<false>(c, G, len, c.W.long_key[k], &s_ref[threadIdx.x >> 5]);
+  }
+}
+
+// Longer pieces: one CTA each.
+__global__ void __launch_bounds__(1024) k_cache_lookup_big(Call c) {
+  __shared__ uint64_t s_ref;
+  const uint64_t n_big = c.W.status->n_biglong, n_cl = c.W.status->n_cl;
+  for (uint64_t k = blockIdx.x; k < n_big + n_cl; k += gridDim.x) {
+    const uint32_t* ent = k < n_big ? &c.W.big_list[2 * k] : &c.W.cl_list[2 * (k - n_big)];
+    const uint64_t key = k < n_big ? c.W.big_key[k] : c.W.cl_key[k - n_big];
+    const int64_t G = c.gb + ent[0], len = ent[1];
+    if (c.W.gsrc[G] != (uint32_t)G) continue;
+    cache_probe<true>(c, G, len, key, &s_ref);
+  }
+}
+
+__global__ void k_cache_insert(Call c) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t gw = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) >> 5;
+  const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+  const CacheDev& C = c.W.cache;
+  const uint64_t mask = (1ull << C.slot_log2) - 1;
+  int64_t p, len;
+  uint64_t key;
+  for (uint64_t k = gw; listed_piece(c, k, &p, &len, &key); k += nw) {
+    const int64_t G = c.gb + p;
+    if (c.W.gsrc[G] != (uint32_t)G) continue;  // a copy, or taken from the cache
+    const uint32_t n_ids = c.W.cnt[G];
+    // reserve an entry, the bytes and the ids (a failed reservation is not
+    // returned: the cache counts as full from then on)
+    unsigned long long e = 0, bo = 0, io = 0;
+    if (lane == 0) {
+      e = atomicAdd(&C.used[0], 1ull);
+      bo = atomicAdd(&C.used[1], (unsigned long long)len);
+      io = atomicAdd(&C.used[2], (unsigned long long)n_ids);
+    }
+    e = __shfl_sync(0xffffffffu, e, 0);
+    bo = __shfl_sync(0xffffffffu, bo, 0);
+    io = __shfl_sync(0xffffffffu, io, 0);
+    if (e >= C.max_entries || bo + len > C.max_bytes || io + n_ids > C.max_ids) continue;
+    for (int64_t q = lane; q < len; q += 32) C.bytes[bo + q] = text_at(c, G + q);
+    for (uint32_t j = lane; j < n_ids; j += 32) C.ids[io + j] = c.W.arena[G + j];
+    if (lane == 0) {
+      C.entries[e] = CacheEntry{bo, io, (uint32_t)len, n_ids};
+      uint64_t slot = key & mask;
+      for (int probe = 0; probe < 64; probe++, slot = (slot + 1) & mask) {
+        if (atomicCAS(&C.slots[2 * slot], 0ull, (unsigned long long)key) == 0ull) {
+          C.slots[2 * slot + 1] = e + 1;  // read by later calls only (stream order)
+          atomicAdd(&c.W.status->n_cache_inserts, 1u);
+          break;
+        }
+      }
+    }
   }
 }
 
@@ -2026,8 +2166,8 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
     return TK_E_ARG;
   }
   *out = nullptr;
-  if (max_bytes > (int64_t)PTOK_MASK - 16) {
-    tk_set_error("tk_workspace_create: max_bytes %lld above 2^31 - 17", (long long)max_bytes);
+  if (max_bytes > (int64_t)PTOK_MASK - 1023) {  // positions (with batch padding) stay below 2^31
+    tk_set_error("tk_workspace_create: max_bytes %lld above 2^31 - 1024", (long long)max_bytes);
     return TK_E_LIMIT;
   }
   tk_workspace* ws = new (std::nothrow) tk_workspace();
@@ -2080,6 +2220,9 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.lsel, (size_t)nbp},
       {(void**)&w.lchg, (size_t)nbp},
       {(void**)&w.huge_list, sizeof(uint64_t) * 3 * (nb / HUGE_IDS + 2)},
+      {(void**)&w.long_key, sizeof(uint64_t) * (nb / (SHORT_MAX + 1) + 2)},
+      {(void**)&w.big_key, sizeof(uint64_t) * (nb / (MEDIUM_MAX + 1) + 2)},
+      {(void**)&w.cl_key, sizeof(uint64_t) * (nb / (CLUSTER_MIN + 1) + 2)},
       {(void**)&ws->d_stage_text, (size_t)nb + 16 * (tk_workspace::PIPE_MAX + 2)},
       {(void**)&ws->d_stage_off, sizeof(int64_t) * (max_segments + 1 + tk_workspace::PIPE_MAX)},
       {(void**)&ws->d_stage_allow, (size_t)max_segments + 1},
@@ -2157,6 +2300,8 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   c.safe = safe ? 1 : 0;
   c.T = tok->t;
   c.W = ws->w;
+  c.W.use_cache = ws->cache ? 1 : 0;
+  if (ws->cache) c.W.cache = ws->cache->d;
   const int64_t n_split_tiles = (n + TILE - 1) / TILE;
   const int64_t n_scan_tiles = (n + 1 + SCAN_TILE - 1) / SCAN_TILE + 1;
   const int64_t cut_words = (n + 64) / 32 + 1;
@@ -2192,12 +2337,22 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     k_dedup_medium<<<sms * 8, ETHREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_dedup_big", st);
     k_dedup_big<<<sms, 1024, 0, st>>>(c);
+    if (c.W.use_cache) {
+      tk_prof_mark(ws, "k_cache_lookup", st);
+      k_cache_lookup<<<sms * 8, ETHREADS, 0, st>>>(c);
+      tk_prof_mark(ws, "k_cache_lookup_big", st);
+      k_cache_lookup_big<<<sms, 1024, 0, st>>>(c);
+    }
     tk_prof_mark(ws, "k_merge_big", st);
     k_merge_big<<<sms, BIG_THREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_merge_cluster", st);
     k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), BIG_THREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_merge_medium", st);
     k_merge_medium<<<sms * 4, ETHREADS, 0, st>>>(c);
+    if (c.W.use_cache) {
+      tk_prof_mark(ws, "k_cache_insert", st);
+      k_cache_insert<<<sms * 8, ETHREADS, 0, st>>>(c);
+    }
     tk_prof_mark(ws, "k_encode_tiles", st);
     k_encode_tiles<<<enc_grid, ETHREADS, sizeof(EncSmem), st>>>(c);
     tk_prof_mark(ws, "k_scan_u32", st);
@@ -2249,6 +2404,13 @@ static int encode_device(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   tk_prof_finish(ws, st);
   if (h_n_ids) *h_n_ids = ws->h_status->n_ids;
   return encode_result(*ws->h_status, cap, 0);
+}
+
+extern "C" int tk_last_cache_stats(const tk_workspace* ws, int64_t* hits, int64_t* inserts) {
+  if (!ws) return TK_E_ARG;
+  if (hits) *hits = ws->h_status->n_cache_hits;
+  if (inserts) *inserts = ws->h_status->n_cache_inserts;
+  return TK_OK;
 }
 
 extern "C" int tk_last_stats(const tk_workspace* ws, int64_t* n_pretokens, int64_t* n_ids,
@@ -2407,6 +2569,8 @@ extern "C" int tk_encode_segments_host(const tk_tokenizer* tok, tk_workspace* ws
     if (brc && !first_rc) first_rc = brc;
     sum.n_ptok += hs.n_ptok;
     sum.n_long += hs.n_long;
+    sum.n_cache_hits += hs.n_cache_hits;
+    sum.n_cache_inserts += hs.n_cache_inserts;
     if (!first_rc && hs.n_ids && total + hs.n_ids <= out_capacity)
       TK_CUDA(cudaMemcpyAsync(h_out_ids + total, ws->d_stage_ids + b0, sizeof(int32_t) * hs.n_ids,
                               cudaMemcpyDeviceToHost, ws->s_d2h), "d2h ids");
@@ -2422,5 +2586,95 @@ extern "C" int tk_encode_segments_host(const tk_tokenizer* tok, tk_workspace* ws
     tk_set_error("output capacity %lld < %lld ids", (long long)out_capacity, (long long)total);
     return TK_E_CAPACITY;
   }
+  return TK_OK;
+}
+
+// --------------------------------------------------------------------------
+// Cross-call word cache: host API.
+extern "C" int tk_cache_create(const tk_tokenizer* tok, int64_t max_bytes, tk_cache** out) {
+  using namespace tk;
+  if (!tok || !out || max_bytes < SHORT_MAX + 1) {
+    tk_set_error("tk_cache_create: bad argument (max_bytes must be at least %d)", SHORT_MAX + 1);
+    return TK_E_ARG;
+  }
+  *out = nullptr;
+  tk_cache* cc = new (std::nothrow) tk_cache();
+  if (!cc) return TK_E_NOMEM;
+  cc->tok = tok;
+  cc->device = tok->device;
+  cudaSetDevice(tok->device);
+  CacheDev& d = cc->d;
+  d.max_bytes = (uint64_t)max_bytes;
+  d.max_ids = (uint64_t)max_bytes;  // a piece never has more ids than bytes
+  d.max_entries = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)max_bytes / (SHORT_MAX + 1), 1ull << 24));
+  d.slot_log2 = 4;
+  while ((1ull << d.slot_log2) < 2 * d.max_entries) d.slot_log2++;
+  struct Req { void** p; size_t bytes; };
+  Req reqs[] = {
+      {(void**)&d.slots, sizeof(unsigned long long) * 2 * ((size_t)1 << d.slot_log2)},
+      {(void**)&d.entries, sizeof(CacheEntry) * (size_t)d.max_entries},
+      {(void**)&d.bytes, (size_t)d.max_bytes},
+      {(void**)&d.ids, sizeof(int32_t) * (size_t)d.max_ids},
+      {(void**)&d.used, sizeof(unsigned long long) * 3},
+  };
+  static_assert(sizeof(reqs) / sizeof(reqs[0]) <= tk_cache::MAX_DEV, "cache buffer table");
+  for (auto& r : reqs) {
+    if (cudaMalloc(r.p, r.bytes) != cudaSuccess) {
+      tk_set_error("tk_cache_create: cudaMalloc(%zu) failed", r.bytes);
+      tk_cache_free(cc);
+      return TK_E_NOMEM;
+    }
+    cc->dev_mem[cc->n_dev++] = *r.p;
+  }
+  if (cudaMemset(d.slots, 0, sizeof(unsigned long long) * 2 * ((size_t)1 << d.slot_log2)) != cudaSuccess ||
+      cudaMemset(d.used, 0, sizeof(unsigned long long) * 3) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    tk_set_error("tk_cache_create: clearing the cache failed");
+    tk_cache_free(cc);
+    return TK_E_CUDA;
+  }
+  *out = cc;
+  return TK_OK;
+}
+
+extern "C" void tk_cache_free(tk_cache* cc) {
+  if (!cc) return;
+  for (int i = 0; i < cc->n_dev; i++) cudaFree(cc->dev_mem[i]);
+  delete cc;
+}
+
+extern "C" int tk_cache_clear(tk_cache* cc, void* cuda_stream) {
+  if (!cc) return TK_E_ARG;
+  cudaSetDevice(cc->device);
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  cudaError_t e = cudaMemsetAsync(cc->d.slots, 0, sizeof(unsigned long long) * 2 * ((size_t)1 << cc->d.slot_log2), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(cc->d.used, 0, sizeof(unsigned long long) * 3, st);
+  if (e != cudaSuccess) {
+    tk_set_error("tk_cache_clear: %s", cudaGetErrorString(e));
+    return TK_E_CUDA;
+  }
+  return TK_OK;
+}
+
+extern "C" int tk_cache_stats(const tk_cache* cc, int64_t* n_entries, int64_t* bytes_used, int64_t* ids_used) {
+  if (!cc) return TK_E_ARG;
+  cudaSetDevice(cc->device);
+  unsigned long long u[3] = {0, 0, 0};
+  if (cudaMemcpy(u, cc->d.used, sizeof(u), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    tk_set_error("tk_cache_stats: copy failed");
+    return TK_E_CUDA;
+  }
+  // reservations past the capacity did not take effect
+  if (n_entries) *n_entries = (int64_t)std::min<unsigned long long>(u[0], cc->d.max_entries);
+  if (bytes_used) *bytes_used = (int64_t)std::min<unsigned long long>(u[1], cc->d.max_bytes);
+  if (ids_used) *ids_used = (int64_t)std::min<unsigned long long>(u[2], cc->d.max_ids);
+  return TK_OK;
+}
+
+extern "C" int tk_workspace_set_cache(tk_workspace* ws, tk_cache* cc) {
+  if (!ws || (cc && cc->tok != ws->tok)) {
+    tk_set_error("tk_workspace_set_cache: the cache belongs to another tokenizer");
+    return TK_E_ARG;
+  }
+  ws->cache = cc;
   return TK_OK;
 }

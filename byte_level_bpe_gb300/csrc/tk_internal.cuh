@@ -58,6 +58,8 @@ struct Status {
   uint32_t cl_next;
   int32_t holdback;      // streaming decode: bytes held back at the end
   uint32_t tail;         // ... and those bytes, little-endian
+  uint32_t n_cache_hits;     // long pieces found in the cross-call cache
+  uint32_t n_cache_inserts;  // long pieces added to it
   uint32_t tile_ctr[8];  // dynamic tile counters of the persistent kernels
   int64_t n_tiles;       // split tiles of this call (element count of the tile scan)
 };
@@ -80,6 +82,24 @@ struct Tables {
   int64_t max_id;
   int32_t pattern;             // TK_PATTERN_CL100K or TK_PATTERN_R50K_DIGITS
 };
+
+// Cross-call word cache: merged ids of pre-tokens over SHORT_MAX bytes, kept
+// between calls.  An entry holds the piece's bytes and ids; a slot maps the
+// dedup key of the bytes to entry index + 1 (key 0 = empty slot).
+struct CacheEntry {
+  uint64_t byte_off, id_off;
+  uint32_t len, n_ids;
+};
+struct CacheDev {
+  unsigned long long* slots;  // [2 << slot_log2]: key, entry + 1
+  CacheEntry* entries;
+  uint8_t* bytes;
+  int32_t* ids;
+  unsigned long long* used;   // [3]: entries, bytes, ids reserved so far
+  uint32_t slot_log2;
+  uint64_t max_entries, max_bytes, max_ids;
+};
+constexpr uint32_t GSRC_CACHED = 0x80000000u;  // gsrc flag: an owner whose ids came from the cache
 
 // Device scratch of one encode (all sized from max_bytes / max_segments).
 struct Work {
@@ -118,6 +138,11 @@ struct Work {
   uint8_t* lchg;        // [max_bytes] long merge: changed flags
   uint64_t* huge_list;  // (output position, arena start, id count) of the long pieces
                         // whose ids the whole grid copies
+  uint64_t* long_key;   // dedup key of each long_list / big_list / cl_list entry
+  uint64_t* big_key;
+  uint64_t* cl_key;
+  CacheDev cache;       // the attached cross-call cache (use_cache) ...
+  int use_cache;
   int64_t max_bytes;
   int64_t max_segments;
 };
@@ -305,10 +330,20 @@ struct tk_profile {
   int n_pending;
 };
 
+struct tk_cache {
+  tk::CacheDev d;
+  const tk_tokenizer* tok;
+  static constexpr int MAX_DEV = 8;
+  void* dev_mem[MAX_DEV];
+  int n_dev;
+  int device;
+};
+
 struct tk_workspace {
   tk::Work w;
   tk_profile prof;
   const tk_tokenizer* tok;
+  tk_cache* cache;  // attached cross-call cache, or null
   static constexpr int MAX_DEV = 64;
   void* dev_mem[MAX_DEV];
   int n_dev;

@@ -48,6 +48,12 @@ SIGNATURES = {
                                ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)]),
     "tk_last_stats": (_INT, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                              ctypes.POINTER(_I64)]),
+    "tk_cache_create": (_INT, [_P, _I64, ctypes.POINTER(_P)]),
+    "tk_cache_free": (None, [_P]),
+    "tk_cache_clear": (_INT, [_P, _P]),
+    "tk_cache_stats": (_INT, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "tk_workspace_set_cache": (_INT, [_P, _P]),
+    "tk_last_cache_stats": (_INT, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "tk_status_string": (ctypes.c_char_p, [_INT]),
     "tk_last_error": (ctypes.c_char_p, []),
 }
@@ -204,3 +210,36 @@ def tk_decode_segments(tok, ws, d_ids, n, d_id_off, S, d_out, cap, d_byte_off, s
     if raise_on_error:
         check(rc, "tk_decode_segments")
     return rc, m.value
+
+
+def tk_cache_create(tok, max_bytes):
+    h = _P()
+    check(load().tk_cache_create(tok, max_bytes, ctypes.byref(h)), "tk_cache_create")
+    return h
+
+
+def tk_cache_free(cache):
+    if cache:
+        load().tk_cache_free(cache)
+
+
+def tk_cache_clear(cache, stream):
+    check(load().tk_cache_clear(cache, stream), "tk_cache_clear")
+
+
+def tk_cache_stats(cache):
+    """-> (entries, bytes, ids) held by the cache."""
+    a, b, c = _I64(0), _I64(0), _I64(0)
+    check(load().tk_cache_stats(cache, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "tk_cache_stats")
+    return a.value, b.value, c.value
+
+
+def tk_workspace_set_cache(ws, cache):
+    check(load().tk_workspace_set_cache(ws, cache), "tk_workspace_set_cache")
+
+
+def tk_last_cache_stats(ws):
+    """-> (pieces found in the cache, pieces added) by the workspace's last encode."""
+    a, b = _I64(0), _I64(0)
+    check(load().tk_last_cache_stats(ws, ctypes.byref(a), ctypes.byref(b)), "tk_last_cache_stats")
+    return a.value, b.value

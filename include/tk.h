@@ -18,7 +18,7 @@
  *     outputs unspecified on error.  tk_last_error() gives a one-line message
  *     for the calling thread's last failure.
  *   - Ids are int32; token byte offsets are int64.  Texts are limited to
- *     2^31 - 1 bytes per call.
+ *     2^31 - 1024 bytes per call.
  */
 #ifndef TK_H
 #define TK_H
@@ -215,6 +215,34 @@ int tk_decode_stream(const tk_tokenizer* tok, tk_workspace* ws, tk_decode_state*
  */
 int tk_decode_noalloc(const tk_tokenizer* tok, const int32_t* d_ids, int64_t n, uint8_t* d_out,
                       int64_t cap, int64_t* h_len, void* cuda_stream);
+
+/*
+ * Cross-call word cache ("Making Kimi K3 Tokenization 18x Faster ...", "Where
+ * the speed comes from": repeated words are merged once; "tokenizers v1",
+ * "Key Technical Improvements": a word cache).  Within one call every
+ * pre-token over 16 bytes is merged once per distinct byte string; a cache
+ * keeps those merges between calls, for agent loops that resend most of
+ * their prompt.  A hit returns the ids merged earlier for the same bytes and
+ * the same tokenizer, so results never change.
+ *
+ *   tk_cache_create: device memory for max_bytes bytes of cached pieces (and
+ *       as many ids, plus an index); nothing is evicted: once full, new
+ *       pieces are merged but not added.  The cache belongs to tok.
+ *   tk_workspace_set_cache: encodes on ws look pieces up in cache (before
+ *       merging) and add the ones they merged (after); NULL detaches.  Encodes
+ *       that share a cache must not overlap in time.
+ *   tk_cache_clear: empties it (on cuda_stream).  tk_cache_stats: entries,
+ *       bytes and ids held (synchronises the device).
+ *   tk_last_cache_stats: pieces the workspace's last encode found in the
+ *       cache and added to it.
+ */
+typedef struct tk_cache tk_cache;
+int tk_cache_create(const tk_tokenizer* tok, int64_t max_bytes, tk_cache** out);
+void tk_cache_free(tk_cache* cache);
+int tk_cache_clear(tk_cache* cache, void* cuda_stream);
+int tk_cache_stats(const tk_cache* cache, int64_t* n_entries, int64_t* bytes_used, int64_t* ids_used);
+int tk_workspace_set_cache(tk_workspace* ws, tk_cache* cache);
+int tk_last_cache_stats(const tk_workspace* ws, int64_t* hits, int64_t* inserts);
 
 /*
  * Per-kernel timing of encodes on a workspace, for benchmarks.  With
