@@ -1260,7 +1260,10 @@ struct EncSmem {
   uint8_t plen[TILE];                   // length of the short piece starting at each byte
   uint32_t cls_cnt[2 * N_CLASSES + 1];  // work list: class starts [0..N], then fill cursors
   int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
-  uint16_t list[TILE + SHORT_MAX];      // work list: x | (len - 1) << 12
+  union {
+    uint16_t list[TILE + SHORT_MAX];    // work list: x | (len - 1) << 12 (until the merges end)
+    __align__(16) int32_t outs[TILE + SHORT_MAX + 4];  // then the tile's short ids in order
+  };
   GPiece gp[MAX_GP];
   uint32_t th_full[ETHREADS];
   uint32_t warp_tot[2 * ETHREADS / 32];
@@ -1473,8 +1476,8 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       th_short = sm.warp_tot[ETHREADS / 32 + warp] + b - my_short;
     }
     __syncthreads();
-    // 5. compaction of short ids into the tile's staging slot (in order);
-    //    offsets of the global pieces
+    // 5. compaction of short ids (in order, in shared memory); offsets of
+    //    the global pieces
     uint32_t* slot = c.W.staging + tile * STG;
     {
       uint32_t f = sm.th_full[tid], s = th_short;
@@ -1490,14 +1493,18 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
           continue;
         }
         const uint32_t m = sm.cnt[x];
-        for (uint32_t j = 0; j < m; j++) slot[s + j] = (uint32_t)sm.stage[x + j];
+        for (uint32_t j = 0; j < m; j++) sm.outs[s + j] = sm.stage[x + j];
         s += m;
         f += m;
       }
     }
     __syncthreads();
-    // 6. the table of pieces merged through global memory at the slot's end;
-    //    the tile's id count; segment offsets relative to the tile
+    // 6. the short ids to the staging slot (16-byte stores: the slot has room
+    //    for the rounding before its long-piece table), the table of pieces
+    //    merged through global memory at the slot's end; the tile's id count;
+    //    segment offsets relative to the tile
+    for (uint32_t v = tid; 4 * v < sm.tile_short; v += ETHREADS)
+      reinterpret_cast<uint4*>(slot)[v] = reinterpret_cast<const uint4*>(sm.outs)[v];
     for (int g = tid; g < ngp; g += ETHREADS) {
       uint32_t* e = slot + STG - 4 * (g + 1);
       e[0] = sm.gp[g].short_excl;
