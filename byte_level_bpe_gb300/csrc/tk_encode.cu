@@ -1112,6 +1112,7 @@ struct CGroup {
 template <class Grp>
 __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t n) {
   constexpr int NW = Grp::kWarps;
+  constexpr int U = 4;  // 32-element strips per batch: U loads in flight per lane
   const int64_t G = c.gb + s;
   uint32_t* A_ids = reinterpret_cast<uint32_t*>(c.W.arena + G);
   uint32_t* A_rk = c.W.lrk + G;
@@ -1130,84 +1131,148 @@ __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t 
   g.sync();
   bool in_b = false;
   for (int64_t round = 0;; round++) {
+    // each warp owns [wlo, whi): whole strips of 32, lanes on consecutive parts
     const int64_t cw = (((n + NW - 1) / NW) + 31) & ~(int64_t)31;
     const int64_t wlo = min(n, (int64_t)w * cw), whi = min(n, wlo + cw);
     // (1) the minimum pair rank
     uint32_t m = RANK_MAX;
-#pragma unroll 4
-    for (int64_t i = wlo + lane; i < whi; i += 32) m = min(m, g.ld(&A_rk[i]));
+    for (int64_t b0 = wlo; b0 < whi; b0 += 32 * U) {
+      uint32_t v[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        v[u] = i < whi ? g.ld(&A_rk[i]) : RANK_MAX;
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) m = min(m, v[u]);
+    }
     const uint32_t rs = g.gmin(m);
     if (rs == RANK_MAX) break;
     // (2) chains of rs-pairs: every other pair from each chain's start.  The
     //     last non-candidate before each part comes from ballots and a carry.
     int64_t ln_w = -1;
-#pragma unroll 4
-    for (int64_t b = wlo; b < whi; b += 32) {
-      const int64_t i = b + lane;
-      const uint32_t nm = __ballot_sync(0xffffffffu, i < whi && g.ld(&A_rk[i]) != rs);
-      if (nm) ln_w = b + 31 - __clz(nm);
+    for (int64_t b0 = wlo; b0 < whi; b0 += 32 * U) {
+      uint32_t v[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        v[u] = i < whi ? g.ld(&A_rk[i]) : rs;
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const uint32_t nm = __ballot_sync(0xffffffffu, v[u] != rs);
+        if (nm) ln_w = b0 + 32 * u + 31 - __clz(nm);
+      }
     }
     int64_t tot;
     int64_t carry = g.warp_excl(ln_w, 1, &tot);
     if (carry < -1) carry = -1;
-#pragma unroll 4
-    for (int64_t b = wlo; b < whi; b += 32) {
-      const int64_t i = b + lane;
-      const bool in = i < whi;
-      const bool cand = in && g.ld(&A_rk[i]) == rs;
-      const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
-      const uint32_t before = nm & lt;
-      const int64_t ln = before ? b + 31 - __clz(before) : carry;
-      if (in) sel[i] = cand && (((i - ln - 1) & 1) == 0);
-      if (nm) carry = b + 31 - __clz(nm);
+    for (int64_t b0 = wlo; b0 < whi; b0 += 32 * U) {
+      uint32_t v[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        v[u] = i < whi ? g.ld(&A_rk[i]) : rs;
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t b = b0 + 32 * u, i = b + lane;
+        const bool in = i < whi;
+        const bool cand = in && v[u] == rs;
+        const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
+        const uint32_t before = nm & lt;
+        const int64_t ln = before ? b + 31 - __clz(before) : carry;
+        if (in) sel[i] = cand && (((i - ln - 1) & 1) == 0);
+        if (nm) carry = b + 31 - __clz(nm);
+      }
     }
     g.sync();
     // (3) the first selected merge that creates a neighbour pair of lower rank
     uint32_t fb = 0xFFFFFFFFu;
-    for (int64_t b = wlo; b < whi && fb == 0xFFFFFFFFu; b += 32) {
-      const int64_t i = b + lane;
-      bool bad = false;
-      if (i < whi && g.ld(&sel[i])) {
-        if (i >= 1) {
-          const uint32_t left = (i >= 2 && g.ld(&sel[i - 2])) ? rs : g.ld(&A_ids[i - 1]);
-          bad = pair_rank(c.T, left, rs) < rs;
-        }
-        if (!bad && i + 2 < n) bad = pair_rank(c.T, rs, g.ld(&A_ids[i + 2])) < rs;
+    for (int64_t b0 = wlo; b0 < whi && fb == 0xFFFFFFFFu; b0 += 32 * U) {
+      uint8_t sv[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        sv[u] = i < whi ? g.ld(&sel[i]) : 0;
       }
-      const uint32_t bm = __ballot_sync(0xffffffffu, bad);
-      if (bm) fb = (uint32_t)(b + __ffs(bm) - 1);
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        bool bad = false;
+        if (sv[u]) {
+          const uint32_t left = i >= 1 ? ((i >= 2 && g.ld(&sel[i - 2])) ? rs : g.ld(&A_ids[i - 1])) : 0u;
+          const uint32_t right = i + 2 < n ? g.ld(&A_ids[i + 2]) : 0u;
+          const uint32_t rl = i >= 1 ? pair_rank(c.T, left, rs) : RANK_MAX;
+          const uint32_t rr = i + 2 < n ? pair_rank(c.T, rs, right) : RANK_MAX;
+          bad = rl < rs || rr < rs;
+        }
+        const uint32_t bm = __ballot_sync(0xffffffffu, bad);
+        if (bm && fb == 0xFFFFFFFFu) fb = (uint32_t)(b0 + 32 * u + __ffs(bm) - 1);
+      }
     }
     const uint32_t limit = g.gmin(fb);
     // (4) merge the selected pairs up to limit, compacting into B
     int64_t keep_w = 0;
-#pragma unroll 4
-    for (int64_t b = wlo; b < whi; b += 32) {
-      const int64_t i = b + lane;
-      const bool kp = i < whi && !(i >= 1 && g.ld(&sel[i - 1]) && (uint64_t)(i - 1) <= (uint64_t)limit);
-      keep_w += __popc(__ballot_sync(0xffffffffu, kp));
+    for (int64_t b0 = wlo; b0 < whi; b0 += 32 * U) {
+      uint8_t pv[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        pv[u] = (i < whi && i >= 1) ? g.ld(&sel[i - 1]) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        const bool kp = i < whi && !(pv[u] && (uint64_t)(i - 1) <= (uint64_t)limit);
+        keep_w += __popc(__ballot_sync(0xffffffffu, kp));
+      }
     }
     int64_t dst = g.warp_excl(keep_w, 0, &tot);
     const int64_t n2 = tot;
-#pragma unroll 4
-    for (int64_t b = wlo; b < whi; b += 32) {
-      const int64_t i = b + lane;
-      const bool kp = i < whi && !(i >= 1 && g.ld(&sel[i - 1]) && (uint64_t)(i - 1) <= (uint64_t)limit);
-      const uint32_t km = __ballot_sync(0xffffffffu, kp);
-      if (kp) {
-        const int64_t pos = dst + __popc(km & lt);
-        const bool merged = g.ld(&sel[i]) && (uint64_t)i <= (uint64_t)limit;
-        B_ids[pos] = merged ? rs : g.ld(&A_ids[i]);
-        B_rk[pos] = g.ld(&A_rk[i]);
-        chg[pos] = merged;
+    for (int64_t b0 = wlo; b0 < whi; b0 += 32 * U) {
+      uint8_t pv[U], sv[U];
+      uint32_t iv[U], rv[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        const bool in = i < whi;
+        pv[u] = (in && i >= 1) ? g.ld(&sel[i - 1]) : 0;
+        sv[u] = in ? g.ld(&sel[i]) : 0;
+        iv[u] = in ? g.ld(&A_ids[i]) : 0u;
+        rv[u] = in ? g.ld(&A_rk[i]) : 0u;
       }
-      dst += __popc(km);
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t i = b0 + 32 * u + lane;
+        const bool kp = i < whi && !(pv[u] && (uint64_t)(i - 1) <= (uint64_t)limit);
+        const uint32_t km = __ballot_sync(0xffffffffu, kp);
+        if (kp) {
+          const int64_t pos = dst + __popc(km & lt);
+          const bool merged = sv[u] && (uint64_t)i <= (uint64_t)limit;
+          B_ids[pos] = merged ? rs : iv[u];
+          B_rk[pos] = rv[u];
+          chg[pos] = merged;
+        }
+        dst += __popc(km);
+      }
     }
     g.sync();
     // (5) re-rank the pairs next to merged pieces
-#pragma unroll 4
-    for (int64_t q = (int64_t)w * 32 + lane; q < n2; q += NW * 32) {
-      if (q + 1 >= n2) B_rk[q] = RANK_MAX;
-      else if (g.ld(&chg[q]) || g.ld(&chg[q + 1])) B_rk[q] = pair_rank(c.T, g.ld(&B_ids[q]), g.ld(&B_ids[q + 1]));
+    for (int64_t q0 = (int64_t)w * 32; q0 < n2; q0 += (int64_t)NW * 32 * U) {
+      uint8_t c0[U], c1[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t q = q0 + (int64_t)NW * 32 * u + lane;
+        c0[u] = q < n2 ? g.ld(&chg[q]) : 0;
+        c1[u] = q + 1 < n2 ? g.ld(&chg[q + 1]) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t q = q0 + (int64_t)NW * 32 * u + lane;
+        if (q + 1 == n2) B_rk[q] = RANK_MAX;
+        else if (q + 1 < n2 && (c0[u] || c1[u])) B_rk[q] = pair_rank(c.T, g.ld(&B_ids[q]), g.ld(&B_ids[q + 1]));
+      }
     }
     g.sync();
     uint32_t* t1 = A_ids; A_ids = B_ids; B_ids = t1;
