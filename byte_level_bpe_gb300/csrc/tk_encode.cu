@@ -1376,11 +1376,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const bool aligned = ((uintptr_t)c.text & 15) == 0;
-  for (;;) {
-    if (tid == 0) sm.tile = atomicAdd(&c.W.status->tile_ctr[4], 1u);
-    __syncthreads();
-    const int64_t tile = sm.tile;
-    if (tile >= ntiles) break;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int64_t t0 = tile * TILE;
     // 1. bytes, start bits (positions >= n read as no start), special starts
     for (int v = tid; v < (TILE + EPAD + 16) / 16; v += ETHREADS) {
@@ -1447,10 +1443,10 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
         sm.plen[x] = (uint8_t)len;
         atomicAdd(&sm.cls_cnt[len_class((int)len)], 1u);
       } else {
-        // merged earlier (k_merge_medium / _big / _cluster): ids in the arena, count in cnt[]
+        // merged by the long-piece kernels, which may still be running: the
+        // tile records where the piece is; k_long_fixup adds its ids' count
         const int g = atomicAdd(&sm.n_gp, 1);
-        const uint32_t src = c.W.gsrc[c.gb + t0 + x] & ~GSRC_CACHED;
-        sm.gp[g] = GPiece{(uint32_t)x, src, c.W.cnt[src], 0u, 0u};
+        sm.gp[g] = GPiece{(uint32_t)x, 0u, 0u, 0u, 0u};
         atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
         sm.cnt[x] = 0;
       }
@@ -1508,13 +1504,8 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       if (ngp) atomicAdd(&c.W.status->n_long, (uint32_t)ngp);
     }
     // 4. per-thread totals -> block scan -> tile total -> look-back
+    // (the counts below leave out the long pieces; k_long_fixup adds them)
     uint32_t my_full = my_short, th_short = 0;
-    for (uint32_t bits = my; bits; bits &= bits - 1) {
-      const int x = xb + __ffs(bits) - 1;
-      if ((sm.gb[x >> 5] >> (x & 31)) & 1u)
-        for (int g = 0; g < ngp; g++)
-          if ((int)sm.gp[g].rel == x) my_full += sm.gp[g].cnt;
-    }
     {
       uint32_t a = my_full, b = my_short;
       for (int o = 1; o < 32; o <<= 1) {
@@ -1573,9 +1564,9 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     for (int g = tid; g < ngp; g += ETHREADS) {
       uint32_t* e = slot + STG - 4 * (g + 1);
       e[0] = sm.gp[g].short_excl;
-      e[1] = sm.gp[g].full_excl;
-      e[2] = sm.gp[g].src;
-      e[3] = sm.gp[g].cnt;
+      e[1] = sm.gp[g].rel;  // k_long_fixup: full_excl, src, cnt
+      e[2] = 0;
+      e[3] = 0;
     }
     if (tid == 0) {
       c.W.tile_count[tile] = sm.tile_full;
@@ -1586,6 +1577,72 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       c.W.seg_rel[s] = (x >= TILE) ? sm.tile_full : ids_before(sm, (int)x);
     }
     __syncthreads();
+  }
+}
+
+// Adds the long pieces to the tile counts once their merges are done: per
+// tile with long pieces (one warp), each entry of the staging slot's table
+// gets its source in the arena, its id count and the ids before it in the
+// tile (full_excl = short ids before it + the long pieces before it); the
+// tile count and the offsets of the tile's segments grow by the long
+// pieces before them.
+constexpr int FIX_PER_LANE = (MAX_GP + 31) / 32;
+__global__ void __launch_bounds__(ETHREADS) k_long_fixup(Call c) {
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t tile = gw; tile < ntiles; tile += nw) {
+    const int ngp = (int)(c.W.tile_meta[tile] >> 24);
+    if (ngp == 0) continue;
+    const int64_t t0 = tile * TILE;
+    uint32_t* slot = c.W.staging + tile * STG;
+    // 1. source and count of each entry
+    for (int g = lane; g < ngp; g += 32) {
+      uint32_t* e = slot + STG - 4 * (g + 1);
+      const uint32_t src = c.W.gsrc[c.gb + t0 + e[1]] & ~GSRC_CACHED;
+      e[2] = src;
+      e[3] = c.W.cnt[src];
+    }
+    __syncwarp();
+    // 2. ids of the long pieces before each entry and before each segment
+    uint32_t fe[FIX_PER_LANE];
+    uint32_t total = 0;
+#pragma unroll
+    for (int k = 0; k < FIX_PER_LANE; k++) {
+      const int g = lane + 32 * k;
+      fe[k] = 0;
+      if (g < ngp) {
+        const uint32_t* e = slot + STG - 4 * (g + 1);
+        uint32_t before = 0;
+        for (int h = 0; h < ngp; h++) {
+          const uint32_t* f = slot + STG - 4 * (h + 1);
+          if (f[1] < e[1]) before += f[3];
+        }
+        fe[k] = e[0] + before;
+        total += e[3];
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    const int64_t sg0 = c.W.tile_segs[4 * tile + 1];
+    const int64_t sg1 = (tile == ntiles - 1) ? c.S + 1 : c.W.tile_segs[4 * tile + 2];
+    for (int64_t sg = sg0 + lane; sg < sg1; sg += 32) {
+      const int64_t x = c.seg_off[sg] - t0;
+      uint32_t add = 0;
+      for (int h = 0; h < ngp; h++) {
+        const uint32_t* f = slot + STG - 4 * (h + 1);
+        if ((int64_t)f[1] < x) add += f[3];
+      }
+      c.W.seg_rel[sg] += add;
+    }
+    __syncwarp();
+    // 3. full_excl replaces the position (every lane has read the positions)
+#pragma unroll
+    for (int k = 0; k < FIX_PER_LANE; k++) {
+      const int g = lane + 32 * k;
+      if (g < ngp) slot[STG - 4 * (g + 1) + 1] = fe[k];
+    }
+    if (lane == 0) c.W.tile_count[tile] += total;
   }
 }
 
@@ -2319,8 +2376,13 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
     tk_set_error("tk_workspace_create: cudaMallocHost failed");
     return TK_E_NOMEM;
   }
+  int prio_lo = 0, prio_hi = 0;
+  cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
   bool ok = cudaStreamCreateWithFlags(&ws->s_h2d, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&ws->s_d2h, cudaStreamNonBlocking) == cudaSuccess;
+            cudaStreamCreateWithFlags(&ws->s_d2h, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&ws->s_side, cudaStreamNonBlocking, prio_hi) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ws->ev_split, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ws->ev_long, cudaEventDisableTiming) == cudaSuccess;
   cudaEvent_t* evs[2 * tk_workspace::PIPE_MAX + 1];
   int ne = 0;
   evs[ne++] = &ws->ev_start;
@@ -2351,8 +2413,12 @@ extern "C" void tk_workspace_free(tk_workspace* ws) {
   // events in creation order: ev_start, then (ev_h2d[k], ev_done[k]) per batch
   for (int k = 0; k < ws->n_events; k++)
     cudaEventDestroy(k == 0 ? ws->ev_start : ((k - 1) % 2 == 0 ? ws->ev_h2d[(k - 1) / 2] : ws->ev_done[(k - 1) / 2]));
+  if (ws->s_side) cudaStreamSynchronize(ws->s_side);
+  if (ws->ev_split) cudaEventDestroy(ws->ev_split);
+  if (ws->ev_long) cudaEventDestroy(ws->ev_long);
   if (ws->s_h2d) cudaStreamDestroy(ws->s_h2d);
   if (ws->s_d2h) cudaStreamDestroy(ws->s_d2h);
+  if (ws->s_side) cudaStreamDestroy(ws->s_side);
   delete ws;
 }
 
@@ -2398,35 +2464,45 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     }
     tk_prof_mark(ws, "k_split", st);
     k_split<<<split_grid, SPLIT_THREADS, 0, st>>>(c);
-    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sizeof(EncSmem)), "smem attribute");
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_encode_tiles, ETHREADS, sizeof(EncSmem));
-    const int enc_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(per_sm, 1));
+    // The long pieces (listing, word cache, merges) run on a second stream
+    // next to the tile kernel, which needs their counts only in k_long_fixup.
+    // With per-kernel profiling on, everything stays on st.
+    cudaStream_t side = st;
+    if (!ws->prof.on) {
+      side = ws->s_side;
+      TK_CUDA(cudaEventRecord(ws->ev_split, st), "fork");
+      TK_CUDA(cudaStreamWaitEvent(side, ws->ev_split, 0), "fork");
+    }
     tk_prof_mark(ws, "k_find_long", st);
-    k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 16) + 255) / 256, (int64_t)sms * 16), 256, 0, st>>>(c);
+    k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 16) + 255) / 256, (int64_t)sms * 16), 256, 0, side>>>(c);
     tk_prof_mark(ws, "k_dedup_medium", st);
-    k_dedup_medium<<<sms * 8, ETHREADS, 0, st>>>(c);
+    k_dedup_medium<<<sms * 8, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_dedup_big", st);
-    k_dedup_big<<<sms, 1024, 0, st>>>(c);
+    k_dedup_big<<<sms, 1024, 0, side>>>(c);
     if (c.W.use_cache) {
       tk_prof_mark(ws, "k_cache_lookup", st);
-      k_cache_lookup<<<sms * 8, ETHREADS, 0, st>>>(c);
+      k_cache_lookup<<<sms * 8, ETHREADS, 0, side>>>(c);
       tk_prof_mark(ws, "k_cache_lookup_big", st);
-      k_cache_lookup_big<<<sms, 1024, 0, st>>>(c);
+      k_cache_lookup_big<<<sms, 1024, 0, side>>>(c);
     }
     tk_prof_mark(ws, "k_merge_big", st);
-    k_merge_big<<<sms, BIG_THREADS, 0, st>>>(c);
+    k_merge_big<<<sms, BIG_THREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_cluster", st);
-    k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), BIG_THREADS, 0, st>>>(c);
+    k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), BIG_THREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_medium", st);
-    k_merge_medium<<<sms * 4, ETHREADS, 0, st>>>(c);
+    k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
     if (c.W.use_cache) {
       tk_prof_mark(ws, "k_cache_insert", st);
-      k_cache_insert<<<sms * 8, ETHREADS, 0, st>>>(c);
+      k_cache_insert<<<sms * 8, ETHREADS, 0, side>>>(c);
     }
+    if (side != st) TK_CUDA(cudaEventRecord(ws->ev_long, side), "join");
+    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(EncSmem)), "smem attribute");
     tk_prof_mark(ws, "k_encode_tiles", st);
-    k_encode_tiles<<<enc_grid, ETHREADS, sizeof(EncSmem), st>>>(c);
+    k_encode_tiles<<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
+    if (side != st) TK_CUDA(cudaStreamWaitEvent(st, ws->ev_long, 0), "join");
+    tk_prof_mark(ws, "k_long_fixup", st);
+    k_long_fixup<<<(int)std::min<int64_t>((n_split_tiles * 32 + ETHREADS - 1) / ETHREADS, (int64_t)sms * 8), ETHREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_scan_u32", st);
     int rc = tk_scan_u32(ws, ws->w.tile_count, ws->w.tile_base, &ws->w.status->n_tiles, n_split_tiles, 3, st);
     if (rc) return rc;

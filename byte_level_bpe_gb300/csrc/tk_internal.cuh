@@ -357,6 +357,8 @@ struct tk_workspace {
   // whose copies in and out overlap the encode of their neighbours
   static constexpr int PIPE_MAX = 16;
   cudaStream_t s_h2d, s_d2h;
+  cudaStream_t s_side;               // the long-piece kernels, next to the tile kernel
+  cudaEvent_t ev_split, ev_long;     // fork after the split, join before the fixup
   cudaEvent_t ev_start, ev_h2d[PIPE_MAX], ev_done[PIPE_MAX];
   int n_events;
   tk::Status* h_pipe_status;  // [PIPE_MAX] pinned
