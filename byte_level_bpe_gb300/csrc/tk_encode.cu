@@ -434,8 +434,33 @@ __device__ int win_special(const Call& c, const SplitSmem& sm, int x, int64_t po
 // check_q: whether q itself must be tested for a piece start.
 __device__ bool g_ws_rest_ends_in_piece(const Call& c, int64_t q, bool check_q) {
   const int64_t seg_end = c.seg_off[seg_of(c, q) + 1];
+  const int64_t lim = min(c.n, seg_end);
+  // 16 bytes at a time through runs of ASCII space / tab / VT / FF: none can be
+  // a CR/LF or end the run; only a chunk cut or a special can end the piece
+  // there (specials are ruled out when none starts with those bytes)
+  const bool ws_specials = c.T.n_spec && (((c.T.spec_first[0x20 >> 5] >> (0x20 & 31)) |
+                                            (c.T.spec_first[0] >> 0x09) | (c.T.spec_first[0] >> 0x0B) |
+                                            (c.T.spec_first[0] >> 0x0C)) & 1u);
+  const bool vec = !ws_specials && (((uintptr_t)c.text & 15) == 0);
   for (bool first = true;; first = false) {
-    if (q >= c.n || q >= seg_end) return false;
+    if (q >= lim) return false;
+    if (vec && !first && (q & 15) == 0 && q + 16 <= lim) {
+      const uint4 v = *reinterpret_cast<const uint4*>(c.text + q);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      bool all_ws = true;
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const uint32_t e = __vcmpeq4(wv[k], 0x20202020u) | __vcmpeq4(wv[k], 0x09090909u) |
+                           __vcmpeq4(wv[k], 0x0B0B0B0Bu) | __vcmpeq4(wv[k], 0x0C0C0C0Cu);
+        all_ws &= e == 0xFFFFFFFFu;
+      }
+      uint32_t cuts = 0;
+      if (c.safe) cuts = ((c.W.win_cut[q >> 5] | c.W.run_cut[q >> 5]) >> (q & 31)) & 0xFFFFu;
+      if (all_ws && cuts == 0) {
+        q += 16;
+        continue;
+      }
+    }
     if (!first || check_q) {
       if (g_chunk_cut(c, q)) return false;
       if (c.T.n_spec && g_special_at(c, q, nullptr)) return false;
