@@ -2227,22 +2227,29 @@ __device__ int merge_warp(const Call& c, int64_t s, int n, uint32_t* dst) {
 // (in registers up to SMALL_WARP_MAX bytes, else the round merge).
 // ids -> arena[start ..], count -> cnt[start].
 constexpr int BIG_THREADS = 1024;
+constexpr int64_t BIG_FIRST = 8192;
 __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
   __shared__ int64_t red64[BIG_THREADS / 32];
   __shared__ uint32_t red32[BIG_THREADS / 32];
   __shared__ uint32_t s_idx;
   const int tid = threadIdx.x;
   const uint32_t n_big = c.W.status->n_biglong;
-  for (;;) {
-    if (tid == 0) s_idx = atomicAdd(&c.W.status->big_next, 1u);
-    __syncthreads();
-    const uint32_t k = s_idx;
-    __syncthreads();
-    if (k >= n_big) break;
-    const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
-    if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
-    const int64_t m = merge_rounds(c, RGroup<BIG_THREADS / 32>{red64, red32}, p, len);
-    if (tid == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
+  // two passes over the list, pieces over BIG_FIRST bytes first, so that no
+  // CTA starts a long piece late (longest-first scheduling, in two buckets)
+  for (int pass = 0; pass < 2; pass++) {
+    uint32_t* next = pass == 0 ? &c.W.status->big_next : &c.W.status->big_next2;
+    for (;;) {
+      if (tid == 0) s_idx = atomicAdd(next, 1u);
+      __syncthreads();
+      const uint32_t k = s_idx;
+      __syncthreads();
+      if (k >= n_big) break;
+      const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
+      if ((len > BIG_FIRST) != (pass == 0)) continue;
+      if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
+      const int64_t m = merge_rounds(c, RGroup<BIG_THREADS / 32>{red64, red32}, p, len);
+      if (tid == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
+    }
   }
 }
 
@@ -2491,41 +2498,39 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     k_split<<<split_grid, SPLIT_THREADS, 0, st>>>(c);
     // The long pieces (listing, word cache, merges) run on a second stream
     // next to the tile kernel, which needs their counts only in k_long_fixup.
-    // With per-kernel profiling on, everything stays on st.
-    cudaStream_t side = st;
-    if (!ws->prof.on) {
-      side = ws->s_side;
-      TK_CUDA(cudaEventRecord(ws->ev_split, st), "fork");
-      TK_CUDA(cudaStreamWaitEvent(side, ws->ev_split, 0), "fork");
-    }
-    tk_prof_mark(ws, "k_find_long", st);
+    cudaStream_t side = ws->s_side;
+    TK_CUDA(cudaEventRecord(ws->ev_split, st), "fork");
+    TK_CUDA(cudaStreamWaitEvent(side, ws->ev_split, 0), "fork");
+    tk_prof_mark(ws, "k_find_long", side);
     k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 16) + 255) / 256, (int64_t)sms * 16), 256, 0, side>>>(c);
-    tk_prof_mark(ws, "k_dedup_medium", st);
+    tk_prof_mark(ws, "k_dedup_medium", side);
     k_dedup_medium<<<sms * 8, ETHREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_dedup_big", st);
+    tk_prof_mark(ws, "k_dedup_big", side);
     k_dedup_big<<<sms, 1024, 0, side>>>(c);
     if (c.W.use_cache) {
-      tk_prof_mark(ws, "k_cache_lookup", st);
+      tk_prof_mark(ws, "k_cache_lookup", side);
       k_cache_lookup<<<sms * 8, ETHREADS, 0, side>>>(c);
-      tk_prof_mark(ws, "k_cache_lookup_big", st);
+      tk_prof_mark(ws, "k_cache_lookup_big", side);
       k_cache_lookup_big<<<sms, 1024, 0, side>>>(c);
     }
-    tk_prof_mark(ws, "k_merge_big", st);
+    tk_prof_mark(ws, "k_merge_big", side);
     k_merge_big<<<sms, BIG_THREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_merge_cluster", st);
+    tk_prof_mark(ws, "k_merge_cluster", side);
     k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), BIG_THREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_merge_medium", st);
+    tk_prof_mark(ws, "k_merge_medium", side);
     k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
     if (c.W.use_cache) {
-      tk_prof_mark(ws, "k_cache_insert", st);
+      tk_prof_mark(ws, "k_cache_insert", side);
       k_cache_insert<<<sms * 8, ETHREADS, 0, side>>>(c);
     }
-    if (side != st) TK_CUDA(cudaEventRecord(ws->ev_long, side), "join");
+    tk_prof_mark(ws, nullptr, side);
+    TK_CUDA(cudaEventRecord(ws->ev_long, side), "join");
     TK_CUDA(cudaFuncSetAttribute(k_encode_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(EncSmem)), "smem attribute");
     tk_prof_mark(ws, "k_encode_tiles", st);
     k_encode_tiles<<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
-    if (side != st) TK_CUDA(cudaStreamWaitEvent(st, ws->ev_long, 0), "join");
+    tk_prof_mark(ws, nullptr, st);
+    TK_CUDA(cudaStreamWaitEvent(st, ws->ev_long, 0), "join");
     tk_prof_mark(ws, "k_long_fixup", st);
     k_long_fixup<<<(int)std::min<int64_t>((n_split_tiles * 32 + ETHREADS - 1) / ETHREADS, (int64_t)sms * 8), ETHREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_scan_u32", st);
@@ -2541,6 +2546,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     tk_prof_mark(ws, "k_empty_offsets", st);
     k_empty_offsets<<<seg_grid, 256, 0, st>>>(c, d_out_offsets, id_base);
   }
+  tk_prof_mark(ws, nullptr, st);
   TK_CUDA(cudaGetLastError(), "encode launch");
   return TK_OK;
 }

@@ -52,6 +52,7 @@ struct Status {
   uint32_t n_biglong;
   uint32_t medium_next;
   uint32_t big_next;
+  uint32_t big_next2;
   uint32_t dedup_big_next;
   uint32_t n_huge;       // entries of huge_list
   uint32_t n_cl;         // entries of cl_list
@@ -319,14 +320,15 @@ struct tk_tokenizer {
 };
 
 struct tk_profile {
-  static constexpr int MAXK = 24;
+  static constexpr int MAXK = 40;
   int on;
-  int n;                      // kernels with totals
+  int n;                        // kernels with totals
   const char* names[MAXK];
   double total_ms[MAXK];
   int64_t launches[MAXK];
-  cudaEvent_t ev[MAXK + 1];   // events of the call in flight
-  const char* pending[MAXK];  // kernel names of the call in flight
+  cudaEvent_t ev[MAXK + 1];     // events of the call in flight, one per mark
+  const char* pending[MAXK];    // kernel starting at each mark (null: an end mark)
+  cudaStream_t pstream[MAXK];   // the stream of each mark
   int n_pending;
 };
 
@@ -372,6 +374,9 @@ struct tk_workspace {
 void tk_set_error(const char* fmt, ...);
 // Profiling helpers: mark() before a launch (records an event when profiling
 // is on); finish() after the call's synchronisation adds up the durations.
+// Marks the start of `kernel` on stream st (kernel null: the end of the previous
+// kernel on st).  A kernel's time runs from its mark to the next mark on the
+// same stream, so kernels on several streams keep running concurrently.
 void tk_prof_mark(tk_workspace* ws, const char* kernel, cudaStream_t st);
 void tk_prof_finish(tk_workspace* ws, cudaStream_t st);
 int tk_scan_u32(tk_workspace* ws, const uint32_t* d_in, uint32_t* d_out, const int64_t* d_n,

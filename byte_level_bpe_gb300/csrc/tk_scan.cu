@@ -99,17 +99,22 @@ void tk_prof_mark(tk_workspace* ws, const char* kernel, cudaStream_t st) {
   tk_profile& p = ws->prof;
   if (!p.on || p.n_pending >= tk_profile::MAXK) return;
   cudaEventRecord(p.ev[p.n_pending], st);
+  p.pstream[p.n_pending] = st;
   p.pending[p.n_pending++] = kernel;
 }
 
 void tk_prof_finish(tk_workspace* ws, cudaStream_t st) {
   tk_profile& p = ws->prof;
   if (!p.on || p.n_pending == 0) return;
-  cudaEventRecord(p.ev[p.n_pending], st);
-  cudaEventSynchronize(p.ev[p.n_pending]);
+  (void)st;
+  for (int i = 0; i < p.n_pending; i++) cudaEventSynchronize(p.ev[i]);
   for (int i = 0; i < p.n_pending; i++) {
+    if (!p.pending[i]) continue;  // an end mark
+    int j = i + 1;
+    while (j < p.n_pending && p.pstream[j] != p.pstream[i]) j++;
+    if (j == p.n_pending) continue;  // no end mark on that stream
     float ms = 0.f;
-    cudaEventElapsedTime(&ms, p.ev[i], p.ev[i + 1]);
+    cudaEventElapsedTime(&ms, p.ev[i], p.ev[j]);
     int k = 0;
     while (k < p.n && strcmp(p.names[k], p.pending[i]) != 0) k++;
     if (k == p.n) {

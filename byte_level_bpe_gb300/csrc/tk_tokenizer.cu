@@ -338,6 +338,7 @@ static int decode_enqueue(const tk_tokenizer* tok, tk_workspace* ws, const int32
   }
   tk_prof_mark(ws, "k_dec_total", st);
   k_dec_total<<<1, 1, 0, st>>>(ws->w, n);
+  tk_prof_mark(ws, nullptr, st);
   return TK_OK;
 }
 
@@ -510,6 +511,7 @@ extern "C" int tk_decode_segments(const tk_tokenizer* tok, tk_workspace* ws, con
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((S + 256) / 256, (int64_t)ws->num_sms * 4));
   tk_prof_mark(ws, "k_dec_seg_offsets", st);
   k_dec_seg_offsets<<<grid, 256, 0, st>>>(ws->w, d_id_off, S, n, d_byte_off);
+  tk_prof_mark(ws, nullptr, st);
   rc = decode_finish(ws, cap, 0, st, "tk_decode_segments");
   if (h_len) *h_len = ws->h_status->n_ids;
   if (rc == TK_E_ARG) tk_set_error("tk_decode_segments: id offsets must run 0 <= ... <= n");
