@@ -704,8 +704,18 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
         for (int j = 0; j < L; j++) atomicOr(&sm.insp[(x + j) >> 5], 1u << ((x + j) & 31));
       }
     }
-    // 4. classes (and UTF-8 validation of the tile's own bytes)
-    for (int x = tid; x < WIN; x += SPLIT_THREADS) {
+    // 4. classes (and UTF-8 validation of the tile's own bytes): four bytes at
+    //    a time where all four are ASCII text, else one by one
+    for (int x4 = tid; 4 * x4 < WIN; x4 += SPLIT_THREADS) {
+      const int64_t pos4 = wlo + 4 * x4;
+      const uint32_t tw = reinterpret_cast<const uint32_t*>(sm.text)[x4];
+      if (pos4 >= 0 && pos4 + 4 <= c.n && (tw & 0x80808080u) == 0) {
+        reinterpret_cast<uint32_t*>(sm.kc)[x4] =
+            (uint32_t)s_asc[tw & 0x7F] | ((uint32_t)s_asc[(tw >> 8) & 0x7F] << 8) |
+            ((uint32_t)s_asc[(tw >> 16) & 0x7F] << 16) | ((uint32_t)s_asc[tw >> 24] << 24);
+        continue;
+      }
+      for (int x = 4 * x4; x < 4 * x4 + 4; x++) {
       const int64_t pos = wlo + x;
       const uint32_t b = sm.text[x];
       uint8_t k;
@@ -738,19 +748,46 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
         k = kclass(cp);
       }
       sm.kc[x] = k;
+      }
     }
     __syncthreads();
     // 5. number-run aggregate of this thread's 16 bytes
     const int xb = HALO + tid * 16;
     uint32_t nreset = 0, ncount = 0;
-    for (int j = 0; j < 16; j++) {
-      const int x = xb + j;
-      const uint8_t k = sm.kc[x] & 7;
-      if (k == K_CONT) continue;
-      if (k == K_OUT) break;
-      if (k != K_N || bit_get(sm.insp, x)) { nreset = 1; ncount = 0; continue; }
-      if (bit_get(sm.pst, x)) { nreset = 1; ncount = 0; }
-      ncount = (ncount + 1) % 3;
+    {
+      // bit-parallel when the 16 bytes hold no continuation byte and no text
+      // end: D = numbers, reset at every non-number (or number inside a
+      // special), restart at every number that starts a piece
+      const uint32_t* kw = reinterpret_cast<const uint32_t*>(&sm.kc[xb]);
+      uint32_t D = 0, CO = 0;
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const uint32_t wv = kw[j];
+        const uint32_t p0 = gather_plane(wv, 0), p1 = gather_plane(wv, 1), p2 = gather_plane(wv, 2);
+        D |= (p0 & ~p1 & ~p2 & 0xFu) << (4 * j);
+        CO |= (p1 & p2 & 0xFu) << (4 * j);
+      }
+      if (CO == 0) {
+        const uint32_t I = (sm.insp[xb >> 5] >> (xb & 31)) & 0xFFFFu;
+        const uint32_t Pm = (sm.pst[xb >> 5] >> (xb & 31)) & 0xFFFFu;
+        const uint32_t non_run = (~D | (D & I)) & 0xFFFFu;
+        const uint32_t restart = D & ~I & Pm;
+        nreset = (non_run | restart) != 0;
+        const int a = non_run ? 31 - __clz(non_run) : -1;
+        const int b = restart ? 31 - __clz(restart) : -1;
+        const int start = max(a + 1, max(b, 0));
+        ncount = (uint32_t)__popc(D & ~I & (0xFFFFu << start) & 0xFFFFu) % 3u;
+      } else {
+        for (int j = 0; j < 16; j++) {
+          const int x = xb + j;
+          const uint8_t k = sm.kc[x] & 7;
+          if (k == K_CONT) continue;
+          if (k == K_OUT) break;
+          if (k != K_N || bit_get(sm.insp, x)) { nreset = 1; ncount = 0; continue; }
+          if (bit_get(sm.pst, x)) { nreset = 1; ncount = 0; }
+          ncount = (ncount + 1) % 3;
+        }
+      }
     }
     {
       // exclusive block scan of the number-run aggregates (warp shuffles)
