@@ -252,6 +252,7 @@ __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int s
     s.n_tiles = n_tiles;
     *W.status = s;
   }
+  for (int64_t i = tid; i < n_tiles; i += stride) W.tile_first[i] = 0xFFFFFFFFu;  // no start yet
   for (int64_t i = tid; i < n_desc_split; i += stride) {
     W.desc_a[i] = 0;
     W.desc_b[i] = 0;
@@ -645,7 +646,6 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
   __shared__ uint8_t s_asc[128];
   __shared__ int s_any_allow;
   const int tid = threadIdx.x;
-  if (tid == 0) sm.first = 0xFFFFFFFFu;
   if (tid < 128) s_asc[tid] = kclass((uint32_t)tid);
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const bool aligned = ((uintptr_t)c.text & 15) == 0;
@@ -895,19 +895,17 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
     }
     __syncthreads();
     // 7. start bitmaps of the tile and the position of its first start
-    for (int i = tid; i < TILE / 32; i += SPLIT_THREADS) {
-      const int64_t word = (t0 >> 5) + i;
-      const uint32_t w = sm.outb[i];
+    //    (tile_first starts at NO_START, set by k_reset).  No barrier after:
+    //    the next tile writes shared memory only after the loop's first one.
+    static_assert(TILE / 32 <= SPLIT_THREADS && (TILE / 32) % 32 == 0, "one bitmap word per thread");
+    if (tid < TILE / 32) {
+      const int64_t word = (t0 >> 5) + tid;
+      const uint32_t w = sm.outb[tid];
       c.W.pbits[word] = w;
-      if (c.T.n_spec) c.W.sbits[word] = w & sm.sst[(HALO >> 5) + i];
-      if (w) atomicMin(&sm.first, (uint32_t)(32 * i + __ffs(w) - 1));
+      if (c.T.n_spec) c.W.sbits[word] = w & sm.sst[(HALO >> 5) + tid];
+      const uint32_t f = __reduce_min_sync(0xffffffffu, w ? (uint32_t)(32 * tid + __ffs(w) - 1) : 0xFFFFFFFFu);
+      if ((tid & 31) == 0 && f != 0xFFFFFFFFu) atomicMin(&c.W.tile_first[tile], f);
     }
-    __syncthreads();
-    if (tid == 0) {
-      c.W.tile_first[tile] = sm.first;
-      sm.first = 0xFFFFFFFFu;
-    }
-    __syncthreads();
   }
 }
 
