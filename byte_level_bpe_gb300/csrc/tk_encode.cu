@@ -401,7 +401,6 @@ struct SplitSmem {
   int64_t tile;
   int64_t seg[2];
   uint64_t ncarry;
-  uint32_t first;  // first pre-token start of the tile (tile-relative), or all ones
 };
 static_assert(offsetof(SplitSmem, kc) % 4 == 0, "class bytes are read as words");
 
@@ -1024,8 +1023,12 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
   }
   if (n <= 4) return merge_reg<4>(T, b, n, out);
   if (n <= 8) return merge_reg<8>(T, b, n, out);
-  if (n <= 12) return merge_reg<12>(T, b, n, out);
-  return merge_reg<16>(T, b, n, out);
+  if constexpr (SHORT_MAX <= 12) {
+    return merge_reg<12>(T, b, n, out);
+  } else {
+    if (n <= 12) return merge_reg<12>(T, b, n, out);
+    return merge_reg<16>(T, b, n, out);
+  }
 }
 
 // Length class of a pre-token for the tile's work list (warps then run
@@ -1370,10 +1373,11 @@ constexpr uint32_t NO_START = 0xFFFFFFFFu;
 constexpr int64_t STG = TILE + SHORT_MAX + 8;       // staging slot per tile (u32 entries)
 constexpr uint32_t DTAB_LOG2 = 20;                  // dedup table of long pieces: 2^20 slots
 
+// A pre-token over SHORT_MAX bytes starting in the tile: merged by the
+// long-piece kernels; its count and source are added by k_long_fixup.
 struct GPiece {
-  uint32_t rel;  // start in the tile
-  uint32_t src;  // start of the piece whose ids it uses (in the arena)
-  uint32_t cnt, short_excl, full_excl;
+  uint32_t rel;         // start in the tile
+  uint32_t short_excl;  // short ids of the tile before it
 };
 
 struct EncSmem {
@@ -1390,16 +1394,14 @@ struct EncSmem {
     __align__(16) int32_t outs[TILE + SHORT_MAX + 4];  // then the tile's short ids in order
   };
   GPiece gp[MAX_GP];
-  uint32_t th_full[ETHREADS];
+  uint32_t th_full[ETHREADS];           // short ids before each thread's 16 bytes
   uint32_t warp_tot[2 * ETHREADS / 32];
   int64_t red64[ETHREADS / 32];
   uint32_t red32[ETHREADS / 32];
   int n_gp;
   uint32_t mnext;  // merge work-list cursor
   uint32_t n_starts;
-  int64_t tile;
-  uint64_t base;
-  uint32_t tile_full, tile_short;
+  uint32_t tile_short;
   int64_t seg[2];
 };
 
@@ -1414,18 +1416,14 @@ __device__ int32_t special_id_smem(const Tables& T, const uint8_t* b, int len) {
   return -1;
 }
 
-// Ids before byte x of the tile (x in [0, TILE)), counted from the tile start.
+// Short ids before byte x of the tile (x in [0, TILE)), counted from the tile
+// start (k_long_fixup adds the long pieces before x).
 __device__ uint32_t ids_before(const EncSmem& sm, int x) {
   const int t = x >> 4;
   uint32_t r = sm.th_full[t];
   for (int y = t << 4; y < x; y++) {
     if (!((sm.pb[y >> 5] >> (y & 31)) & 1u)) continue;  // not a pre-token start
-    if ((sm.gb[y >> 5] >> (y & 31)) & 1u) {
-      for (int g = 0; g < sm.n_gp; g++)
-        if ((int)sm.gp[g].rel == y) r += sm.gp[g].cnt;
-    } else {
-      r += sm.cnt[y];
-    }
+    if (!((sm.gb[y >> 5] >> (y & 31)) & 1u)) r += sm.cnt[y];
   }
   return r;
 }
@@ -1506,7 +1504,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
         // merged by the long-piece kernels, which may still be running: the
         // tile records where the piece is; k_long_fixup adds its ids' count
         const int g = atomicAdd(&sm.n_gp, 1);
-        sm.gp[g] = GPiece{(uint32_t)x, 0u, 0u, 0u, 0u};
+        sm.gp[g] = GPiece{(uint32_t)x, 0u};
         atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
         sm.cnt[x] = 0;
       }
@@ -1563,55 +1561,46 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       atomicAdd((unsigned long long*)&c.W.status->n_ptok, (unsigned long long)sm.n_starts);
       if (ngp) atomicAdd(&c.W.status->n_long, (uint32_t)ngp);
     }
-    // 4. per-thread totals -> block scan -> tile total -> look-back
-    // (the counts below leave out the long pieces; k_long_fixup adds them)
-    uint32_t my_full = my_short, th_short = 0;
+    // 4. per-thread short-id counts -> block scan -> the tile's short ids
+    //    (k_long_fixup adds the long pieces to the counts)
+    uint32_t th_short = 0;
     {
-      uint32_t a = my_full, b = my_short;
+      uint32_t a = my_short;
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t ya = __shfl_up_sync(0xffffffffu, a, o);
-        const uint32_t yb = __shfl_up_sync(0xffffffffu, b, o);
-        if (lane >= o) { a += ya; b += yb; }
+        if (lane >= o) a += ya;
       }
-      if (lane == 31) { sm.warp_tot[warp] = a; sm.warp_tot[ETHREADS / 32 + warp] = b; }
+      if (lane == 31) sm.warp_tot[warp] = a;
       __syncthreads();
       if (tid == 0) {
-        uint32_t ra = 0, rb = 0;
+        uint32_t ra = 0;
         for (int w = 0; w < ETHREADS / 32; w++) {
-          const uint32_t ta = sm.warp_tot[w], tb = sm.warp_tot[ETHREADS / 32 + w];
+          const uint32_t ta = sm.warp_tot[w];
           sm.warp_tot[w] = ra;
-          sm.warp_tot[ETHREADS / 32 + w] = rb;
           ra += ta;
-          rb += tb;
         }
-        sm.tile_full = ra;
-        sm.tile_short = rb;
+        sm.tile_short = ra;
       }
       __syncthreads();
-      sm.th_full[tid] = sm.warp_tot[warp] + a - my_full;
-      th_short = sm.warp_tot[ETHREADS / 32 + warp] + b - my_short;
+      th_short = sm.warp_tot[warp] + a - my_short;
+      sm.th_full[tid] = th_short;
     }
     __syncthreads();
     // 5. compaction of short ids (in order, in shared memory); offsets of
     //    the global pieces
     uint32_t* slot = c.W.staging + tile * STG;
     {
-      uint32_t f = sm.th_full[tid], s = th_short;
+      uint32_t s = th_short;
       for (uint32_t bits = my; bits; bits &= bits - 1) {
         const int x = xb + __ffs(bits) - 1;
         if ((sm.gb[x >> 5] >> (x & 31)) & 1u) {
           for (int g = 0; g < ngp; g++)
-            if ((int)sm.gp[g].rel == x) {
-              sm.gp[g].short_excl = s;
-              sm.gp[g].full_excl = f;
-              f += sm.gp[g].cnt;
-            }
+            if ((int)sm.gp[g].rel == x) sm.gp[g].short_excl = s;
           continue;
         }
         const uint32_t m = sm.cnt[x];
         for (uint32_t j = 0; j < m; j++) sm.outs[s + j] = sm.stage[x + j];
         s += m;
-        f += m;
       }
     }
     __syncthreads();
@@ -1629,12 +1618,12 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       e[3] = 0;
     }
     if (tid == 0) {
-      c.W.tile_count[tile] = sm.tile_full;
+      c.W.tile_count[tile] = sm.tile_short;
       c.W.tile_meta[tile] = sm.tile_short | ((uint32_t)ngp << 24);
     }
     for (int64_t s = sm.seg[0] + tid; s < sm.seg[1]; s += ETHREADS) {
       const int64_t x = c.seg_off[s] - t0;
-      c.W.seg_rel[s] = (x >= TILE) ? sm.tile_full : ids_before(sm, (int)x);
+      c.W.seg_rel[s] = (x >= TILE) ? sm.tile_short : ids_before(sm, (int)x);
     }
     __syncthreads();
   }
@@ -1879,7 +1868,7 @@ __global__ void k_find_long(Call c) {
     if ((wi << 5) + 32 > c.n) bits &= (1u << (c.n - (wi << 5))) - 1u;
     if (!bits) continue;
     const int last = 31 - __clz(bits);
-    // starts followed by another start within SHORT_MAX (= 16) bytes, from
+    // starts followed by another start within SHORT_MAX bytes, from
     // this word and the next (the text end counts as a start)
     uint64_t w = bits;
     if ((wi << 5) + 32 < c.n) {
@@ -1889,12 +1878,16 @@ __global__ void k_find_long(Call c) {
     } else {
       w |= ~0ull << (c.n - (wi << 5));
     }
-    static_assert(SHORT_MAX == 16, "the shift ladder below covers 16 positions");
-    uint64_t near = w >> 1;  // near = OR of w >> d for d = 1 .. 16
-    near |= near >> 1;
-    near |= near >> 2;
-    near |= near >> 4;
-    near |= near >> 8;
+    static_assert(SHORT_MAX >= 2 && SHORT_MAX <= 31, "the shift ladder covers 1 .. SHORT_MAX");
+    uint64_t near = w >> 1;  // near = OR of w >> d for d = 1 .. SHORT_MAX
+    int span = 1;            // near covers d = 1 .. span
+#pragma unroll
+    for (int k = 0; k < 5; k++)
+      if (2 * span <= SHORT_MAX) {
+        near |= near >> span;
+        span *= 2;
+      }
+    if (span < SHORT_MAX) near |= near >> (SHORT_MAX - span);
     for (uint32_t bb = bits & ~(1u << last) & ~(uint32_t)near; bb; bb &= bb - 1) {
       const int x = __ffs(bb) - 1;
       const uint32_t later = bits & ~((2u << x) - 1u);
