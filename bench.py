@@ -53,6 +53,23 @@ def make_workload(name, rank=0, total_mb=256):
         desc = ("agentic prompt: ~4 M characters in 2,000 typed segments (alternating "
                 "allow_special), prose/JSON/code/white-space runs up to 60k; tiktoken_safe=1")
         safe = True
+    elif name == "prose":
+        text = np.frombuffer(workloads.prose_text(table, 1 << 20, seed=2 + 1000 * rank), np.uint8)
+        off = np.array([0, text.size], np.int64)
+        allow = np.zeros(1, np.uint8)
+        desc = ("full-size table, 1 MiB of mixed text (Zipf over the table's letter tokens with "
+                "punctuation, digits and newlines), one segment, tiktoken_safe=0")
+        safe = False
+    elif name == "multilingual":
+        ext = workloads.multilingual_table(table)
+        table = [(t, i) for i, t in enumerate(table)] + ext
+        text = workloads.multilingual_text(workloads.full_table(), seed=4 + 1000 * rank)
+        text = np.frombuffer(text.tobytes() if isinstance(text, np.ndarray) else bytes(text), np.uint8)
+        off = np.array([0, text.size], np.int64)
+        allow = np.zeros(1, np.uint8)
+        desc = ("multilingual UTF-8 stress: table + 20,000 merges over UTF-8 byte sequences, 8 MiB "
+                "(ASCII 35%, CJK 30%, Devanagari 20%, emoji 10%, control bytes 5%), one segment")
+        safe = False
     else:
         raise SystemExit(f"unknown workload {name}")
     return table, np.ascontiguousarray(text), off, np.ascontiguousarray(allow), safe, desc
@@ -282,7 +299,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="serving", choices=["serving", "agentic"])
+    ap.add_argument("--workload", default="serving", choices=["serving", "agentic", "prose", "multilingual"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--total-mb", type=int, default=256,
                     help="serving batch size in MiB (256 = the benchmark workload; smaller for profiling)")

@@ -2184,10 +2184,18 @@ __global__ void k_cache_insert(Call c) {
 // (rank << 6 | position), merges it, shifts the later elements down one
 // place, and looks up the two new neighbour pairs in two lanes at once.
 // ids -> dst[0 ..]; returns the count.
-constexpr int SMALL_WARP_MAX = 64;
+constexpr int SMALL_WARP_MAX = 128;
+// the value of slot s (uniform across the warp) of a per-lane array
+template <int K>
+__device__ __forceinline__ uint32_t slot_of(const uint32_t (&v)[K], int s) {
+  uint32_t r = v[0];
+#pragma unroll
+  for (int k = 1; k < K; k++) r = s == k ? v[k] : r;
+  return r;
+}
 template <int K>
 __device__ int merge_warp(const Call& c, int64_t s, int n, uint32_t* dst) {
-  static_assert(K == 1 || K == 2, "one or two elements per lane");
+  static_assert(K >= 1 && K <= 4, "one to four elements per lane (positions in seven bits)");
   const int lane = threadIdx.x & 31;
   constexpr uint32_t NOKEY = 0xFFFFFFFFu;
   uint32_t id[K], rk[K];
@@ -2204,12 +2212,12 @@ __device__ int merge_warp(const Call& c, int64_t s, int n, uint32_t* dst) {
 #pragma unroll
     for (int k = 0; k < K; k++) {
       const int i = 32 * k + lane;
-      if (i + 1 < m && rk[k] != RANK_MAX) key = min(key, (rk[k] << 6) | (uint32_t)i);
+      if (i + 1 < m && rk[k] != RANK_MAX) key = min(key, (rk[k] << 7) | (uint32_t)i);
     }
     for (int o = 16; o > 0; o >>= 1) key = min(key, __shfl_xor_sync(0xffffffffu, key, o));
     if (key == NOKEY) break;
-    const uint32_t rs = key >> 6;
-    const int j = (int)(key & 63);
+    const uint32_t rs = key >> 7;
+    const int j = (int)(key & 127);
     // element j becomes rs; elements after j move down one place
 #pragma unroll
     for (int k = 0; k < K; k++) {
@@ -2228,8 +2236,8 @@ __device__ int merge_warp(const Call& c, int64_t s, int n, uint32_t* dst) {
     m--;
     // neighbours of the new element: j - 1 and j + 1 (after the shift)
     const int jl = j - 1, jr = j + 1;
-    const uint32_t idl = jl >= 0 ? __shfl_sync(0xffffffffu, (K == 2 && jl >= 32) ? id[K - 1] : id[0], jl & 31) : 0u;
-    const uint32_t idr = jr < m ? __shfl_sync(0xffffffffu, (K == 2 && jr >= 32) ? id[K - 1] : id[0], jr & 31) : 0u;
+    const uint32_t idl = jl >= 0 ? __shfl_sync(0xffffffffu, slot_of<K>(id, jl >> 5), jl & 31) : 0u;
+    const uint32_t idr = jr < m ? __shfl_sync(0xffffffffu, slot_of<K>(id, jr >> 5), jr & 31) : 0u;
     const bool do_l = jl >= 0 && lane == (jl & 31);
     const bool do_r = lane == (j & 31);
     // one call site, so the two lanes' lookups run together (ranks < 2^20)
@@ -2252,7 +2260,8 @@ __device__ int merge_warp(const Call& c, int64_t s, int n, uint32_t* dst) {
 // Merges the listed pieces that are the first of their kind (see the word
 // cache above).  k_merge_big: one 1024-thread CTA per piece over MEDIUM_MAX
 // bytes; k_merge_medium: one warp per piece of SHORT_MAX+1..MEDIUM_MAX bytes
-// (in registers up to SMALL_WARP_MAX bytes, else the round merge).
+// (in registers up to SMALL_WARP_MAX bytes, else and for runs of one byte the
+// round merge).
 // ids -> arena[start ..], count -> cnt[start].
 constexpr int BIG_THREADS = 1024;
 constexpr int64_t BIG_FIRST = 8192;
@@ -2315,9 +2324,17 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
     if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
     int64_t m;
     uint32_t* dst = reinterpret_cast<uint32_t*>(c.W.arena + c.gb + p);
-    if (len <= 32) m = merge_warp<1>(c, p, (int)len, dst);
-    else if (len <= SMALL_WARP_MAX) m = merge_warp<2>(c, p, (int)len, dst);
-    else m = merge_rounds(c, RGroup<1>{nullptr, nullptr}, p, len);
+    // a run of one repeated byte (white space, "----") merges in a few
+    // rounds; other pieces of up to SMALL_WARP_MAX bytes one merge at a time
+    bool run = true;
+    const uint32_t b0 = gbyte(c, p);
+    for (int64_t q = lane; q < len; q += 32) run &= gbyte(c, p + q) == b0;
+    run = __all_sync(0xffffffffu, run);
+    if (run || len > SMALL_WARP_MAX) m = merge_rounds(c, RGroup<1>{nullptr, nullptr}, p, len);
+    else if (len <= 32) m = merge_warp<1>(c, p, (int)len, dst);
+    else if (len <= 64) m = merge_warp<2>(c, p, (int)len, dst);
+    else if (len <= 96) m = merge_warp<3>(c, p, (int)len, dst);
+    else m = merge_warp<4>(c, p, (int)len, dst);
     if (lane == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
   }
 }

@@ -326,6 +326,8 @@ def test_mid_length_pieces(full_gpu, full_enc):
         for alpha in ["ab", "etaoinshr", "abcdefghijklmnopqrstuvwxyz"]:
             w = "".join(rng.choice(list(alpha), n))
             parts += [" " + w[1:], w, " " + w[1:]]
+    for n in [17, 40, 64, 65, 96, 97, 128, 129, 300]:
+        parts += ["-" * n, "=" * n, "a" * n, "x" + " " * n + "y"]
     rng.shuffle(parts)
     text = " ".join(parts).encode()
     segs = [(text[i:i + 5000], False) for i in range(0, len(text), 5000)]
