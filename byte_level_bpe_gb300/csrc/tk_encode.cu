@@ -389,6 +389,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) 
 // --------------------------------------------------------------------------
 // Split kernel: per 4 KiB tile, pre-token starts -> ordered records.
 
+constexpr int WSEG_MAX = 64;
 struct SplitSmem {
   uint8_t text[WIN + 16];
   uint8_t kc[WIN];
@@ -396,6 +397,12 @@ struct SplitSmem {
   uint32_t insp[WIN / 32];  // bytes inside special spans
   uint32_t sst[WIN / 32];   // special span starts
   uint32_t outb[TILE / 32]; // pre-token starts of the tile
+  // the segments that meet the window (at most WSEG_MAX): their starts
+  // relative to the window (-1: before it), one more entry for the end of the
+  // last, and their allow_special flags; nwseg = -1 when there are more
+  int32_t wseg[WSEG_MAX + 1];
+  uint8_t wallow[WSEG_MAX];
+  int nwseg;
   uint32_t scan[SPLIT_THREADS];
   uint32_t nagg[SPLIT_THREADS];
   int64_t tile;
@@ -409,9 +416,18 @@ static_assert(offsetof(SplitSmem, kc) % 4 == 0, "class bytes are read as words")
 __device__ int win_special(const Call& c, const SplitSmem& sm, int x, int64_t pos) {
   const uint32_t b = sm.text[x];
   if (!((c.T.spec_first[b >> 5] >> (b & 31)) & 1u)) return 0;
-  const int64_t s = seg_of(c, pos);
-  if (!c.allow[s]) return 0;
-  const int64_t send = c.seg_off[s + 1];
+  int64_t send;
+  if (sm.nwseg > 0) {
+    // the window's own segment table (shared memory)
+    int e = sm.nwseg - 1;
+    while (e > 0 && sm.wseg[e] > x) e--;
+    if (!sm.wallow[e]) return 0;
+    send = pos - x + sm.wseg[e + 1];
+  } else {
+    const int64_t s = seg_of(c, pos);
+    if (!c.allow[s]) return 0;
+    send = c.seg_off[s + 1];
+  }
   int best = 0;
   for (int k = 0; k < c.T.n_spec; k++) {
     const int L = c.T.spec_off[k + 1] - c.T.spec_off[k];
@@ -686,6 +702,20 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       if (s < c.S && c.allow[s]) s_any_allow = 1;
     }
     if (tid == 0 && seg_lo > 0 && c.allow[seg_lo - 1]) s_any_allow = 1;
+    {
+      // segments from the one holding the window's first byte to the last that starts in it
+      const int64_t sb = seg_lo > 0 ? seg_lo - 1 : 0;
+      const int64_t ne = seg_hi - sb;
+      const bool fits = ne >= 1 && ne <= WSEG_MAX;
+      if (tid == 0) sm.nwseg = fits ? (int)ne : -1;
+      if (fits)
+        for (int64_t e = tid; e <= ne; e += SPLIT_THREADS) {
+          const int64_t s = sb + e;
+          const int64_t rel = c.seg_off[s < c.S ? s : c.S] - wlo;
+          sm.wseg[e] = (int32_t)(rel < -1 ? -1 : rel);
+          if (e < ne) sm.wallow[e] = (s < c.S) ? c.allow[s] : 0;
+        }
+    }
     __syncthreads();
     // 3. specials in allow_special segments: find, then mark
     if (c.T.n_spec > 0 && s_any_allow) {
