@@ -1005,26 +1005,73 @@ __device__ __forceinline__ int merge_reg(const MergeTabs T, const uint8_t* b, in
 }
 
 // Three bytes: the parts loop written out.  First round: ranks r01, r12 of the
-// two byte pairs; the leftmost minimum merges; then the one remaining pair.
+// two byte pairs; the leftmost minimum merges; then the one remaining pair,
+// whose bytes are the whole piece: its rank is the slice table's entry for
+// the three bytes, loaded beside the pair ranks (one round trip in all).
 struct Ids3 {
   uint32_t n, a, b, c;
 };
 __device__ __forceinline__ Ids3 merge3(const MergeTabs T, const uint8_t* b) {
   const uint32_t b0 = b[0], b1 = b[1], b2 = b[2];
+  const uint32_t k = b0 | b1 << 8 | b2 << 16;
+  const uint64_t s = s34_first(T, k);
   const uint32_t r01 = dense_rank(T, b0, b1), r12 = dense_rank(T, b1, b2);
   const uint32_t i0 = __ldg(&T.byte_id[b0]), i1 = __ldg(&T.byte_id[b1]), i2 = __ldg(&T.byte_id[b2]);
+  const uint32_t r = s34_rank(T, s, k, false);
   if (r01 == RANK_MAX && r12 == RANK_MAX) return Ids3{3u, i0, i1, i2};
   const bool left = r01 <= r12;
-  const uint32_t a = left ? r01 : i0, c = left ? i2 : r12;
-  const uint32_t r = pair_rank(T, a, c);
   if (r != RANK_MAX) return Ids3{1u, r, 0u, 0u};
-  return Ids3{2u, a, c, 0u};
+  return Ids3{2u, left ? r01 : i0, left ? i2 : r12, 0u};
 }
 
 __device__ __forceinline__ void put3(int32_t* out, const Ids3& m) {
   out[0] = (int32_t)m.a;
   if (m.n > 1) out[1] = (int32_t)m.b;
   if (m.n > 2) out[2] = (int32_t)m.c;
+}
+
+// Four bytes.  Every pair of adjacent parts spans a slice of the piece, so
+// the loop only ever asks for the ranks of the three byte pairs, the two
+// triples and the whole: six independent loads, then the loop written out
+// by cases on the cut each round removes (cuts 1, 2, 3 between the bytes).
+__device__ __forceinline__ int merge4(const MergeTabs T, const uint8_t* b, int32_t* out) {
+  const uint32_t b0 = b[0], b1 = b[1], b2 = b[2], b3 = b[3];
+  const uint32_t ka = b0 | b1 << 8 | b2 << 16, kb = b1 | b2 << 8 | b3 << 16, kw = ka | b3 << 24;
+  const uint64_t sa = s34_first(T, ka), sb = s34_first(T, kb), sw = s34_first(T, kw);
+  const uint32_t r01 = dense_rank(T, b0, b1), r12 = dense_rank(T, b1, b2), r23 = dense_rank(T, b2, b3);
+  const uint32_t i0 = __ldg(&T.byte_id[b0]), i1 = __ldg(&T.byte_id[b1]);
+  const uint32_t i2 = __ldg(&T.byte_id[b2]), i3 = __ldg(&T.byte_id[b3]);
+  const uint32_t r012 = s34_rank(T, sa, ka, false), r123 = s34_rank(T, sb, kb, false);
+  const uint32_t r0123 = s34_rank(T, sw, kw, true);
+  if (r01 == RANK_MAX && r12 == RANK_MAX && r23 == RANK_MAX) {
+    out[0] = (int32_t)i0; out[1] = (int32_t)i1; out[2] = (int32_t)i2; out[3] = (int32_t)i3;
+    return 4;
+  }
+  // round 1 removes cut c1 (the leftmost least pair rank)
+  const int c1 = (r01 <= r12 && r01 <= r23) ? 1 : (r12 <= r23 ? 2 : 3);
+  // round 2: the pairs around the two remaining cuts
+  //   c1 = 1: [01][2][3]  left slice 012, right slice 23
+  //   c1 = 2: [0][12][3]  left slice 012, right slice 123
+  //   c1 = 3: [0][1][23]  left slice 01,  right slice 123
+  const uint32_t rl = c1 == 3 ? r01 : r012, rr = c1 == 1 ? r23 : r123;
+  if (rl == RANK_MAX && rr == RANK_MAX) {
+    out[0] = (int32_t)(c1 == 1 ? r01 : i0);
+    out[1] = (int32_t)(c1 == 1 ? i2 : (c1 == 2 ? r12 : i1));
+    out[2] = (int32_t)(c1 == 3 ? r23 : i3);
+    return 3;
+  }
+  // round 3: the two parts left span the whole piece
+  if (r0123 != RANK_MAX) {
+    out[0] = (int32_t)r0123;
+    return 1;
+  }
+  const bool left = rl <= rr;
+  //   left,  c1 != 3: [012][3];  left,  c1 == 3: [01][23]
+  //   right, c1 == 1: [01][23];  right, c1 != 1: [0][123]
+  const bool split22 = left ? c1 == 3 : c1 == 1;
+  out[0] = (int32_t)(split22 ? r01 : (left ? r012 : i0));
+  out[1] = (int32_t)(split22 ? r23 : (left ? i3 : r123));
+  return 2;
 }
 
 // One pre-token of 1..16 bytes: closed forms for one and two bytes (the
@@ -1051,7 +1098,7 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
     put3(out, m);
     return (int)m.n;
   }
-  if (n <= 4) return merge_reg<4>(T, b, n, out);
+  if (n == 4) return merge4(T, b, out);
   if (n <= 8) return merge_reg<8>(T, b, n, out);
   if constexpr (SHORT_MAX <= 12) {
     return merge_reg<12>(T, b, n, out);
@@ -1063,7 +1110,7 @@ __device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, 
 
 // Length class of a pre-token for the tile's work list (warps then run
 // pieces of one class together).
-constexpr int N_CLASSES = SHORT_MAX;  // one class per length: a warp's lanes get
+constexpr int N_CLASSES = MID_MIN - 1;  // one class per length: a warp's lanes get
                                      // pieces of one length (the same loop width
                                      // and similar step counts)
 __device__ __forceinline__ int len_class(int n) { return n - 1; }
@@ -1387,28 +1434,27 @@ __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t 
 }
 
 // --------------------------------------------------------------------------
-// Fused encode of one 4 KiB tile: the pre-tokens that start in the tile are
-// merged (one thread each up to SHORT_MAX bytes, one warp up to MEDIUM_MAX,
-// the whole CTA above), their ids compacted in shared memory, the tile's
-// output offset taken by decoupled look-back, and the ids written in order.
+// Fused encode of one 4 KiB tile: the pre-tokens of up to MID_MIN - 1 bytes
+// that start in the tile are merged here (one thread each), their ids
+// compacted in shared memory and staged with the tile's count.  Longer ones
+// (merged by k_merge_mid and the long-piece kernels, on the side stream) are
+// entries of the slot's table, in text order, for k_long_fixup.
 
 constexpr int ETHREADS = 256;
 constexpr int EPAD = 96;                 // bytes loaded past the tile (short pieces, specials)
 constexpr int MEDIUM_MAX = 1024;
 constexpr int64_t CLUSTER_MIN = 32768;   // longer pieces merge on a CTA cluster
 constexpr int MERGE_CL = 8;              // CTAs per cluster (portable size)
-constexpr int MAX_GP = TILE / (SHORT_MAX + 1) + 2;  // pieces merged through global memory
+constexpr int MAX_GP = TILE / MID_MIN + 2;  // table entries of a tile (pieces of >= MID_MIN bytes)
 constexpr int REG_MAX = 16;  // pieces up to this length merge in registers
 constexpr uint32_t NO_START = 0xFFFFFFFFu;
-constexpr int64_t STG = TILE + SHORT_MAX + 8;       // staging slot per tile (u32 entries)
+// Staging slot per tile (u32 entries): the short ids from the front (rounded
+// up to 4), 4 words per table entry from the back.  Pieces starting in the
+// tile are disjoint and the table's are at least MID_MIN bytes long, so the
+// short ids + MID_MIN * entries <= TILE + MID_MIN - 1: both parts fit.
+constexpr int64_t STG = TILE + SHORT_MAX + 8;
+static_assert(MID_MIN >= 5 && TILE + MID_MIN - 1 + 3 <= STG, "staging slot bound");
 constexpr uint32_t DTAB_LOG2 = 20;                  // dedup table of long pieces: 2^20 slots
-
-// A pre-token over SHORT_MAX bytes starting in the tile: merged by the
-// long-piece kernels; its count and source are added by k_long_fixup.
-struct GPiece {
-  uint32_t rel;         // start in the tile
-  uint32_t short_excl;  // short ids of the tile before it
-};
 
 struct EncSmem {
   uint8_t text[TILE + EPAD + 16];
@@ -1423,8 +1469,8 @@ struct EncSmem {
     uint16_t list[TILE + SHORT_MAX];    // work list: x | (len - 1) << 12 (until the merges end)
     __align__(16) int32_t outs[TILE + SHORT_MAX + 4];  // then the tile's short ids in order
   };
-  GPiece gp[MAX_GP];
   uint32_t th_full[ETHREADS];           // short ids before each thread's 16 bytes
+  uint16_t th_gp[ETHREADS];             // table entries before each thread's 16 bytes
   uint32_t warp_tot[2 * ETHREADS / 32];
   int64_t red64[ETHREADS / 32];
   uint32_t red32[ETHREADS / 32];
@@ -1447,15 +1493,17 @@ __device__ int32_t special_id_smem(const Tables& T, const uint8_t* b, int len) {
 }
 
 // Short ids before byte x of the tile (x in [0, TILE)), counted from the tile
-// start (k_long_fixup adds the long pieces before x).
+// start, | the table entries before x << 16 (k_long_fixup replaces them by
+// the ids of those entries).
 __device__ uint32_t ids_before(const EncSmem& sm, int x) {
   const int t = x >> 4;
-  uint32_t r = sm.th_full[t];
+  uint32_t r = sm.th_full[t], g = sm.th_gp[t];
   for (int y = t << 4; y < x; y++) {
     if (!((sm.pb[y >> 5] >> (y & 31)) & 1u)) continue;  // not a pre-token start
     if (!((sm.gb[y >> 5] >> (y & 31)) & 1u)) r += sm.cnt[y];
+    else g++;
   }
-  return r;
+  return r | (g << 16);
 }
 
 __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
@@ -1490,7 +1538,6 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     }
     if (tid < 2 * N_CLASSES + 1) sm.cls_cnt[tid] = 0;
     if (tid == 0) {
-      sm.n_gp = 0;
       sm.mnext = 0;
       sm.n_starts = 0;
       sm.seg[0] = c.W.tile_segs[4 * tile + 1];
@@ -1527,16 +1574,14 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       if ((sm.sb[x >> 5] >> (x & 31)) & 1u) {
         sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)len);
         sm.cnt[x] = 1;
-      } else if (len <= SHORT_MAX) {
+      } else if (len < MID_MIN) {
         sm.plen[x] = (uint8_t)len;
         atomicAdd(&sm.cls_cnt[len_class((int)len)], 1u);
       } else {
-        // merged by the long-piece kernels, which may still be running: the
-        // tile records where the piece is; k_long_fixup adds its ids' count
-        const int g = atomicAdd(&sm.n_gp, 1);
-        sm.gp[g] = GPiece{(uint32_t)x, 0u};
+        // merged on the side stream, which may still be running: the tile
+        // records where the piece is; k_long_fixup adds its ids' count
         atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
-        sm.cnt[x] = 0;
+        sm.cnt[x] = len <= SHORT_MAX;  // 1: a mid piece, its own source (no dedup)
       }
     }
     __syncthreads();
@@ -1580,22 +1625,17 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     }
     __syncthreads();
     uint32_t my_short = 0;
-    for (uint32_t bits = my; bits; bits &= bits - 1) {
-      const int x = xb + __ffs(bits) - 1;
-      if (!((sm.gb[x >> 5] >> (x & 31)) & 1u)) my_short += sm.cnt[x];
-    }
+    const uint32_t my_g = my & ((sm.gb[xb >> 5] >> (xb & 31)) & 0xFFFFu);
+    for (uint32_t bits = my & ~my_g; bits; bits &= bits - 1) my_short += sm.cnt[xb + __ffs(bits) - 1];
     atomicAdd(&sm.n_starts, (uint32_t)__popc(my));
     __syncthreads();
-    const int ngp = sm.n_gp;
-    if (tid == 0) {
-      atomicAdd((unsigned long long*)&c.W.status->n_ptok, (unsigned long long)sm.n_starts);
-      if (ngp) atomicAdd(&c.W.status->n_long, (uint32_t)ngp);
-    }
-    // 4. per-thread short-id counts -> block scan -> the tile's short ids
-    //    (k_long_fixup adds the long pieces to the counts)
-    uint32_t th_short = 0;
+    if (tid == 0) atomicAdd((unsigned long long*)&c.W.status->n_ptok, (unsigned long long)sm.n_starts);
+    // 4. per-thread counts (short ids | table entries << 16; a tile has fewer
+    //    than 2^16 of each) -> block scan (k_long_fixup adds the table's ids)
+    uint32_t th_short = 0, th_g = 0;
+    const uint32_t mine = my_short | ((uint32_t)__popc(my_g) << 16);
     {
-      uint32_t a = my_short;
+      uint32_t a = mine;
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t ya = __shfl_up_sync(0xffffffffu, a, o);
         if (lane >= o) a += ya;
@@ -1612,20 +1652,24 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
         sm.tile_short = ra;
       }
       __syncthreads();
-      th_short = sm.warp_tot[warp] + a - my_short;
+      const uint32_t ex = sm.warp_tot[warp] + a - mine;
+      th_short = ex & 0xFFFFu;
+      th_g = ex >> 16;
       sm.th_full[tid] = th_short;
+      sm.th_gp[tid] = (uint16_t)th_g;
     }
     __syncthreads();
-    // 5. compaction of short ids (in order, in shared memory); offsets of
-    //    the global pieces
+    const uint32_t tile_short = sm.tile_short & 0xFFFFu, ngp = sm.tile_short >> 16;
+    // 5. compaction of short ids (in order, in shared memory); the table
+    //    entries (short ids before the piece, its start in the tile) in order
     uint32_t* slot = c.W.staging + tile * STG;
     {
-      uint32_t s = th_short;
+      uint32_t s = th_short, g = th_g;
       for (uint32_t bits = my; bits; bits &= bits - 1) {
         const int x = xb + __ffs(bits) - 1;
-        if ((sm.gb[x >> 5] >> (x & 31)) & 1u) {
-          for (int g = 0; g < ngp; g++)
-            if ((int)sm.gp[g].rel == x) sm.gp[g].short_excl = s;
+        if ((my_g >> (x - xb)) & 1u) {
+          *reinterpret_cast<uint4*>(slot + STG - 4 * (g + 1)) = make_uint4(s, (uint32_t)x, sm.cnt[x], 0u);
+          g++;
           continue;
         }
         const uint32_t m = sm.cnt[x];
@@ -1635,21 +1679,13 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     }
     __syncthreads();
     // 6. the short ids to the staging slot (16-byte stores: the slot has room
-    //    for the rounding before its long-piece table), the table of pieces
-    //    merged through global memory at the slot's end; the tile's id count;
-    //    segment offsets relative to the tile
-    for (uint32_t v = tid; 4 * v < sm.tile_short; v += ETHREADS)
+    //    for the rounding before its table); the tile's id count; segment
+    //    offsets relative to the tile
+    for (uint32_t v = tid; 4 * v < tile_short; v += ETHREADS)
       reinterpret_cast<uint4*>(slot)[v] = reinterpret_cast<const uint4*>(sm.outs)[v];
-    for (int g = tid; g < ngp; g += ETHREADS) {
-      uint32_t* e = slot + STG - 4 * (g + 1);
-      e[0] = sm.gp[g].short_excl;
-      e[1] = sm.gp[g].rel;  // k_long_fixup: full_excl, src, cnt
-      e[2] = 0;
-      e[3] = 0;
-    }
     if (tid == 0) {
-      c.W.tile_count[tile] = sm.tile_short;
-      c.W.tile_meta[tile] = sm.tile_short | ((uint32_t)ngp << 24);
+      c.W.tile_count[tile] = tile_short;
+      c.W.tile_meta[tile] = tile_short | (ngp << 16);
     }
     for (int64_t s = sm.seg[0] + tid; s < sm.seg[1]; s += ETHREADS) {
       const int64_t x = c.seg_off[s] - t0;
@@ -1659,90 +1695,111 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
   }
 }
 
-// Adds the long pieces to the tile counts once their merges are done: per
-// tile with long pieces (one warp), each entry of the staging slot's table
-// gets its source in the arena, its id count and the ids before it in the
-// tile (full_excl = short ids before it + the long pieces before it); the
-// tile count and the offsets of the tile's segments grow by the long
-// pieces before them.
-constexpr int FIX_PER_LANE = (MAX_GP + 31) / 32;
+// Adds the table's pieces to the tile counts once their merges are done: per
+// tile with table entries (one warp), each entry (in text order) gets its
+// source in the arena, its id count and the ids of the tile before it
+// (full_excl = short ids before it + the table's ids before it: a warp scan
+// over the entries); the tile count grows by the table's ids, and each
+// segment offset in the tile by the ids of the entries before it.
+constexpr int FIX_BATCH = 4;
 __global__ void __launch_bounds__(ETHREADS) k_long_fixup(Call c) {
   const int lane = threadIdx.x & 31;
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t tile = gw; tile < ntiles; tile += nw) {
-    const int ngp = (int)(c.W.tile_meta[tile] >> 24);
+    const int ngp = (int)(c.W.tile_meta[tile] >> 16);
     if (ngp == 0) continue;
     const int64_t t0 = tile * TILE;
     uint32_t* slot = c.W.staging + tile * STG;
-    // 1. source and count of each entry
-    for (int g = lane; g < ngp; g += 32) {
-      uint32_t* e = slot + STG - 4 * (g + 1);
-      const uint32_t src = c.W.gsrc[c.gb + t0 + e[1]] & ~GSRC_CACHED;
-      e[2] = src;
-      e[3] = c.W.cnt[src];
-    }
-    __syncwarp();
-    // 2. ids of the long pieces before each entry and before each segment
-    uint32_t fe[FIX_PER_LANE];
-    uint32_t total = 0;
+    uint32_t carry = 0;  // the table's ids before this group of entries
+    // FIX_BATCH entries per lane per pass, their loads issued together (the
+    // entry, then for a long piece its source, then the count)
+    for (int g0 = 0; g0 < ngp; g0 += 32 * FIX_BATCH) {
+      uint4 e[FIX_BATCH];
 #pragma unroll
-    for (int k = 0; k < FIX_PER_LANE; k++) {
-      const int g = lane + 32 * k;
-      fe[k] = 0;
-      if (g < ngp) {
-        const uint32_t* e = slot + STG - 4 * (g + 1);
-        uint32_t before = 0;
-        for (int h = 0; h < ngp; h++) {
-          const uint32_t* f = slot + STG - 4 * (h + 1);
-          if (f[1] < e[1]) before += f[3];
+      for (int u = 0; u < FIX_BATCH; u++) {
+        const int g = g0 + 32 * u + lane;
+        e[u] = g < ngp ? *reinterpret_cast<const uint4*>(slot + STG - 4 * (g + 1)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < FIX_BATCH; u++) {
+        const int g = g0 + 32 * u + lane;
+        const uint32_t G = (uint32_t)(c.gb + t0 + e[u].y);
+        // z = 1: a mid piece (its own source); else the owner from gsrc
+        if (g < ngp) e[u].z = e[u].z ? G : (c.W.gsrc[G] & ~GSRC_CACHED);
+      }
+#pragma unroll
+      for (int u = 0; u < FIX_BATCH; u++) {
+        const int g = g0 + 32 * u + lane;
+        e[u].w = g < ngp ? c.W.cnt[e[u].z] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < FIX_BATCH; u++) {
+        const int g = g0 + 32 * u + lane;
+        uint32_t incl = e[u].w;
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        fe[k] = e[0] + before;
-        total += e[3];
+        if (g < ngp) {
+          e[u].y = e[u].x + carry + incl - e[u].w;
+          *reinterpret_cast<uint4*>(slot + STG - 4 * (g + 1)) = e[u];
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
-    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    __syncwarp();
+    // segment offsets: short ids | entries before << 16 -> ids before
     const int64_t sg0 = c.W.tile_segs[4 * tile + 1];
     const int64_t sg1 = (tile == ntiles - 1) ? c.S + 1 : c.W.tile_segs[4 * tile + 2];
     for (int64_t sg = sg0 + lane; sg < sg1; sg += 32) {
-      const int64_t x = c.seg_off[sg] - t0;
+      const uint32_t v = c.W.seg_rel[sg];
+      const uint32_t j = v >> 16;
       uint32_t add = 0;
-      for (int h = 0; h < ngp; h++) {
-        const uint32_t* f = slot + STG - 4 * (h + 1);
-        if ((int64_t)f[1] < x) add += f[3];
+      if (j > 0) {
+        const uint4 e = *reinterpret_cast<const uint4*>(slot + STG - 4 * j);  // entry j - 1
+        add = e.y + e.w - e.x;
       }
-      c.W.seg_rel[sg] += add;
+      c.W.seg_rel[sg] = (v & 0xFFFFu) + add;
     }
-    __syncwarp();
-    // 3. full_excl replaces the position (every lane has read the positions)
-#pragma unroll
-    for (int k = 0; k < FIX_PER_LANE; k++) {
-      const int g = lane + 32 * k;
-      if (g < ngp) slot[STG - 4 * (g + 1) + 1] = fe[k];
-    }
-    if (lane == 0) c.W.tile_count[tile] += total;
+    if (lane == 0) c.W.tile_count[tile] += carry;
   }
 }
 
 // Ordered output: each tile's staged ids go to out[tile_base + ...], with the
-// ids of its long pieces inserted from the arena.  A tile without long pieces
-// is one straight copy, 16 ids per thread in flight.  Long pieces of more than
-// HUGE_IDS ids are listed for k_copy_huge, which spreads them over the grid.
+// ids of its table's pieces inserted from the arena.  A tile without table
+// entries is one straight copy, 16 ids per thread in flight; with entries,
+// each output position finds the last entry that starts at or before it and
+// so its source: that entry's ids in the arena or the short ids after it.  A
+// table of the entry count at every 32nd output (one binary search each over
+// the entries' full_excl in shared memory) leaves each output a step or two.
+// Pieces of more than HUGE_IDS ids are listed for k_copy_huge, which spreads
+// them over the grid (their tiles take the per-part path below).
 constexpr uint32_t HUGE_IDS = 8192;
 constexpr int COPY_UNROLL = 16;
+// output blocks of 32 ids per tile on the searched path: the tile's own ids
+// (at most TILE + 4) and one piece of up to HUGE_IDS ids that starts in it
+constexpr int COPY_BLK = (TILE + 2 * (int)HUGE_IDS) / 32 + 2;
 static_assert((STG * sizeof(uint32_t)) % 16 == 0, "staging slots stay 16-byte aligned");
 
 __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int64_t cap) {
-  __shared__ uint32_t s_gp[MAX_GP * 4];
+  __shared__ uint4 s_gp[MAX_GP];  // (short_excl, full_excl, src, cnt) in text order
+  __shared__ uint16_t s_blk[COPY_BLK];  // entries with full_excl <= 32 b
+  __shared__ int s_huge;
+  static_assert(MAX_GP <= 1024, "the block search steps from 512");
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const int tid = threadIdx.x;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const uint64_t base = c.W.tile_base[tile];
-    const uint32_t meta = c.W.tile_meta[tile];
-    const uint32_t n_short = meta & 0xFFFFFFu;
-    const int ngp = (int)(meta >> 24);
     const uint32_t* slot = c.W.staging + tile * STG;
+    // the tile's count, base and first ETHREADS entries, loaded together
+    // (an entry past the table reads other words of the slot: unused)
+    const uint64_t base = c.W.tile_base[tile];
+    const uint32_t n_out = c.W.tile_base[tile + 1] - (uint32_t)base;
+    const uint32_t meta = c.W.tile_meta[tile];
+    const uint4 e0 = *reinterpret_cast<const uint4*>(slot + STG - 4 * (tid + 1));
+    const uint32_t n_short = meta & 0xFFFFu;
+    const int ngp = (int)(meta >> 16);
     if (ngp == 0) {
       for (uint32_t q0 = 0; q0 < n_short; q0 += COPY_UNROLL * ETHREADS) {
         uint32_t v[COPY_UNROLL];
@@ -1759,8 +1816,53 @@ __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int
       }
       continue;
     }
-    for (int i = tid; i < 4 * ngp; i += blockDim.x) s_gp[i] = slot[STG - 4 * ngp + i];
+    const uint32_t nblk = (n_out + 31) >> 5;
+    if (tid == 0) s_huge = nblk > (uint32_t)COPY_BLK;
     __syncthreads();
+    for (int g = tid; g < ngp; g += blockDim.x) {
+      const uint4 e = g == tid ? e0 : *reinterpret_cast<const uint4*>(slot + STG - 4 * (g + 1));
+      s_gp[g] = e;
+      if (e.w > HUGE_IDS) s_huge = 1;
+    }
+    __syncthreads();
+    if (!s_huge) {
+      for (uint32_t b = tid; b < nblk; b += blockDim.x) {
+        int j = 0;
+#pragma unroll
+        for (int step = 512; step > 0; step >>= 1)
+          if (j + step <= ngp && s_gp[j + step - 1].y <= 32 * b) j += step;
+        s_blk[b] = (uint16_t)j;
+      }
+      __syncthreads();
+      for (uint32_t o0 = 0; o0 < n_out; o0 += COPY_UNROLL * ETHREADS) {
+        int32_t v[COPY_UNROLL];
+#pragma unroll
+        for (int k = 0; k < COPY_UNROLL; k++) {
+          const uint32_t o = o0 + k * ETHREADS + tid;
+          v[k] = 0;
+          if (o < n_out) {
+            int j = s_blk[o >> 5];  // entries with full_excl <= o
+            while (j < ngp && s_gp[j].y <= o) j++;
+            const int32_t* a = reinterpret_cast<const int32_t*>(slot) + o;
+            if (j > 0) {
+              const uint4 e = s_gp[j - 1];
+              const uint32_t r = o - e.y;
+              a = r < e.w ? c.W.arena + e.z + r : reinterpret_cast<const int32_t*>(slot) + (e.x + r - e.w);
+            }
+            v[k] = *a;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < COPY_UNROLL; k++) {
+          const uint32_t o = o0 + k * ETHREADS + tid;
+          if (o < n_out && base + o < (uint64_t)cap) out[base + o] = v[k];
+        }
+      }
+      __syncthreads();
+      continue;
+    }
+    // short id q follows the entries whose short_excl <= q: the last such
+    // entry j gives its shift, full_excl + cnt - short_excl
     for (uint32_t q0 = 0; q0 < n_short; q0 += COPY_UNROLL * ETHREADS) {
       uint32_t v[COPY_UNROLL];
 #pragma unroll
@@ -1772,27 +1874,46 @@ __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int
       for (int k = 0; k < COPY_UNROLL; k++) {
         const uint32_t q = q0 + k * ETHREADS + tid;
         if (q >= n_short) continue;
-        // short id q follows every long piece whose short prefix is <= q
+        int lo = 0, hi = ngp;  // entries [0, lo) have short_excl <= q
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s_gp[mid].x <= q) lo = mid + 1;
+          else hi = mid;
+        }
         uint64_t pos = base + q;
-        for (int g = 0; g < ngp; g++)
-          if (s_gp[4 * g] <= q) pos += s_gp[4 * g + 3];
+        if (lo > 0) {
+          const uint4 e = s_gp[lo - 1];
+          pos += e.y + e.w - e.x;
+        }
         if (pos < (uint64_t)cap) out[pos] = (int32_t)v[k];
       }
     }
-    for (int g = 0; g < ngp; g++) {
-      const uint32_t* e = s_gp + 4 * (ngp - 1 - g);
-      const uint64_t o = base + e[1];
-      if (e[3] > HUGE_IDS) {
-        if (tid == 0) {
+    // the entries' ids: up to 32 by one thread each, longer ones by a warp
+    // each, over HUGE_IDS listed for k_copy_huge
+    for (int g = tid; g < ngp; g += blockDim.x) {
+      const uint4 e = s_gp[g];
+      if (e.w > 32) continue;
+      const int32_t* src = c.W.arena + e.z;
+      const uint64_t o = base + e.y;
+      for (uint32_t j = 0; j < e.w; j++)
+        if (o + j < (uint64_t)cap) out[o + j] = src[j];
+    }
+    const int lane = tid & 31;
+    for (int g = tid >> 5; g < ngp; g += blockDim.x >> 5) {
+      const uint4 e = s_gp[g];
+      if (e.w <= 32) continue;
+      const uint64_t o = base + e.y;
+      if (e.w > HUGE_IDS) {
+        if (lane == 0) {
           const uint32_t k = atomicAdd(&c.W.status->n_huge, 1u);
           c.W.huge_list[3 * (uint64_t)k] = o;
-          c.W.huge_list[3 * (uint64_t)k + 1] = e[2];
-          c.W.huge_list[3 * (uint64_t)k + 2] = e[3];
+          c.W.huge_list[3 * (uint64_t)k + 1] = e.z;
+          c.W.huge_list[3 * (uint64_t)k + 2] = e.w;
         }
         continue;
       }
-      const int32_t* src = c.W.arena + e[2];
-      for (uint32_t j = tid; j < e[3]; j += blockDim.x)
+      const int32_t* src = c.W.arena + e.z;
+      for (uint32_t j = lane; j < e.w; j += 32)
         if (o + j < (uint64_t)cap) out[o + j] = src[j];
     }
     __syncthreads();
@@ -1838,6 +1959,7 @@ __global__ void k_seg_offsets(Call c, int64_t* out_offsets, int64_t* id_base) {
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     c.W.status->n_ids = c.W.tile_base[ntiles];
+    c.W.status->n_long = c.W.status->n_medium + c.W.status->n_biglong + c.W.status->n_cl;
     if (id_base) id_base[1] = b + c.W.tile_base[ntiles];
   }
 }
@@ -1869,11 +1991,8 @@ __device__ int64_t piece_end(const Call& c, int64_t p, int64_t ntiles) {
 
 // Pre-tokens longer than SHORT_MAX bytes -> three work lists (medium: one warp
 // each, big: one CTA each, longest: one CTA cluster each), as (start, length)
-// pairs.  One thread per word of the start bitmap: a start's length is the
-// distance to the next start in the word; for the word's last start the next
-// words decide.
+// pairs.
 __device__ __forceinline__ void list_long(const Call& c, int64_t p, int64_t len) {
-  if (c.T.n_spec && bit_get(c.W.sbits, p)) return;  // specials are one id
   if (len <= MEDIUM_MAX) {
     const uint32_t k = atomicAdd(&c.W.status->n_medium, 1u);
     c.W.long_list[2 * k] = (uint32_t)p;
@@ -1889,54 +2008,85 @@ __device__ __forceinline__ void list_long(const Call& c, int64_t p, int64_t len)
   }
 }
 
-__global__ void k_find_long(Call c) {
+// The pre-tokens of MID_MIN bytes or more: mid pieces (up to SHORT_MAX
+// bytes) -> mid_list, up to 8 bytes from the front and longer ones from the
+// back (k_merge_mid gives a warp one of the two); longer ones -> list_long.
+// Each thread reads FIND_WPT words of the start bitmap; a start's length is
+// the distance to the next start bit (the next word is in reach of every
+// start of the word; the text end counts as a start), else piece_end.  The
+// mid entries of a warp take one atomic per list: a count pass, a warp scan,
+// then a write pass.  Specials are one id each, left to the tile kernel.
+constexpr int FIND_WPT = 8;
+__global__ void __launch_bounds__(256) k_find_long(Call c) {
+  const int lane = threadIdx.x & 31;
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const int64_t nwords = (c.n + 31) >> 5;
-  for (int64_t wi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; wi < nwords;
-       wi += (int64_t)gridDim.x * blockDim.x) {
-    uint32_t bits = c.W.pbits[wi];
-    if ((wi << 5) + 32 > c.n) bits &= (1u << (c.n - (wi << 5))) - 1u;
-    if (!bits) continue;
-    const int last = 31 - __clz(bits);
-    // starts followed by another start within SHORT_MAX bytes, from
-    // this word and the next (the text end counts as a start)
-    uint64_t w = bits;
-    if ((wi << 5) + 32 < c.n) {
-      uint32_t nx = c.W.pbits[wi + 1];
-      if ((wi << 5) + 64 > c.n) nx |= ~((1u << (c.n - (wi << 5) - 32)) - 1u);
-      w |= (uint64_t)nx << 32;
-    } else {
-      w |= ~0ull << (c.n - (wi << 5));
-    }
-    static_assert(SHORT_MAX >= 2 && SHORT_MAX <= 31, "the shift ladder covers 1 .. SHORT_MAX");
-    uint64_t near = w >> 1;  // near = OR of w >> d for d = 1 .. SHORT_MAX
-    int span = 1;            // near covers d = 1 .. span
-#pragma unroll
-    for (int k = 0; k < 5; k++)
-      if (2 * span <= SHORT_MAX) {
-        near |= near >> span;
-        span *= 2;
+  const int64_t nch = (nwords + FIND_WPT - 1) / FIND_WPT;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b0 = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); b0 < nch; b0 += stride) {
+    const int64_t ch = b0 + lane;
+    uint32_t ia = 0, ib = 0;
+    for (int pass = 0; pass < 2; pass++) {
+      if (pass == 1) {
+        // exclusive warp scans of the counts, one atomic per list
+        uint32_t sa = ia, sb = ib;
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t ya = __shfl_up_sync(0xffffffffu, sa, o), yb = __shfl_up_sync(0xffffffffu, sb, o);
+          if (lane >= o) { sa += ya; sb += yb; }
+        }
+        uint32_t ba = 0, bb = 0;
+        if (lane == 31) {
+          if (sa) ba = atomicAdd(&c.W.status->n_mid_a, sa);
+          if (sb) bb = atomicAdd(&c.W.status->n_mid_b, sb);
+        }
+        ba = __shfl_sync(0xffffffffu, ba, 31);
+        bb = __shfl_sync(0xffffffffu, bb, 31);
+        ia = ba + sa - ia;
+        ib = bb + sb - ib;
       }
-    if (span < SHORT_MAX) near |= near >> (SHORT_MAX - span);
-    for (uint32_t bb = bits & ~(1u << last) & ~(uint32_t)near; bb; bb &= bb - 1) {
-      const int x = __ffs(bb) - 1;
-      const uint32_t later = bits & ~((2u << x) - 1u);
-      list_long(c, (wi << 5) + x, __ffs(later) - 1 - x);
+      for (int k = 0; k < FIND_WPT; k++) {
+        const int64_t wi = ch * FIND_WPT + k;
+        if (ch >= nch || wi >= nwords) break;
+        uint32_t bits = c.W.pbits[wi];
+        if ((wi << 5) + 32 > c.n) bits &= (1u << (c.n - (wi << 5))) - 1u;
+        if (!bits) continue;
+        uint64_t w = bits;
+        if ((wi << 5) + 32 < c.n) {
+          uint32_t nx = c.W.pbits[wi + 1];
+          if ((wi << 5) + 64 > c.n) nx |= ~((1u << (c.n - (wi << 5) - 32)) - 1u);
+          w |= (uint64_t)nx << 32;
+        } else {
+          w |= ~0ull << (c.n - (wi << 5));
+        }
+        static_assert(MID_MIN == 5 && SHORT_MAX <= 32, "one look at the next word covers SHORT_MAX");
+        const uint64_t near4 = (w >> 1) | (w >> 2) | (w >> 3) | (w >> 4);
+        for (uint32_t cand = bits & ~(uint32_t)near4; cand; cand &= cand - 1) {
+          const int x = __ffs(cand) - 1;
+          const int64_t p = (wi << 5) + x;
+          if (c.T.n_spec && bit_get(c.W.sbits, p)) continue;
+          const uint64_t nxt = w >> (x + 1);
+          const int d = nxt ? __ffsll((long long)nxt) : 0;  // length, if the next start is in w
+          if (d >= MID_MIN && d <= SHORT_MAX) {
+            if (pass == 0) {
+              if (d <= 8) ia++;
+              else ib++;
+            } else if (d <= 8) {
+              c.W.mid_list[2 * (int64_t)ia] = (uint32_t)p;
+              c.W.mid_list[2 * (int64_t)ia + 1] = (uint32_t)d;
+              ia++;
+            } else {
+              const int64_t e = c.W.mid_cap - 1 - ib;
+              c.W.mid_list[2 * e] = (uint32_t)p;
+              c.W.mid_list[2 * e + 1] = (uint32_t)d;
+              ib++;
+            }
+          } else if (pass == 1) {
+            const int64_t len = d ? d : piece_end(c, p, ntiles) - p;
+            if (len > SHORT_MAX) list_long(c, p, len);
+          }
+        }
+      }
     }
-    const int64_t p = (wi << 5) + last;
-    // the last start: is there another start within SHORT_MAX bytes?
-    bool short_piece = false;
-    for (int k = 1; k <= 3 && !short_piece; k++) {
-      const int64_t w2 = wi + k;
-      if ((w2 << 5) >= c.n) { short_piece = (c.n - p) <= SHORT_MAX; break; }
-      uint32_t b2 = c.W.pbits[w2];
-      if ((w2 << 5) + 32 > c.n) b2 |= ~((1u << (c.n - (w2 << 5))) - 1u);  // the text end ends the piece
-      if (b2) short_piece = (w2 << 5) + __ffs(b2) - 1 - p <= SHORT_MAX;
-      else if ((w2 << 5) + 32 - p > SHORT_MAX) break;
-    }
-    if (short_piece) continue;
-    const int64_t e = piece_end(c, p, ntiles);
-    if (e - p > SHORT_MAX) list_long(c, p, e - p);
   }
 }
 
@@ -2369,6 +2519,41 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
   }
 }
 
+// Mid pieces (MID_MIN..SHORT_MAX bytes): one thread each over the whole
+// grid, the register loop of the width the warp's longest piece needs (the
+// front of mid_list: up to 8 bytes; the back: 12 or 16).  Ids to the arena at
+// the piece's start, the count beside them; each piece is its own source (the
+// tile kernel marks its table entry so).
+__global__ void __launch_bounds__(ETHREADS) k_merge_mid(Call c) {
+  const MergeTabs MT(c.T);
+  const int lane = threadIdx.x & 31;
+  const int64_t na = c.W.status->n_mid_a, nm = na + c.W.status->n_mid_b;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b0 = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); b0 < nm; b0 += stride) {
+    const int64_t i = b0 + lane;
+    const bool valid = i < nm, front = i < na;
+    int len = 0;
+    int64_t p = 0;
+    if (valid) {
+      const int64_t k = front ? i : c.W.mid_cap - 1 - (i - na);
+      p = c.W.mid_list[2 * k];
+      len = (int)c.W.mid_list[2 * k + 1];
+    }
+    const int wmax = __reduce_max_sync(0xffffffffu, (valid && !front) ? len : 0);
+    if (!valid) continue;
+    uint8_t b[16];
+#pragma unroll
+    for (int j = 0; j < 16; j++) b[j] = j < len ? gbyte(c, p + j) : 0;
+    const int64_t G = c.gb + p;
+    int32_t* dst = c.W.arena + G;
+    int m;
+    if (front) m = merge_reg<8>(MT, b, len, dst);
+    else if (wmax <= 12) m = merge_reg<12>(MT, b, len, dst);
+    else m = merge_reg<16>(MT, b, len, dst);
+    c.W.cnt[G] = (uint32_t)m;
+  }
+}
+
 // Offsets of an encode with no text: every segment is empty.
 __global__ void k_empty_offsets(Call c, int64_t* out_offsets, int64_t* id_base) {
   const int64_t b = id_base ? id_base[0] : 0;
@@ -2423,6 +2608,7 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
   w.max_bytes = max_bytes;
   w.max_segments = max_segments;
   w.dtab_log2 = DTAB_LOG2;
+  w.mid_cap = nb / MID_MIN + 2;
   struct Req { void** p; size_t bytes; };
   Req reqs[] = {
       {(void**)&w.status, sizeof(Status)},
@@ -2440,6 +2626,7 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.offs, sizeof(uint32_t) * nbp},
       {(void**)&w.arena, sizeof(int32_t) * nbp},
       {(void**)&w.long_list, sizeof(uint32_t) * 2 * (nb / (SHORT_MAX + 1) + 2)},
+      {(void**)&w.mid_list, sizeof(uint32_t) * 2 * (size_t)(nb / MID_MIN + 2)},
       {(void**)&w.staging, sizeof(uint32_t) * (size_t)(n_split_tiles * STG)},
       {(void**)&w.tile_count, sizeof(uint32_t) * (n_split_tiles + 1)},
       {(void**)&w.tile_base, sizeof(uint32_t) * (n_split_tiles + 2)},
@@ -2577,7 +2764,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     TK_CUDA(cudaEventRecord(ws->ev_split, st), "fork");
     TK_CUDA(cudaStreamWaitEvent(side, ws->ev_split, 0), "fork");
     tk_prof_mark(ws, "k_find_long", side);
-    k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 16) + 255) / 256, (int64_t)sms * 16), 256, 0, side>>>(c);
+    k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 32 / FIND_WPT) + 255) / 256, (int64_t)sms * 16), 256, 0, side>>>(c);
     tk_prof_mark(ws, "k_dedup_medium", side);
     k_dedup_medium<<<sms * 8, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_dedup_big", side);
@@ -2594,6 +2781,8 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), BIG_THREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_medium", side);
     k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
+    tk_prof_mark(ws, "k_merge_mid", side);
+    k_merge_mid<<<sms * 8, ETHREADS, 0, side>>>(c);
     if (c.W.use_cache) {
       tk_prof_mark(ws, "k_cache_insert", side);
       k_cache_insert<<<sms * 8, ETHREADS, 0, side>>>(c);
@@ -2612,7 +2801,10 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     int rc = tk_scan_u32(ws, ws->w.tile_count, ws->w.tile_base, &ws->w.status->n_tiles, n_split_tiles, 3, st);
     if (rc) return rc;
     tk_prof_mark(ws, "k_copy_out", st);
-    k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * 8), ETHREADS, 0, st>>>(c, d_out, cap);
+    int copy_per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&copy_per_sm, k_copy_out, ETHREADS, 0);
+    k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(copy_per_sm, 1)), ETHREADS, 0, st>>>(
+        c, d_out, cap);
     tk_prof_mark(ws, "k_copy_huge", st);
     k_copy_huge<<<sms * 4, ETHREADS, 0, st>>>(c, d_out, cap);
     tk_prof_mark(ws, "k_seg_offsets", st);

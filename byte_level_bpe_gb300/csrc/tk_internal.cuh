@@ -22,7 +22,9 @@ constexpr int HALO = 128;
 constexpr int TRUST = 64;
 constexpr int WIN = TILE + 2 * HALO;
 
-constexpr int SHORT_MAX = 16;   // pre-tokens up to this length merge inside the tile kernel
+constexpr int SHORT_MAX = 16;   // pre-tokens up to this length merge one per thread
+constexpr int MID_MIN = 5;      // ... those of MID_MIN..SHORT_MAX bytes over the whole grid
+                                // (k_merge_mid), the shorter ones inside the tile kernel
 constexpr int SCAN_THREADS = 256;
 constexpr int SCAN_ITEMS = 8;    // u32 counts per scan thread
 constexpr int SCAN_TILE = SCAN_THREADS * SCAN_ITEMS;
@@ -47,7 +49,9 @@ struct Status {
   int64_t err_pos;   // smallest invalid UTF-8 byte offset (INT64_MAX if none)
   int64_t n_ptok;    // pre-tokens found by the split
   int64_t n_ids;     // ids produced (may exceed the output capacity)
-  uint32_t n_long;   // pre-tokens merged through global memory (medium + long)
+  uint32_t n_long;   // pre-tokens over SHORT_MAX bytes (the long-piece lists)
+  uint32_t n_mid_a;  // mid pieces of MID_MIN..8 bytes (front of mid_list)
+  uint32_t n_mid_b;  // mid pieces of 9..SHORT_MAX bytes (back of mid_list)
   uint32_t n_medium;    // work list sizes and cursors of k_merge_global
   uint32_t n_biglong;
   uint32_t medium_next;
@@ -72,6 +76,10 @@ struct Tables {
   const uint64_t* pair_slots;  // open addressing: (a << 40) | (b << 20) | rank; empty = ~0
   uint32_t pair_log2;          // log2(number of slots)
   uint32_t pair_max_probe;     // longest probe sequence present in the table
+  const uint64_t* s34_slots;   // open addressing over the 3- and 4-byte tokens:
+                               // (bytes << 21) | (len == 4) << 20 | rank; empty = ~0
+  uint32_t s34_log2;
+  uint32_t s34_max_probe;
   const uint8_t* spec_bytes;   // specials, concatenated
   const int32_t* spec_off;     // [n_spec + 1]
   const int32_t* spec_ids;     // [n_spec]
@@ -119,12 +127,15 @@ struct Work {
   uint32_t* offs;       // [max_bytes + 1] decode: exclusive scan of cnt
   int32_t* arena;       // [max_bytes] ids of pieces merged through global memory, at their byte offset
   uint32_t* long_list;  // (start, length) of pre-tokens of SHORT_MAX+1 .. MEDIUM_MAX bytes
+  uint32_t* mid_list;   // (start, length) of pre-tokens of MID_MIN .. SHORT_MAX bytes:
+                        // up to 8 bytes from the front, longer ones from the back
+  int64_t mid_cap;      // entries of mid_list
   uint32_t* big_list;   // (start, length) of pre-tokens of MEDIUM_MAX+1 .. CLUSTER_MIN bytes
   uint32_t* cl_list;    // (start, length) of pre-tokens longer than CLUSTER_MIN bytes
   uint32_t* staging;    // per split tile: compacted short ids, long-piece table at the end
   uint32_t* tile_count; // per split tile: ids (then: exclusive scan -> tile_base)
   uint32_t* tile_base;  // [n_tiles + 1]
-  uint32_t* tile_meta;  // per split tile: short ids (low 24 bits) | long pieces << 24
+  uint32_t* tile_meta;  // per split tile: short ids (low 16 bits) | pieces merged outside << 16
   uint32_t* seg_rel;    // [max_segments + 1] ids before each segment start, within its tile
   uint32_t* tile_segs;  // per split tile: first segment index at or after t0 - HALO, t0,
                         // t0 + TILE, t0 + TILE + HALO
@@ -220,10 +231,20 @@ struct MergeTabs {
   const uint64_t* pair_slots;
   uint32_t pair_log2;
   uint32_t pair_max_probe;
+  const uint64_t* s34_slots;
+  uint32_t s34_log2;
+  uint32_t s34_max_probe;
   __device__ __host__ explicit MergeTabs(const Tables& T)
       : byte_id(T.byte_id), dense(T.dense), pair_slots(T.pair_slots), pair_log2(T.pair_log2),
-        pair_max_probe(T.pair_max_probe) {}
+        pair_max_probe(T.pair_max_probe), s34_slots(T.s34_slots), s34_log2(T.s34_log2),
+        s34_max_probe(T.s34_max_probe) {}
 };
+
+// Slot of a 3- or 4-byte slice (bytes little-endian in a 32-bit key) in the
+// slice table.
+__host__ __device__ __forceinline__ uint32_t s34_hash(uint32_t key, uint32_t log2) {
+  return (key * 0x9E3779B1u) >> (32 - log2);
+}
 
 // Load that bypasses L1 allocation (streams and big random tables), keeping
 // L1 for the small tables the merge reads on every pre-token.
@@ -305,6 +326,27 @@ __device__ __forceinline__ uint32_t pair_rank(const TT& T, uint32_t a, uint32_t 
     h = (h + 1) & mask;
   }
   return RANK_MAX;
+}
+
+// Rank of the 3- or 4-byte slice `key` (RANK_MAX if it is not a token),
+// given the slot `s` its first probe read (loaded early, so that this load
+// overlaps the pair loads it does not depend on).
+template <class TT>
+__device__ __forceinline__ uint32_t s34_rank(const TT& T, uint64_t s, uint32_t key, bool four) {
+  const uint64_t k = ((uint64_t)key << 1) | (four ? 1u : 0u);
+  uint32_t h = s34_hash(key, T.s34_log2);
+  for (uint32_t probe = 0;;) {
+    if (s == ~0ull) return RANK_MAX;
+    if ((s >> 20) == k) return (uint32_t)(s & 0xFFFFF);
+    if (++probe > T.s34_max_probe) return RANK_MAX;
+    h = (h + 1) & ((1u << T.s34_log2) - 1u);
+    s = __ldg(&T.s34_slots[h]);
+  }
+}
+
+template <class TT>
+__device__ __forceinline__ uint64_t s34_first(const TT& T, uint32_t key) {
+  return __ldg(&T.s34_slots[s34_hash(key, T.s34_log2)]);
 }
 
 }  // namespace tk

@@ -211,6 +211,27 @@ extern "C" int tk_load(const uint8_t* rank_bytes, const int64_t* rank_off, const
     slots[h] = (kv.first << 20) | kv.second;
     max_probe = std::max(max_probe, probe);
   }
+  // slice table of the 3- and 4-byte tokens (one probe, independent of the
+  // pair ranks, gives a three- or four-byte piece its longer slices)
+  std::vector<uint64_t> s34_items;
+  for (int64_t i = 0; i < n; i++) {
+    const int64_t len = rank_off[i + 1] - rank_off[i];
+    if (len != 3 && len != 4) continue;
+    const uint8_t* p = rank_bytes + rank_off[i];
+    const uint32_t key = p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (len == 4 ? (uint32_t)p[3] << 24 : 0u);
+    s34_items.push_back(((uint64_t)key << 21) | ((uint64_t)(len == 4) << 20) | rank_ids[i]);
+  }
+  uint32_t s34_log2 = 10;
+  while ((1ull << s34_log2) < 4 * s34_items.size() + 16) s34_log2++;
+  std::vector<uint64_t> s34(1ull << s34_log2, ~0ull);
+  uint32_t s34_max_probe = 0;
+  for (uint64_t it : s34_items) {
+    uint32_t h = s34_hash((uint32_t)(it >> 21), s34_log2);
+    uint32_t probe = 0;
+    while (s34[h] != ~0ull) { h = (h + 1) & (uint32_t)((1ull << s34_log2) - 1); probe++; }
+    s34[h] = it;
+    s34_max_probe = std::max(s34_max_probe, probe);
+  }
   // ---- decode table
   std::vector<uint32_t> tok_start((size_t)max_id + 1, 0);
   std::vector<int32_t> tok_len((size_t)max_id + 1, -1);
@@ -248,6 +269,7 @@ extern "C" int tk_load(const uint8_t* rank_bytes, const int64_t* rank_off, const
   rc = rc ? rc : upload(tok, byte_id, 256, &t.byte_id);
   rc = rc ? rc : upload(tok, dense.data(), dense.size(), &t.dense);
   rc = rc ? rc : upload(tok, slots.data(), slots.size(), &t.pair_slots);
+  rc = rc ? rc : upload(tok, s34.data(), s34.size(), &t.s34_slots);
   rc = rc ? rc : upload(tok, sbytes.data(), sbytes.size(), &t.spec_bytes);
   rc = rc ? rc : upload(tok, soff.data(), soff.size(), &t.spec_off);
   rc = rc ? rc : upload(tok, sid.data(), sid.size(), &t.spec_ids);
@@ -261,6 +283,8 @@ extern "C" int tk_load(const uint8_t* rank_bytes, const int64_t* rank_off, const
   t.pattern = pattern_id;
   t.pair_log2 = log2cap;
   t.pair_max_probe = max_probe;
+  t.s34_log2 = s34_log2;
+  t.s34_max_probe = s34_max_probe;
   t.n_spec = (int32_t)n_spec;
   t.max_id = max_id;
   tok->t = t;
