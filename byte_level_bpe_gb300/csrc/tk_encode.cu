@@ -1004,116 +1004,79 @@ __device__ __forceinline__ int merge_reg(const MergeTabs T, const uint8_t* b, in
   return m;
 }
 
-// Three bytes: the parts loop written out.  First round: ranks r01, r12 of the
-// two byte pairs; the leftmost minimum merges; then the one remaining pair,
-// whose bytes are the whole piece: its rank is the slice table's entry for
-// the three bytes, loaded beside the pair ranks (one round trip in all).
-struct Ids3 {
-  uint32_t n, a, b, c;
+// Pre-tokens of 1..4 bytes, one code path for every length.  Every pair of
+// adjacent parts spans a slice of the piece, so the loop only ever asks for
+// the ranks of the byte pairs (dense table), the triples and the whole piece
+// (slice table): loaded all at once (le4_load), then the loop written out by
+// cases on the cut each round removes (le4_finish; cuts 1, 2, 3 between the
+// bytes).  Positions past the piece's length take part in no slice, so they
+// stay parts of their own at the end and are dropped from the result.
+struct Le4 {
+  int n;
+  uint32_t w;               // the 4 bytes, little-endian
+  uint32_t r01, r12, r23;   // byte pairs
+  uint64_t sa, sb, sw;      // first probes of the slices 0-2, 1-3, 0-3 (~0: none)
 };
-__device__ __forceinline__ Ids3 merge3(const MergeTabs T, const uint8_t* b) {
-  const uint32_t b0 = b[0], b1 = b[1], b2 = b[2];
-  const uint32_t k = b0 | b1 << 8 | b2 << 16;
-  const uint64_t s = s34_first(T, k);
-  const uint32_t r01 = dense_rank(T, b0, b1), r12 = dense_rank(T, b1, b2);
-  const uint32_t i0 = __ldg(&T.byte_id[b0]), i1 = __ldg(&T.byte_id[b1]), i2 = __ldg(&T.byte_id[b2]);
-  const uint32_t r = s34_rank(T, s, k, false);
-  if (r01 == RANK_MAX && r12 == RANK_MAX) return Ids3{3u, i0, i1, i2};
-  const bool left = r01 <= r12;
-  if (r != RANK_MAX) return Ids3{1u, r, 0u, 0u};
-  return Ids3{2u, left ? r01 : i0, left ? i2 : r12, 0u};
+
+__device__ __forceinline__ Le4 le4_load(const MergeTabs& T, const uint8_t* b, int n) {
+  Le4 L;
+  L.n = n;
+  const uint32_t b0 = b[0], b1 = b[1], b2 = b[2], b3 = b[3];  // b has 4 readable bytes
+  L.w = b0 | b1 << 8 | b2 << 16 | b3 << 24;
+  L.sa = n > 2 ? s34_first(T, L.w & 0xFFFFFFu) : ~0ull;
+  L.sb = n > 3 ? s34_first(T, L.w >> 8) : ~0ull;
+  L.sw = n > 3 ? s34_first(T, L.w) : ~0ull;
+  L.r01 = n > 1 ? dense_rank(T, b0, b1) : RANK_MAX;
+  L.r12 = n > 2 ? dense_rank(T, b1, b2) : RANK_MAX;
+  L.r23 = n > 3 ? dense_rank(T, b2, b3) : RANK_MAX;
+  return L;
 }
 
-__device__ __forceinline__ void put3(int32_t* out, const Ids3& m) {
-  out[0] = (int32_t)m.a;
-  if (m.n > 1) out[1] = (int32_t)m.b;
-  if (m.n > 2) out[2] = (int32_t)m.c;
-}
-
-// Four bytes.  Every pair of adjacent parts spans a slice of the piece, so
-// the loop only ever asks for the ranks of the three byte pairs, the two
-// triples and the whole: six independent loads, then the loop written out
-// by cases on the cut each round removes (cuts 1, 2, 3 between the bytes).
-__device__ __forceinline__ int merge4(const MergeTabs T, const uint8_t* b, int32_t* out) {
-  const uint32_t b0 = b[0], b1 = b[1], b2 = b[2], b3 = b[3];
-  const uint32_t ka = b0 | b1 << 8 | b2 << 16, kb = b1 | b2 << 8 | b3 << 16, kw = ka | b3 << 24;
-  const uint64_t sa = s34_first(T, ka), sb = s34_first(T, kb), sw = s34_first(T, kw);
-  const uint32_t r01 = dense_rank(T, b0, b1), r12 = dense_rank(T, b1, b2), r23 = dense_rank(T, b2, b3);
-  const uint32_t i0 = __ldg(&T.byte_id[b0]), i1 = __ldg(&T.byte_id[b1]);
-  const uint32_t i2 = __ldg(&T.byte_id[b2]), i3 = __ldg(&T.byte_id[b3]);
-  const uint32_t r012 = s34_rank(T, sa, ka, false), r123 = s34_rank(T, sb, kb, false);
-  const uint32_t r0123 = s34_rank(T, sw, kw, true);
+// Writes the piece's ids to out[0 .. count) and returns count (single-byte
+// ids come from the 1 KB byte table here, after the slice loads).
+__device__ __forceinline__ int le4_finish(const MergeTabs& T, const Le4& L, int32_t* out) {
+  const uint32_t r012 = s34_rank(T, L.sa, L.w & 0xFFFFFFu, false), r123 = s34_rank(T, L.sb, L.w >> 8, false);
+  const uint32_t r0123 = s34_rank(T, L.sw, L.w, true);
+  const uint32_t r01 = L.r01, r12 = L.r12, r23 = L.r23;
+  const uint32_t i0 = __ldg(&T.byte_id[L.w & 255u]), i1 = __ldg(&T.byte_id[(L.w >> 8) & 255u]);
+  const uint32_t i2 = __ldg(&T.byte_id[(L.w >> 16) & 255u]), i3 = __ldg(&T.byte_id[L.w >> 24]);
+  uint32_t p0, p1 = 0, p2 = 0, p3 = 0;
+  int parts;
   if (r01 == RANK_MAX && r12 == RANK_MAX && r23 == RANK_MAX) {
-    out[0] = (int32_t)i0; out[1] = (int32_t)i1; out[2] = (int32_t)i2; out[3] = (int32_t)i3;
-    return 4;
-  }
-  // round 1 removes cut c1 (the leftmost least pair rank)
-  const int c1 = (r01 <= r12 && r01 <= r23) ? 1 : (r12 <= r23 ? 2 : 3);
-  // round 2: the pairs around the two remaining cuts
-  //   c1 = 1: [01][2][3]  left slice 012, right slice 23
-  //   c1 = 2: [0][12][3]  left slice 012, right slice 123
-  //   c1 = 3: [0][1][23]  left slice 01,  right slice 123
-  const uint32_t rl = c1 == 3 ? r01 : r012, rr = c1 == 1 ? r23 : r123;
-  if (rl == RANK_MAX && rr == RANK_MAX) {
-    out[0] = (int32_t)(c1 == 1 ? r01 : i0);
-    out[1] = (int32_t)(c1 == 1 ? i2 : (c1 == 2 ? r12 : i1));
-    out[2] = (int32_t)(c1 == 3 ? r23 : i3);
-    return 3;
-  }
-  // round 3: the two parts left span the whole piece
-  if (r0123 != RANK_MAX) {
-    out[0] = (int32_t)r0123;
-    return 1;
-  }
-  const bool left = rl <= rr;
-  //   left,  c1 != 3: [012][3];  left,  c1 == 3: [01][23]
-  //   right, c1 == 1: [01][23];  right, c1 != 1: [0][123]
-  const bool split22 = left ? c1 == 3 : c1 == 1;
-  out[0] = (int32_t)(split22 ? r01 : (left ? r012 : i0));
-  out[1] = (int32_t)(split22 ? r23 : (left ? i3 : r123));
-  return 2;
-}
-
-// One pre-token of 1..16 bytes: closed forms for one and two bytes (the
-// loop's result written out), else the register loop of the smallest width.
-__device__ __forceinline__ int merge_small(const MergeTabs T, const uint8_t* b, int n, int32_t* out) {
-  const uint32_t b0 = b[0];
-  if (n == 1) {
-    out[0] = (int32_t)__ldg(&T.byte_id[b0]);
-    return 1;
-  }
-  if (n == 2) {
-    const uint32_t b1 = b[1];
-    const uint32_t r = dense_rank(T, b0, b1);
-    if (r != RANK_MAX) {
-      out[0] = (int32_t)r;
-      return 1;
-    }
-    out[0] = (int32_t)__ldg(&T.byte_id[b0]);
-    out[1] = (int32_t)__ldg(&T.byte_id[b1]);
-    return 2;
-  }
-  if (n == 3) {
-    const Ids3 m = merge3(T, b);
-    put3(out, m);
-    return (int)m.n;
-  }
-  if (n == 4) return merge4(T, b, out);
-  if (n <= 8) return merge_reg<8>(T, b, n, out);
-  if constexpr (SHORT_MAX <= 12) {
-    return merge_reg<12>(T, b, n, out);
+    p0 = i0; p1 = i1; p2 = i2; p3 = i3;
+    parts = 4;
   } else {
-    if (n <= 12) return merge_reg<12>(T, b, n, out);
-    return merge_reg<16>(T, b, n, out);
+    // round 1 removes cut c1 (the leftmost least pair rank); round 2 sees
+    //   c1 = 1: [01][2][3]  left slice 012, right slice 23
+    //   c1 = 2: [0][12][3]  left slice 012, right slice 123
+    //   c1 = 3: [0][1][23]  left slice 01,  right slice 123
+    const int c1 = (r01 <= r12 && r01 <= r23) ? 1 : (r12 <= r23 ? 2 : 3);
+    const uint32_t rl = c1 == 3 ? r01 : r012, rr = c1 == 1 ? r23 : r123;
+    if (rl == RANK_MAX && rr == RANK_MAX) {
+      p0 = c1 == 1 ? r01 : i0;
+      p1 = c1 == 1 ? i2 : (c1 == 2 ? r12 : i1);
+      p2 = c1 == 3 ? r23 : i3;
+      parts = 3;
+    } else if (r0123 != RANK_MAX) {  // round 3: the two parts left span the piece
+      p0 = r0123;
+      parts = 1;
+    } else {
+      //   left,  c1 != 3: [012][3];  left,  c1 == 3: [01][23]
+      //   right, c1 == 1: [01][23];  right, c1 != 1: [0][123]
+      const bool left = rl <= rr;
+      const bool split22 = left ? c1 == 3 : c1 == 1;
+      p0 = split22 ? r01 : (left ? r012 : i0);
+      p1 = split22 ? r23 : (left ? i3 : r123);
+      parts = 2;
+    }
   }
+  const int m = parts - (4 - L.n);
+  out[0] = (int32_t)p0;
+  if (m > 1) out[1] = (int32_t)p1;
+  if (m > 2) out[2] = (int32_t)p2;
+  if (m > 3) out[3] = (int32_t)p3;
+  return m;
 }
-
-// Length class of a pre-token for the tile's work list (warps then run
-// pieces of one class together).
-constexpr int N_CLASSES = MID_MIN - 1;  // one class per length: a warp's lanes get
-                                     // pieces of one length (the same loop width
-                                     // and similar step counts)
-__device__ __forceinline__ int len_class(int n) { return n - 1; }
 
 // The group that runs one round merge: NW warps (NW = 1: one warp, no block
 // barriers; else the whole CTA).  s64 / s32 are shared scratch of NW entries.
@@ -1441,6 +1404,7 @@ __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t 
 // entries of the slot's table, in text order, for k_long_fixup.
 
 constexpr int ETHREADS = 256;
+constexpr int MERGE_U = 2;  // short pieces per thread per merge round
 constexpr int EPAD = 96;                 // bytes loaded past the tile (short pieces, specials)
 constexpr int MEDIUM_MAX = 1024;
 constexpr int64_t CLUSTER_MIN = 32768;   // longer pieces merge on a CTA cluster
@@ -1462,8 +1426,6 @@ struct EncSmem {
   uint32_t sb[TILE / 32];               // special starts
   uint32_t gb[TILE / 32];               // starts of pieces merged through global memory
   uint8_t cnt[TILE];                    // ids of the short piece starting at each byte
-  uint8_t plen[TILE];                   // length of the short piece starting at each byte
-  uint32_t cls_cnt[2 * N_CLASSES + 1];  // work list: class starts [0..N], then fill cursors
   int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
   union {
     uint16_t list[TILE + SHORT_MAX];    // work list: x | (len - 1) << 12 (until the merges end)
@@ -1472,10 +1434,7 @@ struct EncSmem {
   uint32_t th_full[ETHREADS];           // short ids before each thread's 16 bytes
   uint16_t th_gp[ETHREADS];             // table entries before each thread's 16 bytes
   uint32_t warp_tot[2 * ETHREADS / 32];
-  int64_t red64[ETHREADS / 32];
-  uint32_t red32[ETHREADS / 32];
   int n_gp;
-  uint32_t mnext;  // merge work-list cursor
   uint32_t n_starts;
   uint32_t tile_short;
   int64_t seg[2];
@@ -1506,7 +1465,7 @@ __device__ uint32_t ids_before(const EncSmem& sm, int x) {
   return r | (g << 16);
 }
 
-__global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
+__global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   EncSmem& sm = *reinterpret_cast<EncSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1536,9 +1495,7 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
       sm.sb[i] = c.T.n_spec ? c.W.sbits[(t0 >> 5) + i] : 0u;
       sm.gb[i] = 0;
     }
-    if (tid < 2 * N_CLASSES + 1) sm.cls_cnt[tid] = 0;
     if (tid == 0) {
-      sm.mnext = 0;
       sm.n_starts = 0;
       sm.seg[0] = c.W.tile_segs[4 * tile + 1];
       sm.seg[1] = (tile == ntiles - 1) ? c.S + 1 : c.W.tile_segs[4 * tile + 2];
@@ -1547,12 +1504,21 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
     // 2. each thread: its pre-tokens (starts in bytes [16 tid, 16 tid + 16))
     const int xb = tid * 16;
     const uint32_t my = (sm.pb[xb >> 5] >> (xb & 31)) & 0xFFFFu;
-    // 2a. ends and length classes of this thread's pre-tokens
+    // 2a. lengths (exact up to 32 bytes from the start bitmap, specials in
+    //     full): pieces of up to MID_MIN - 1 bytes are listed for the merge
+    //     below, longer ones flagged for the side stream's merges
+    uint32_t n_sh = 0;
     for (uint32_t bits = my; bits; bits &= bits - 1) {
       const int x = xb + __ffs(bits) - 1;
-      // end: the next start bit, else the first start of a later tile, else n
-      int64_t e = -1;
-      {
+      const int wi = x >> 5;  // pb has a word past the tile's last
+      const uint64_t nx = ((((uint64_t)sm.pb[wi + 1] << 32) | sm.pb[wi]) >> (x & 31)) >> 1;
+      int64_t len = nx ? __ffsll((long long)nx) : 64;  // 33 or more bytes: "long"
+      const int64_t rem = c.n - (t0 + x);               // the text end ends a piece
+      if (rem < len) len = rem;
+      if ((sm.sb[x >> 5] >> (x & 31)) & 1u) {
+        // a special: its exact end (the next start bit, else the first start
+        // of a later tile, else n)
+        int64_t e = -1;
         int y = x + 1;
         while (y < TILE + EPAD) {
           const uint32_t w = sm.pb[y >> 5] >> (y & 31);
@@ -1568,15 +1534,10 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
           }
           if (e < 0) e = c.n;
         }
-      }
-      const int64_t len = e - (t0 + x);
-      sm.plen[x] = 0;
-      if ((sm.sb[x >> 5] >> (x & 31)) & 1u) {
-        sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)len);
+        sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)(e - (t0 + x)));
         sm.cnt[x] = 1;
       } else if (len < MID_MIN) {
-        sm.plen[x] = (uint8_t)len;
-        atomicAdd(&sm.cls_cnt[len_class((int)len)], 1u);
+        n_sh++;
       } else {
         // merged on the side stream, which may still be running: the tile
         // records where the piece is; k_long_fixup adds its ids' count
@@ -1584,43 +1545,56 @@ __global__ void __launch_bounds__(ETHREADS) k_encode_tiles(Call c) {
         sm.cnt[x] = len <= SHORT_MAX;  // 1: a mid piece, its own source (no dedup)
       }
     }
-    __syncthreads();
-    if (tid == 0) {
-      // class k occupies list[cls_cnt[k] .. cls_cnt[k + 1]); cls_cnt[N_CLASSES] = length.
-      // The fill below advances cursor k from the start of class k to its end.
-      uint32_t run = 0;
-      for (int k = 0; k < N_CLASSES; k++) {
-        const uint32_t a = sm.cls_cnt[k];
-        sm.cls_cnt[k] = run;
-        sm.cls_cnt[N_CLASSES + 1 + k] = run;
-        run += a;
+    // the list of short pieces: x | (len - 1) << 12, in text order (a block
+    // scan of the per-thread counts)
+    uint32_t n_list;
+    {
+      uint32_t a = n_sh;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, a, o);
+        if (lane >= o) a += y;
       }
-      sm.cls_cnt[N_CLASSES] = run;
+      if (lane == 31) sm.warp_tot[ETHREADS / 32 + warp] = a;
+      __syncthreads();
+      uint32_t before = 0;
+      n_list = 0;
+#pragma unroll
+      for (int w = 0; w < ETHREADS / 32; w++) {
+        const uint32_t t = sm.warp_tot[ETHREADS / 32 + w];
+        before += w < warp ? t : 0u;
+        n_list += t;
+      }
+      uint32_t q = before + a - n_sh;
+      // the same lengths again (specials and longer pieces have their bits)
+      const uint32_t skip = ((sm.sb[xb >> 5] | sm.gb[xb >> 5]) >> (xb & 31)) & 0xFFFFu;
+      for (uint32_t bits = my & ~skip; bits; bits &= bits - 1) {
+        const int x = xb + __ffs(bits) - 1;
+        const int wi = x >> 5;
+        const uint64_t nx = ((((uint64_t)sm.pb[wi + 1] << 32) | sm.pb[wi]) >> (x & 31)) >> 1;
+        int len = nx ? __ffsll((long long)nx) : 64;
+        const int64_t rem = c.n - (t0 + x);
+        if (rem < len) len = (int)rem;
+        sm.list[q++] = (uint16_t)(x | ((len - 1) << 12));
+      }
     }
     __syncthreads();
-    uint16_t* list = sm.list;
-    for (uint32_t bits = my; bits; bits &= bits - 1) {
-      const int x = xb + __ffs(bits) - 1;
-      const int len = sm.plen[x];
-      if (len) list[atomicAdd(&sm.cls_cnt[N_CLASSES + 1 + len_class(len)], 1u)] = (uint16_t)(x | ((len - 1) << 12));
-    }
-    __syncthreads();
-    // 2b. the list, longest pieces first: each warp takes the next 32 entries
-    //     (one length, or two at a class boundary) until none is left, so no
-    //     warp holds the tile back with a late long piece.
+    // 2b. the short pieces, MERGE_U per thread per round with their loads
+    //     issued together (every length takes the same code path)
     {
       const MergeTabs MT(c.T);
-      const uint32_t total = sm.cls_cnt[N_CLASSES];
-      for (;;) {
-        uint32_t pos = 0;
-        if (lane == 0) pos = atomicAdd(&sm.mnext, 32u);
-        pos = __shfl_sync(0xffffffffu, pos, 0);
-        if (pos >= total) break;
-        if (pos + lane < total) {
-          const uint32_t ent = list[total - 1 - (pos + lane)];
-          const int x = ent & 0xFFF, len = (int)(ent >> 12) + 1;
-          sm.cnt[x] = (uint8_t)merge_small(MT, &sm.text[x], len, &sm.stage[x]);
+      for (uint32_t i = tid; i < n_list; i += MERGE_U * ETHREADS) {
+        Le4 L[MERGE_U];
+        int xs[MERGE_U];
+#pragma unroll
+        for (int u = 0; u < MERGE_U; u++) {
+          const uint32_t k = i + u * ETHREADS;
+          const uint32_t e = sm.list[k < n_list ? k : i];
+          xs[u] = k < n_list ? (int)(e & 0xFFF) : -1;
+          L[u] = le4_load(MT, &sm.text[e & 0xFFF], (int)(e >> 12) + 1);
         }
+#pragma unroll
+        for (int u = 0; u < MERGE_U; u++)
+          if (xs[u] >= 0) sm.cnt[xs[u]] = (uint8_t)le4_finish(MT, L[u], &sm.stage[xs[u]]);
       }
     }
     __syncthreads();
@@ -1769,11 +1743,12 @@ __global__ void __launch_bounds__(ETHREADS) k_long_fixup(Call c) {
 
 // Ordered output: each tile's staged ids go to out[tile_base + ...], with the
 // ids of its table's pieces inserted from the arena.  A tile without table
-// entries is one straight copy, 16 ids per thread in flight; with entries,
-// each output position finds the last entry that starts at or before it and
-// so its source: that entry's ids in the arena or the short ids after it.  A
-// table of the entry count at every 32nd output (one binary search each over
-// the entries' full_excl in shared memory) leaves each output a step or two.
+// entries is one straight copy, 16 ids per thread in flight.  With entries the
+// output is a sequence of parts (the short ids before entry 0, entry 0's ids,
+// the short ids after it, ...): a shared table holds each part's first output
+// and the address of its ids minus that start, a second one the part at
+// every 32nd output (one binary search each), so an output finds its part in
+// a step or two and reads its id from the staging slot or the arena.
 // Pieces of more than HUGE_IDS ids are listed for k_copy_huge, which spreads
 // them over the grid (their tiles take the per-part path below).
 constexpr uint32_t HUGE_IDS = 8192;
@@ -1781,23 +1756,27 @@ constexpr int COPY_UNROLL = 16;
 // output blocks of 32 ids per tile on the searched path: the tile's own ids
 // (at most TILE + 4) and one piece of up to HUGE_IDS ids that starts in it
 constexpr int COPY_BLK = (TILE + 2 * (int)HUGE_IDS) / 32 + 2;
+constexpr int COPY_E0 = 96;  // table entries read with the tile's count (most tiles have fewer)
 static_assert((STG * sizeof(uint32_t)) % 16 == 0, "staging slots stay 16-byte aligned");
 
-__global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int64_t cap) {
+__global__ void __launch_bounds__(ETHREADS, 5) k_copy_out(Call c, int32_t* out, int64_t cap) {
   __shared__ uint4 s_gp[MAX_GP];  // (short_excl, full_excl, src, cnt) in text order
-  __shared__ uint16_t s_blk[COPY_BLK];  // entries with full_excl <= 32 b
+  __shared__ uint32_t s_ps[2 * MAX_GP + 1];           // part starts in the tile's output
+  __shared__ unsigned long long s_pp[2 * MAX_GP + 1];  // part address - 4 * start
+  __shared__ uint16_t s_blk[COPY_BLK];                 // the part holding output 32 b
   __shared__ int s_huge;
-  static_assert(MAX_GP <= 1024, "the block search steps from 512");
+  static_assert(2 * MAX_GP + 1 <= 2048, "the block search steps from 1024");
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const int tid = threadIdx.x;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const uint32_t* slot = c.W.staging + tile * STG;
-    // the tile's count, base and first ETHREADS entries, loaded together
+    // the tile's count, base and first COPY_E0 entries, loaded together
     // (an entry past the table reads other words of the slot: unused)
     const uint64_t base = c.W.tile_base[tile];
     const uint32_t n_out = c.W.tile_base[tile + 1] - (uint32_t)base;
     const uint32_t meta = c.W.tile_meta[tile];
-    const uint4 e0 = *reinterpret_cast<const uint4*>(slot + STG - 4 * (tid + 1));
+    const uint4 e0 = tid < COPY_E0 ? *reinterpret_cast<const uint4*>(slot + STG - 4 * (tid + 1))
+                                   : make_uint4(0u, 0u, 0u, 0u);
     const uint32_t n_short = meta & 0xFFFFu;
     const int ngp = (int)(meta >> 16);
     if (ngp == 0) {
@@ -1820,20 +1799,42 @@ __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int
     if (tid == 0) s_huge = nblk > (uint32_t)COPY_BLK;
     __syncthreads();
     for (int g = tid; g < ngp; g += blockDim.x) {
-      const uint4 e = g == tid ? e0 : *reinterpret_cast<const uint4*>(slot + STG - 4 * (g + 1));
+      const uint4 e = g < COPY_E0 ? e0 : *reinterpret_cast<const uint4*>(slot + STG - 4 * (g + 1));
       s_gp[g] = e;
       if (e.w > HUGE_IDS) s_huge = 1;
     }
     __syncthreads();
     if (!s_huge) {
-      for (uint32_t b = tid; b < nblk; b += blockDim.x) {
-        int j = 0;
-#pragma unroll
-        for (int step = 512; step > 0; step >>= 1)
-          if (j + step <= ngp && s_gp[j + step - 1].y <= 32 * b) j += step;
-        s_blk[b] = (uint16_t)j;
+      const int np = 2 * ngp + 1;
+      for (int p = tid; p < np; p += blockDim.x) {
+        const int r = p >> 1;
+        uint32_t st;
+        const int32_t* src;
+        if (p & 1) {  // entry r
+          const uint4 e = s_gp[r];
+          st = e.y;
+          src = c.W.arena + e.z;
+        } else if (r == 0) {  // the short ids before entry 0
+          st = 0;
+          src = reinterpret_cast<const int32_t*>(slot);
+        } else {  // the short ids after entry r - 1
+          const uint4 e = s_gp[r - 1];
+          st = e.y + e.w;
+          src = reinterpret_cast<const int32_t*>(slot) + e.x;
+        }
+        s_ps[p] = st;
+        s_pp[p] = (unsigned long long)(uintptr_t)src - 4ull * st;
       }
       __syncthreads();
+      for (uint32_t b = tid; b < nblk; b += blockDim.x) {
+        int j = 0;  // parts that start at or before output 32 b (part 0 starts at 0)
+#pragma unroll
+        for (int step = 1024; step > 0; step >>= 1)
+          if (j + step <= np && s_ps[j + step - 1] <= 32 * b) j += step;
+        s_blk[b] = (uint16_t)(j - 1);
+      }
+      __syncthreads();
+      const bool fits = base + n_out <= (uint64_t)cap;
       for (uint32_t o0 = 0; o0 < n_out; o0 += COPY_UNROLL * ETHREADS) {
         int32_t v[COPY_UNROLL];
 #pragma unroll
@@ -1841,21 +1842,15 @@ __global__ void __launch_bounds__(ETHREADS) k_copy_out(Call c, int32_t* out, int
           const uint32_t o = o0 + k * ETHREADS + tid;
           v[k] = 0;
           if (o < n_out) {
-            int j = s_blk[o >> 5];  // entries with full_excl <= o
-            while (j < ngp && s_gp[j].y <= o) j++;
-            const int32_t* a = reinterpret_cast<const int32_t*>(slot) + o;
-            if (j > 0) {
-              const uint4 e = s_gp[j - 1];
-              const uint32_t r = o - e.y;
-              a = r < e.w ? c.W.arena + e.z + r : reinterpret_cast<const int32_t*>(slot) + (e.x + r - e.w);
-            }
-            v[k] = *a;
+            int p = s_blk[o >> 5];
+            while (p + 1 < np && s_ps[p + 1] <= o) p++;
+            v[k] = *reinterpret_cast<const int32_t*>((uintptr_t)(s_pp[p] + 4ull * o));
           }
         }
 #pragma unroll
         for (int k = 0; k < COPY_UNROLL; k++) {
           const uint32_t o = o0 + k * ETHREADS + tid;
-          if (o < n_out && base + o < (uint64_t)cap) out[base + o] = v[k];
+          if (o < n_out && (fits || base + o < (uint64_t)cap)) out[base + o] = v[k];
         }
       }
       __syncthreads();
@@ -2520,36 +2515,38 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
 }
 
 // Mid pieces (MID_MIN..SHORT_MAX bytes): one thread each over the whole
-// grid, the register loop of the width the warp's longest piece needs (the
-// front of mid_list: up to 8 bytes; the back: 12 or 16).  Ids to the arena at
-// the piece's start, the count beside them; each piece is its own source (the
-// tile kernel marks its table entry so).
+// grid, the register loop of the width the warp's longest piece needs: the
+// front of mid_list (up to 8 bytes, BACK = false) or its back (12 or 16), one
+// launch each so that the narrow loop runs at its own occupancy.  Ids to the
+// arena at the piece's start, the count beside them; each piece is its own
+// source (the tile kernel marks its table entry so).
+template <bool BACK>
 __global__ void __launch_bounds__(ETHREADS) k_merge_mid(Call c) {
   const MergeTabs MT(c.T);
   const int lane = threadIdx.x & 31;
-  const int64_t na = c.W.status->n_mid_a, nm = na + c.W.status->n_mid_b;
+  const int64_t nm = BACK ? c.W.status->n_mid_b : c.W.status->n_mid_a;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t b0 = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); b0 < nm; b0 += stride) {
     const int64_t i = b0 + lane;
-    const bool valid = i < nm, front = i < na;
+    const bool valid = i < nm;
     int len = 0;
     int64_t p = 0;
     if (valid) {
-      const int64_t k = front ? i : c.W.mid_cap - 1 - (i - na);
+      const int64_t k = BACK ? c.W.mid_cap - 1 - i : i;
       p = c.W.mid_list[2 * k];
       len = (int)c.W.mid_list[2 * k + 1];
     }
-    const int wmax = __reduce_max_sync(0xffffffffu, (valid && !front) ? len : 0);
+    const int wmax = BACK ? __reduce_max_sync(0xffffffffu, len) : 8;
     if (!valid) continue;
-    uint8_t b[16];
+    constexpr int NB = BACK ? 16 : 8;
+    uint8_t b[NB];
 #pragma unroll
-    for (int j = 0; j < 16; j++) b[j] = j < len ? gbyte(c, p + j) : 0;
+    for (int j = 0; j < NB; j++) b[j] = j < len ? gbyte(c, p + j) : 0;
     const int64_t G = c.gb + p;
     int32_t* dst = c.W.arena + G;
     int m;
-    if (front) m = merge_reg<8>(MT, b, len, dst);
-    else if (wmax <= 12) m = merge_reg<12>(MT, b, len, dst);
-    else m = merge_reg<16>(MT, b, len, dst);
+    if constexpr (!BACK) m = merge_reg<8>(MT, b, len, dst);
+    else m = wmax <= 12 ? merge_reg<12>(MT, b, len, dst) : merge_reg<16>(MT, b, len, dst);
     c.W.cnt[G] = (uint32_t)m;
   }
 }
@@ -2782,7 +2779,9 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     tk_prof_mark(ws, "k_merge_medium", side);
     k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_mid", side);
-    k_merge_mid<<<sms * 8, ETHREADS, 0, side>>>(c);
+    k_merge_mid<false><<<sms * 8, ETHREADS, 0, side>>>(c);
+    tk_prof_mark(ws, "k_merge_mid_long", side);
+    k_merge_mid<true><<<sms * 4, ETHREADS, 0, side>>>(c);
     if (c.W.use_cache) {
       tk_prof_mark(ws, "k_cache_insert", side);
       k_cache_insert<<<sms * 8, ETHREADS, 0, side>>>(c);

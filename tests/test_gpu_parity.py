@@ -374,3 +374,40 @@ def test_r50k_digit_clause(full_table):
     _compare(gpu, enc, long_segs, False)
     _compare(gpu, enc, long_segs, True)
     gpu.close()
+
+
+def test_tile_tables_dense_and_ragged(full_gpu, full_enc):
+    """Pieces of 5..16 bytes (merged over the whole grid) and of 1..4 bytes
+    (merged in the tile kernel) at every offset around tile ends and the text
+    end; a tile packed with 5-byte pieces (the most table entries a tile can
+    hold); segment starts inside such tiles, empty ones included; specials
+    next to mid pieces; a piece of over 8192 ids in a tile whose other
+    pieces are mid pieces (the per-part copy path)."""
+    rng = np.random.default_rng(31)
+    letters = list("etaoinshrdlucmfwypvbgkqjxz")
+    segs = []
+    # every length 1..18 ending at every offset around the first tile end
+    for L in range(1, 19):
+        for shift in range(-3, 4):
+            pre = 4096 - L + shift
+            filler = (" ab" * ((pre // 3) + 1))[:pre]
+            w = "".join(rng.choice(letters, L - 1))
+            segs.append((filler + " " + w + " x", False))
+            segs.append((filler + " " + w, False))  # ends at the text end
+    # dense: " abcd" is a 5-byte piece, 819 of them per tile
+    dense = " abcd" * 2500
+    segs.append((dense, False))
+    cuts = sorted(int(c) for c in rng.integers(0, len(dense), size=40))
+    prev = 0
+    for c in cuts + [len(dense)]:
+        segs.append((dense[prev:c], False))
+        segs.append(("", False))
+        prev = c
+    # specials (13 and 15 bytes) between mid pieces
+    sp = list(workloads.SPECIALS)
+    segs.append(((" hello" + sp[0] + " worldly" + sp[-1] + " abcdefghij") * 50, True))
+    # over 8192 ids in one piece, after mid pieces in the same tile
+    big = "".join(rng.choice(letters, 30000))
+    segs.append((" mixture parsing tokens" * 20 + " " + big + " tail", False))
+    _compare(full_gpu, full_enc, segs, False)
+    _compare(full_gpu, full_enc, segs, True)
