@@ -1743,173 +1743,111 @@ __global__ void __launch_bounds__(ETHREADS) k_long_fixup(Call c) {
 
 // Ordered output: each tile's staged ids go to out[tile_base + ...], with the
 // ids of its table's pieces inserted from the arena.  A tile without table
-// entries is one straight copy, 16 ids per thread in flight.  With entries the
-// output is a sequence of parts (the short ids before entry 0, entry 0's ids,
-// the short ids after it, ...): a shared table holds each part's first output
-// and the address of its ids minus that start, a second one the part at
-// every 32nd output (one binary search each), so an output finds its part in
-// a step or two and reads its id from the staging slot or the arena.
-// Pieces of more than HUGE_IDS ids are listed for k_copy_huge, which spreads
-// them over the grid (their tiles take the per-part path below).
+// entries is one straight copy, COPY_UNROLL ids per thread in flight.  With
+// entries the output is a sequence of parts (the short ids before entry 0,
+// entry 0's ids, the short ids after it, ...): a shared table holds each
+// part's first output and the address of its ids minus that start, a second
+// one the part at every 32nd output (one binary search each), so an output
+// finds its part in a step or two and reads its id from the staging slot or
+// the arena.  Only a tile's last piece can reach past the tile, so a tile
+// holds at most one piece of more than HUGE_IDS ids: it is listed for
+// k_copy_huge, which spreads it over the grid, and takes no width here (the
+// outputs after it shift by its count).  Small CTAs keep many tiles in flight.
 constexpr uint32_t HUGE_IDS = 8192;
-constexpr int COPY_UNROLL = 16;
-// output blocks of 32 ids per tile on the searched path: the tile's own ids
-// (at most TILE + 4) and one piece of up to HUGE_IDS ids that starts in it
-constexpr int COPY_BLK = (TILE + 2 * (int)HUGE_IDS) / 32 + 2;
-constexpr int COPY_E0 = 96;  // table entries read with the tile's count (most tiles have fewer)
+constexpr int COPY_THREADS = 128;
+constexpr int COPY_UNROLL = 24;
+// output blocks of 32 ids per tile without its huge piece: the pieces
+// inside the tile (at most TILE + 4 ids) and a last one of up to HUGE_IDS
+constexpr int COPY_BLK = (TILE + 4 + (int)HUGE_IDS + 31) / 32 + 1;
 static_assert((STG * sizeof(uint32_t)) % 16 == 0, "staging slots stay 16-byte aligned");
 
-__global__ void __launch_bounds__(ETHREADS, 5) k_copy_out(Call c, int32_t* out, int64_t cap) {
-  __shared__ uint4 s_gp[MAX_GP];  // (short_excl, full_excl, src, cnt) in text order
+__global__ void __launch_bounds__(COPY_THREADS, 10) k_copy_out(Call c, int32_t* out, int64_t cap) {
   __shared__ uint32_t s_ps[2 * MAX_GP + 1];           // part starts in the tile's output
   __shared__ unsigned long long s_pp[2 * MAX_GP + 1];  // part address - 4 * start
   __shared__ uint16_t s_blk[COPY_BLK];                 // the part holding output 32 b
-  __shared__ int s_huge;
+  __shared__ uint32_t s_h[2];                          // the huge piece's start and count
   static_assert(2 * MAX_GP + 1 <= 2048, "the block search steps from 1024");
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
   const int tid = threadIdx.x;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const uint32_t* slot = c.W.staging + tile * STG;
-    // the tile's count, base and first COPY_E0 entries, loaded together
-    // (an entry past the table reads other words of the slot: unused)
     const uint64_t base = c.W.tile_base[tile];
     const uint32_t n_out = c.W.tile_base[tile + 1] - (uint32_t)base;
     const uint32_t meta = c.W.tile_meta[tile];
-    const uint4 e0 = tid < COPY_E0 ? *reinterpret_cast<const uint4*>(slot + STG - 4 * (tid + 1))
-                                   : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t n_short = meta & 0xFFFFu;
     const int ngp = (int)(meta >> 16);
     if (ngp == 0) {
-      for (uint32_t q0 = 0; q0 < n_short; q0 += COPY_UNROLL * ETHREADS) {
+      for (uint32_t q0 = 0; q0 < n_out; q0 += COPY_UNROLL * COPY_THREADS) {
         uint32_t v[COPY_UNROLL];
 #pragma unroll
         for (int k = 0; k < COPY_UNROLL; k++) {
-          const uint32_t q = q0 + k * ETHREADS + tid;
-          v[k] = q < n_short ? __ldcs(slot + q) : 0u;
+          const uint32_t q = q0 + k * COPY_THREADS + tid;
+          v[k] = q < n_out ? __ldcs(slot + q) : 0u;
         }
 #pragma unroll
         for (int k = 0; k < COPY_UNROLL; k++) {
-          const uint32_t q = q0 + k * ETHREADS + tid;
-          if (q < n_short && base + q < (uint64_t)cap) out[base + q] = (int32_t)v[k];
+          const uint32_t q = q0 + k * COPY_THREADS + tid;
+          if (q < n_out && base + q < (uint64_t)cap) out[base + q] = (int32_t)v[k];
         }
       }
       continue;
     }
-    const uint32_t nblk = (n_out + 31) >> 5;
-    if (tid == 0) s_huge = nblk > (uint32_t)COPY_BLK;
-    __syncthreads();
-    for (int g = tid; g < ngp; g += blockDim.x) {
-      const uint4 e = g < COPY_E0 ? e0 : *reinterpret_cast<const uint4*>(slot + STG - 4 * (g + 1));
-      s_gp[g] = e;
-      if (e.w > HUGE_IDS) s_huge = 1;
-    }
-    __syncthreads();
-    if (!s_huge) {
-      const int np = 2 * ngp + 1;
-      for (int p = tid; p < np; p += blockDim.x) {
-        const int r = p >> 1;
-        uint32_t st;
-        const int32_t* src;
-        if (p & 1) {  // entry r
-          const uint4 e = s_gp[r];
-          st = e.y;
-          src = c.W.arena + e.z;
-        } else if (r == 0) {  // the short ids before entry 0
-          st = 0;
-          src = reinterpret_cast<const int32_t*>(slot);
-        } else {  // the short ids after entry r - 1
-          const uint4 e = s_gp[r - 1];
-          st = e.y + e.w;
-          src = reinterpret_cast<const int32_t*>(slot) + e.x;
-        }
-        s_ps[p] = st;
-        s_pp[p] = (unsigned long long)(uintptr_t)src - 4ull * st;
-      }
-      __syncthreads();
-      for (uint32_t b = tid; b < nblk; b += blockDim.x) {
-        int j = 0;  // parts that start at or before output 32 b (part 0 starts at 0)
-#pragma unroll
-        for (int step = 1024; step > 0; step >>= 1)
-          if (j + step <= np && s_ps[j + step - 1] <= 32 * b) j += step;
-        s_blk[b] = (uint16_t)(j - 1);
-      }
-      __syncthreads();
-      const bool fits = base + n_out <= (uint64_t)cap;
-      for (uint32_t o0 = 0; o0 < n_out; o0 += COPY_UNROLL * ETHREADS) {
-        int32_t v[COPY_UNROLL];
-#pragma unroll
-        for (int k = 0; k < COPY_UNROLL; k++) {
-          const uint32_t o = o0 + k * ETHREADS + tid;
-          v[k] = 0;
-          if (o < n_out) {
-            int p = s_blk[o >> 5];
-            while (p + 1 < np && s_ps[p + 1] <= o) p++;
-            v[k] = *reinterpret_cast<const int32_t*>((uintptr_t)(s_pp[p] + 4ull * o));
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < COPY_UNROLL; k++) {
-          const uint32_t o = o0 + k * ETHREADS + tid;
-          if (o < n_out && (fits || base + o < (uint64_t)cap)) out[base + o] = v[k];
-        }
-      }
-      __syncthreads();
-      continue;
-    }
-    // short id q follows the entries whose short_excl <= q: the last such
-    // entry j gives its shift, full_excl + cnt - short_excl
-    for (uint32_t q0 = 0; q0 < n_short; q0 += COPY_UNROLL * ETHREADS) {
-      uint32_t v[COPY_UNROLL];
-#pragma unroll
-      for (int k = 0; k < COPY_UNROLL; k++) {
-        const uint32_t q = q0 + k * ETHREADS + tid;
-        v[k] = q < n_short ? __ldcs(slot + q) : 0u;
-      }
-#pragma unroll
-      for (int k = 0; k < COPY_UNROLL; k++) {
-        const uint32_t q = q0 + k * ETHREADS + tid;
-        if (q >= n_short) continue;
-        int lo = 0, hi = ngp;  // entries [0, lo) have short_excl <= q
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (s_gp[mid].x <= q) lo = mid + 1;
-          else hi = mid;
-        }
-        uint64_t pos = base + q;
-        if (lo > 0) {
-          const uint4 e = s_gp[lo - 1];
-          pos += e.y + e.w - e.x;
-        }
-        if (pos < (uint64_t)cap) out[pos] = (int32_t)v[k];
-      }
-    }
-    // the entries' ids: up to 32 by one thread each, longer ones by a warp
-    // each, over HUGE_IDS listed for k_copy_huge
-    for (int g = tid; g < ngp; g += blockDim.x) {
-      const uint4 e = s_gp[g];
-      if (e.w > 32) continue;
-      const int32_t* src = c.W.arena + e.z;
-      const uint64_t o = base + e.y;
-      for (uint32_t j = 0; j < e.w; j++)
-        if (o + j < (uint64_t)cap) out[o + j] = src[j];
-    }
-    const int lane = tid & 31;
-    for (int g = tid >> 5; g < ngp; g += blockDim.x >> 5) {
-      const uint4 e = s_gp[g];
-      if (e.w <= 32) continue;
-      const uint64_t o = base + e.y;
-      if (e.w > HUGE_IDS) {
-        if (lane == 0) {
+    // parts: 0 = the short ids before entry 0; 2g + 1 = entry g; 2g + 2 =
+    // the short ids after entry g
+    const int np = 2 * ngp + 1;
+    for (int g = tid; g < ngp; g += COPY_THREADS) {
+      const uint4 e = *reinterpret_cast<const uint4*>(slot + STG - 4 * (g + 1));
+      const bool huge = e.w > HUGE_IDS;
+      const uint32_t rs = huge ? e.y : e.y + e.w;  // where the short ids after it start
+      s_ps[2 * g + 1] = e.y;
+      s_pp[2 * g + 1] = (unsigned long long)(uintptr_t)(c.W.arena + e.z) - 4ull * e.y;
+      s_ps[2 * g + 2] = rs;
+      s_pp[2 * g + 2] = (unsigned long long)(uintptr_t)(slot + e.x) - 4ull * rs;
+      if (g == ngp - 1) {
+        s_h[0] = e.y;
+        s_h[1] = huge ? e.w : 0u;
+        if (huge) {
           const uint32_t k = atomicAdd(&c.W.status->n_huge, 1u);
-          c.W.huge_list[3 * (uint64_t)k] = o;
+          c.W.huge_list[3 * (uint64_t)k] = base + e.y;
           c.W.huge_list[3 * (uint64_t)k + 1] = e.z;
           c.W.huge_list[3 * (uint64_t)k + 2] = e.w;
         }
-        continue;
       }
-      const int32_t* src = c.W.arena + e.z;
-      for (uint32_t j = lane; j < e.w; j += 32)
-        if (o + j < (uint64_t)cap) out[o + j] = src[j];
+    }
+    if (tid == 0) {
+      s_ps[0] = 0;
+      s_pp[0] = (unsigned long long)(uintptr_t)slot;
+    }
+    __syncthreads();
+    const uint32_t hst = s_h[0], hcnt = s_h[1];
+    const uint32_t n_cmp = n_out - hcnt;  // outputs copied here
+    const uint32_t nblk = (n_cmp + 31) >> 5;
+    for (uint32_t b = tid; b < nblk; b += COPY_THREADS) {
+      int j = 0;  // parts that start at or before output 32 b (part 0 starts at 0)
+#pragma unroll
+      for (int step = 1024; step > 0; step >>= 1)
+        if (j + step <= np && s_ps[j + step - 1] <= 32 * b) j += step;
+      s_blk[b] = (uint16_t)(j - 1);
+    }
+    __syncthreads();
+    const bool fits = base + n_out <= (uint64_t)cap;
+    for (uint32_t o0 = 0; o0 < n_cmp; o0 += COPY_UNROLL * COPY_THREADS) {
+      int32_t v[COPY_UNROLL];
+#pragma unroll
+      for (int k = 0; k < COPY_UNROLL; k++) {
+        const uint32_t o = o0 + k * COPY_THREADS + tid;
+        v[k] = 0;
+        if (o < n_cmp) {
+          int p = s_blk[o >> 5];
+          while (p + 1 < np && s_ps[p + 1] <= o) p++;
+          v[k] = *reinterpret_cast<const int32_t*>((uintptr_t)(s_pp[p] + 4ull * o));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < COPY_UNROLL; k++) {
+        const uint32_t o = o0 + k * COPY_THREADS + tid;
+        const uint64_t pos = base + o + (o >= hst ? hcnt : 0u);
+        if (o < n_cmp && (fits || pos < (uint64_t)cap)) out[pos] = v[k];
+      }
     }
     __syncthreads();
   }
@@ -2801,9 +2739,9 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     if (rc) return rc;
     tk_prof_mark(ws, "k_copy_out", st);
     int copy_per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&copy_per_sm, k_copy_out, ETHREADS, 0);
-    k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(copy_per_sm, 1)), ETHREADS, 0, st>>>(
-        c, d_out, cap);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&copy_per_sm, k_copy_out, COPY_THREADS, 0);
+    k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(copy_per_sm, 1)), COPY_THREADS, 0,
+                 st>>>(c, d_out, cap);
     tk_prof_mark(ws, "k_copy_huge", st);
     k_copy_huge<<<sms * 4, ETHREADS, 0, st>>>(c, d_out, cap);
     tk_prof_mark(ws, "k_seg_offsets", st);
