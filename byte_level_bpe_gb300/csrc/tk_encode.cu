@@ -1154,17 +1154,18 @@ __device__ __forceinline__ int64_t cl_ld64(uint32_t a) {
   return v;
 }
 
-// The round-merge group of a whole cluster of CL 1024-thread CTAs (one piece
+// The round-merge group of a whole cluster of CL CTAs of CW warps (one piece
 // spread over CL SMs).  Reductions go through each CTA's shared memory and
 // distributed shared memory; the merge buffers are read through L2 (.cg),
 // since the CTAs sit on different SMs.  s64 / s32: 33 entries per CTA.
-template <int CL>
+template <int CL, int CW>
 struct CGroup {
-  static constexpr int kWarps = CL * 32;
+  static_assert(CW >= 1 && CW <= 32, "warps per CTA");
+  static constexpr int kWarps = CL * CW;
   int64_t* s64;
   uint32_t* s32;
   uint32_t rank;
-  __device__ int warp() const { return (int)(rank * 32 + (threadIdx.x >> 5)); }
+  __device__ int warp() const { return (int)(rank * CW + (threadIdx.x >> 5)); }
   __device__ void sync() const { cl_sync(); }
   template <class T>
   __device__ T ld(const T* p) const { return __ldcg(p); }
@@ -1173,7 +1174,7 @@ struct CGroup {
     if ((threadIdx.x & 31) == 0) s32[threadIdx.x >> 5] = v;
     __syncthreads();
     if (threadIdx.x < 32) {
-      uint32_t u = s32[threadIdx.x];
+      uint32_t u = threadIdx.x < CW ? s32[threadIdx.x] : 0xFFFFFFFFu;
       for (int o = 16; o > 0; o >>= 1) u = min(u, __shfl_xor_sync(0xffffffffu, u, o));
       if (threadIdx.x == 0) s32[32] = u;
     }
@@ -1190,7 +1191,7 @@ struct CGroup {
     __syncthreads();
     if (threadIdx.x == 0) {
       int64_t t = idv;
-      for (int k = 0; k < 32; k++) t = op ? max(t, s64[k]) : t + s64[k];
+      for (int k = 0; k < CW; k++) t = op ? max(t, s64[k]) : t + s64[k];
       s64[32] = t;
     }
     cl_sync();
@@ -2403,10 +2404,11 @@ __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
   }
 }
 
-// k_merge_cluster: one cluster of MERGE_CL 1024-thread CTAs per piece over
-// CLUSTER_MIN bytes; rank 0 takes the next piece and shares it through
+// k_merge_cluster: one cluster of MERGE_CL CL_THREADS-thread CTAs per piece
+// over CLUSTER_MIN bytes; rank 0 takes the next piece and shares it through
 // distributed shared memory.
-__global__ void __cluster_dims__(MERGE_CL, 1, 1) __launch_bounds__(BIG_THREADS, 1) k_merge_cluster(Call c) {
+constexpr int CL_THREADS = 1024;
+__global__ void __cluster_dims__(MERGE_CL, 1, 1) __launch_bounds__(CL_THREADS, 1024 / CL_THREADS) k_merge_cluster(Call c) {
   __shared__ int64_t s64[33];
   __shared__ uint32_t s32[33];
   __shared__ uint32_t s_idx;
@@ -2420,7 +2422,7 @@ __global__ void __cluster_dims__(MERGE_CL, 1, 1) __launch_bounds__(BIG_THREADS, 
     if (k >= n_cl) break;
     const int64_t p = c.W.cl_list[2 * k], len = c.W.cl_list[2 * k + 1];
     if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
-    const int64_t m = merge_rounds(c, CGroup<MERGE_CL>{s64, s32, rank}, p, len);
+    const int64_t m = merge_rounds(c, CGroup<MERGE_CL, CL_THREADS / 32>{s64, s32, rank}, p, len);
     if (rank == 0 && threadIdx.x == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
   }
 }
@@ -2713,7 +2715,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     tk_prof_mark(ws, "k_merge_big", side);
     k_merge_big<<<sms, BIG_THREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_cluster", side);
-    k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), BIG_THREADS, 0, side>>>(c);
+    k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), CL_THREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_medium", side);
     k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_mid", side);
