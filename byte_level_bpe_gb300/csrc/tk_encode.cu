@@ -244,6 +244,12 @@ struct SegCountOp {
 
 __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int safe,
                         int64_t n_cut_words, int64_t n_tiles, int clear_dtab) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (1ll << W.mtab_log2);
+       i += (int64_t)gridDim.x * blockDim.x)
+  {  // every word: a waiter must never see an owner left by an earlier call
+    reinterpret_cast<uint4*>(W.mtab)[2 * i] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(W.mtab)[2 * i + 1] = make_uint4(0u, 0u, 0u, 0u);
+  }
   const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (tid == 0) {
@@ -1543,7 +1549,7 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
         // merged on the side stream, which may still be running: the tile
         // records where the piece is; k_long_fixup adds its ids' count
         atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
-        sm.cnt[x] = len <= SHORT_MAX;  // 1: a mid piece, its own source (no dedup)
+        sm.cnt[x] = 0;
       }
     }
     // the list of short pieces: x | (len - 1) << 12, in text order (a block
@@ -1643,7 +1649,7 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
       for (uint32_t bits = my; bits; bits &= bits - 1) {
         const int x = xb + __ffs(bits) - 1;
         if ((my_g >> (x - xb)) & 1u) {
-          *reinterpret_cast<uint4*>(slot + STG - 4 * (g + 1)) = make_uint4(s, (uint32_t)x, sm.cnt[x], 0u);
+          *reinterpret_cast<uint4*>(slot + STG - 4 * (g + 1)) = make_uint4(s, (uint32_t)x, 0u, 0u);
           g++;
           continue;
         }
@@ -1689,7 +1695,7 @@ __global__ void __launch_bounds__(ETHREADS) k_long_fixup(Call c) {
     uint32_t* slot = c.W.staging + tile * STG;
     uint32_t carry = 0;  // the table's ids before this group of entries
     // FIX_BATCH entries per lane per pass, their loads issued together (the
-    // entry, then for a long piece its source, then the count)
+    // entry, then its source, then the count)
     for (int g0 = 0; g0 < ngp; g0 += 32 * FIX_BATCH) {
       uint4 e[FIX_BATCH];
 #pragma unroll
@@ -1700,9 +1706,7 @@ __global__ void __launch_bounds__(ETHREADS) k_long_fixup(Call c) {
 #pragma unroll
       for (int u = 0; u < FIX_BATCH; u++) {
         const int g = g0 + 32 * u + lane;
-        const uint32_t G = (uint32_t)(c.gb + t0 + e[u].y);
-        // z = 1: a mid piece (its own source); else the owner from gsrc
-        if (g < ngp) e[u].z = e[u].z ? G : (c.W.gsrc[G] & ~GSRC_CACHED);
+        if (g < ngp) e[u].z = c.W.gsrc[c.gb + t0 + e[u].y] & ~GSRC_CACHED;
       }
 #pragma unroll
       for (int u = 0; u < FIX_BATCH; u++) {
@@ -2454,17 +2458,102 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
   }
 }
 
-// Mid pieces (MID_MIN..SHORT_MAX bytes): one thread each over the whole
-// grid, the register loop of the width the warp's longest piece needs: the
-// front of mid_list (up to 8 bytes, BACK = false) or its back (12 or 16), one
-// launch each so that the narrow loop runs at its own occupancy.  Ids to the
-// arena at the piece's start, the count beside them; each piece is its own
-// source (the tile kernel marks its table entry so).
+// Word cache of the mid pieces (MID_MIN..SHORT_MAX bytes): a repeated word
+// is merged once.  The key is the piece's bytes themselves (two words,
+// zero-padded), so equal keys of equal length are equal pieces and no byte
+// comparison is needed.  Slot: key0 + 1 (0 = empty; claimed by CAS), key1,
+// then (owner G + 1) | len << 32 published with release.  Each word is
+// written once per call (k_reset clears them in an earlier kernel), so a
+// plain load, which may hit a stale L1 line, returns either 0 or the final
+// value: frequent words are then found in L1 without an atomic, and only a
+// slot that reads empty is claimed by CAS (a hot word's slot would otherwise
+// serialise hundreds of thousands of atomics).  Returns the start of the
+// piece whose ids p uses (G itself for the first occurrence, or when the
+// table is full or a wait gives up).
+__device__ int64_t mid_claim(const Call& c, uint64_t k0, uint64_t k1, int len, int64_t G) {
+  const uint64_t key = k0 + 1;  // 0 only for 8 bytes of 0xFF: not cached
+  if (key == 0) return G;
+  const uint64_t mask = (1ull << c.W.mtab_log2) - 1;
+  uint64_t slot = mix64(k0 ^ mix64(k1 ^ (uint64_t)len)) & mask;
+  for (int probe = 0; probe < 32; probe++, slot = (slot + 1) & mask) {
+    unsigned long long* e = c.W.mtab + 4 * slot;
+    unsigned long long cur = e[0];
+    if (cur == 0) {
+      cur = atomicCAS(&e[0], 0ull, (unsigned long long)key);
+      if (cur == 0) {
+        e[1] = k1;
+        st_release_u64(reinterpret_cast<uint64_t*>(&e[2]), (uint64_t)(G + 1) | ((uint64_t)len << 32));
+        return G;
+      }
+    }
+    if (cur != key) continue;
+    uint64_t v = e[2];
+    for (uint32_t spins = 0; v == 0 && spins < SPIN_LIMIT; spins++) {
+      v = ld_acquire_u64(reinterpret_cast<const uint64_t*>(&e[2]));
+      if (!v) __nanosleep(32);
+    }
+    if (!v) return G;
+    if ((int)(v >> 32) != len) continue;
+    const int64_t owner = (int64_t)(v & 0xFFFFFFFFu) - 1;
+    if (len <= 8) return owner;  // key0 holds every byte
+    // key1: a plain load is 0 or final; 0 (or a mismatch) is confirmed coherently
+    uint64_t w1 = e[1];
+    if (w1 != k1 || k1 == 0) w1 = ld_acquire_u64(reinterpret_cast<const uint64_t*>(&e[1]));
+    if (w1 == k1) return owner;
+  }
+  return G;
+}
+
+// One thread per listed mid piece: its source (gsrc) from the word cache;
+// the first occurrences go to mid_own (front or back like mid_list, one
+// atomic per warp).
+template <bool BACK>
+__global__ void __launch_bounds__(ETHREADS) k_dedup_mid(Call c) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nm = BACK ? c.W.status->n_mid_b : c.W.status->n_mid_a;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b0 = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); b0 < nm; b0 += stride) {
+    const int64_t i = b0 + lane;
+    bool own = false;
+    uint32_t p = 0, len = 0;
+    if (i < nm) {
+      const int64_t k = BACK ? c.W.mid_cap - 1 - i : i;
+      p = c.W.mid_list[2 * k];
+      len = c.W.mid_list[2 * k + 1];
+      uint64_t k0 = 0, k1 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        k0 |= (uint64_t)((uint32_t)j < len ? gbyte(c, (int64_t)p + j) : 0) << (8 * j);
+        if (BACK) k1 |= (uint64_t)((uint32_t)(j + 8) < len ? gbyte(c, (int64_t)p + j + 8) : 0) << (8 * j);
+      }
+      const int64_t G = c.gb + p;
+      const int64_t src = mid_claim(c, k0, k1, (int)len, G);
+      c.W.gsrc[G] = (uint32_t)src;
+      own = src == G;
+    }
+    const uint32_t om = __ballot_sync(0xffffffffu, own);
+    uint32_t base = 0;
+    if (lane == 0 && om) base = atomicAdd(BACK ? &c.W.status->n_own_b : &c.W.status->n_own_a, (uint32_t)__popc(om));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (own) {
+      const int64_t r = base + __popc(om & ((1u << lane) - 1u));
+      const int64_t k = BACK ? c.W.mid_cap - 1 - r : r;
+      c.W.mid_own[2 * k] = p;
+      c.W.mid_own[2 * k + 1] = len;
+    }
+  }
+}
+
+// The distinct mid pieces: one thread each over the whole grid, the register
+// loop of the width the warp's longest piece needs (the front of mid_own: up
+// to 8 bytes, BACK = false; its back: 12 or 16), one launch each so that the
+// narrow loop runs at its own occupancy.  Ids to the arena at the piece's
+// start, the count beside them.
 template <bool BACK>
 __global__ void __launch_bounds__(ETHREADS) k_merge_mid(Call c) {
   const MergeTabs MT(c.T);
   const int lane = threadIdx.x & 31;
-  const int64_t nm = BACK ? c.W.status->n_mid_b : c.W.status->n_mid_a;
+  const int64_t nm = BACK ? c.W.status->n_own_b : c.W.status->n_own_a;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t b0 = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); b0 < nm; b0 += stride) {
     const int64_t i = b0 + lane;
@@ -2473,8 +2562,8 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_mid(Call c) {
     int64_t p = 0;
     if (valid) {
       const int64_t k = BACK ? c.W.mid_cap - 1 - i : i;
-      p = c.W.mid_list[2 * k];
-      len = (int)c.W.mid_list[2 * k + 1];
+      p = c.W.mid_own[2 * k];
+      len = (int)c.W.mid_own[2 * k + 1];
     }
     const int wmax = BACK ? __reduce_max_sync(0xffffffffu, len) : 8;
     if (!valid) continue;
@@ -2517,6 +2606,14 @@ static int cuda_fail(cudaError_t e, const char* what) {
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
 
+// Slots of the mid-piece word cache for a call of n bytes: one per 64 bytes
+// (the serving batch repeats most words), at least 2^10, at most 2^22.
+static uint32_t mtab_log2_for(int64_t n) {
+  uint32_t l = 10;
+  while (l < 22 && (1ll << l) < n / 64) l++;
+  return l;
+}
+
 extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, int64_t max_segments,
                                    tk_workspace** out) {
   if (!tok || !out || max_bytes < 0 || max_segments < 0) {
@@ -2546,6 +2643,8 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
   w.max_segments = max_segments;
   w.dtab_log2 = DTAB_LOG2;
   w.mid_cap = nb / MID_MIN + 2;
+  w.mtab_log2_max = mtab_log2_for(nb);
+  w.mtab_log2 = w.mtab_log2_max;
   struct Req { void** p; size_t bytes; };
   Req reqs[] = {
       {(void**)&w.status, sizeof(Status)},
@@ -2564,6 +2663,8 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
       {(void**)&w.arena, sizeof(int32_t) * nbp},
       {(void**)&w.long_list, sizeof(uint32_t) * 2 * (nb / (SHORT_MAX + 1) + 2)},
       {(void**)&w.mid_list, sizeof(uint32_t) * 2 * (size_t)(nb / MID_MIN + 2)},
+      {(void**)&w.mid_own, sizeof(uint32_t) * 2 * (size_t)(nb / MID_MIN + 2)},
+      {(void**)&w.mtab, sizeof(unsigned long long) * 4 * ((size_t)1 << mtab_log2_for(nb))},
       {(void**)&w.staging, sizeof(uint32_t) * (size_t)(n_split_tiles * STG)},
       {(void**)&w.tile_count, sizeof(uint32_t) * (n_split_tiles + 1)},
       {(void**)&w.tile_base, sizeof(uint32_t) * (n_split_tiles + 2)},
@@ -2669,6 +2770,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   c.safe = safe ? 1 : 0;
   c.T = tok->t;
   c.W = ws->w;
+  c.W.mtab_log2 = std::min(mtab_log2_for(n), ws->w.mtab_log2_max);
   c.W.use_cache = ws->cache ? 1 : 0;
   if (ws->cache) c.W.cache = ws->cache->d;
   const int64_t n_split_tiles = (n + TILE - 1) / TILE;
@@ -2677,7 +2779,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   const int sms = ws->num_sms;
   const int seg_grid = (int)std::max<int64_t>(1, std::min<int64_t>((S + 256) / 256, (int64_t)sms * 4));
   tk_prof_mark(ws, "k_reset", st);
-  k_reset<<<sms * 2, 256, 0, st>>>(ws->w, n_split_tiles + 1, n_scan_tiles, c.safe, cut_words,
+  k_reset<<<sms * 2, 256, 0, st>>>(c.W, n_split_tiles + 1, n_scan_tiles, c.safe, cut_words,
                                    n_split_tiles, gb == 0 ? 1 : 0);
   tk_prof_mark(ws, "k_check_segments", st);
   k_check_segments<<<seg_grid, 256, 0, st>>>(c);
@@ -2718,6 +2820,9 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), CL_THREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_medium", side);
     k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
+    tk_prof_mark(ws, "k_dedup_mid", side);
+    k_dedup_mid<false><<<sms * 8, ETHREADS, 0, side>>>(c);
+    k_dedup_mid<true><<<sms * 4, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_mid", side);
     k_merge_mid<false><<<sms * 8, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_mid_long", side);

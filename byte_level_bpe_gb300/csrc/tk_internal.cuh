@@ -52,6 +52,8 @@ struct Status {
   uint32_t n_long;   // pre-tokens over SHORT_MAX bytes (the long-piece lists)
   uint32_t n_mid_a;  // mid pieces of MID_MIN..8 bytes (front of mid_list)
   uint32_t n_mid_b;  // mid pieces of 9..SHORT_MAX bytes (back of mid_list)
+  uint32_t n_own_a;  // distinct mid pieces (first occurrences) of each list, in mid_own
+  uint32_t n_own_b;
   uint32_t n_medium;    // work list sizes and cursors of k_merge_global
   uint32_t n_biglong;
   uint32_t medium_next;
@@ -129,7 +131,11 @@ struct Work {
   uint32_t* long_list;  // (start, length) of pre-tokens of SHORT_MAX+1 .. MEDIUM_MAX bytes
   uint32_t* mid_list;   // (start, length) of pre-tokens of MID_MIN .. SHORT_MAX bytes:
                         // up to 8 bytes from the front, longer ones from the back
-  int64_t mid_cap;      // entries of mid_list
+  int64_t mid_cap;      // entries of mid_list (and of mid_own)
+  uint32_t* mid_own;    // the distinct mid pieces, laid out as mid_list
+  unsigned long long* mtab;  // dedup table of mid pieces: 4 words per slot (key, key2, owner | len, -)
+  uint32_t mtab_log2;        // slots of this call: 2^mtab_log2 (cleared by k_reset)
+  uint32_t mtab_log2_max;
   uint32_t* big_list;   // (start, length) of pre-tokens of MEDIUM_MAX+1 .. CLUSTER_MIN bytes
   uint32_t* cl_list;    // (start, length) of pre-tokens longer than CLUSTER_MIN bytes
   uint32_t* staging;    // per split tile: compacted short ids, long-piece table at the end
