@@ -244,7 +244,7 @@ struct SegCountOp {
 
 __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int safe,
                         int64_t n_cut_words, int64_t n_tiles, int clear_dtab) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (1ll << W.mtab_log2);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; W.mid_dedup && i < (1ll << W.mtab_log2);
        i += (int64_t)gridDim.x * blockDim.x)
   {  // every word: a waiter must never see an owner left by an earlier call
     reinterpret_cast<uint4*>(W.mtab)[2 * i] = make_uint4(0u, 0u, 0u, 0u);
@@ -2544,16 +2544,20 @@ __global__ void __launch_bounds__(ETHREADS) k_dedup_mid(Call c) {
   }
 }
 
-// The distinct mid pieces: one thread each over the whole grid, the register
-// loop of the width the warp's longest piece needs (the front of mid_own: up
-// to 8 bytes, BACK = false; its back: 12 or 16), one launch each so that the
-// narrow loop runs at its own occupancy.  Ids to the arena at the piece's
-// start, the count beside them.
+// The distinct mid pieces (every mid piece when the call does not use the
+// word cache, each then its own source): one thread each over the whole
+// grid, the register loop of the width the warp's longest piece needs (the
+// front of the list: up to 8 bytes, BACK = false; its back: 12 or 16), one
+// launch each so that the narrow loop runs at its own occupancy.  Ids to the
+// arena at the piece's start, the count beside them.
 template <bool BACK>
 __global__ void __launch_bounds__(ETHREADS) k_merge_mid(Call c) {
   const MergeTabs MT(c.T);
   const int lane = threadIdx.x & 31;
-  const int64_t nm = BACK ? c.W.status->n_own_b : c.W.status->n_own_a;
+  const bool dd = c.W.mid_dedup;
+  const int64_t nm = BACK ? (dd ? c.W.status->n_own_b : c.W.status->n_mid_b)
+                          : (dd ? c.W.status->n_own_a : c.W.status->n_mid_a);
+  const uint32_t* lst = dd ? c.W.mid_own : c.W.mid_list;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t b0 = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); b0 < nm; b0 += stride) {
     const int64_t i = b0 + lane;
@@ -2562,8 +2566,8 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_mid(Call c) {
     int64_t p = 0;
     if (valid) {
       const int64_t k = BACK ? c.W.mid_cap - 1 - i : i;
-      p = c.W.mid_own[2 * k];
-      len = (int)c.W.mid_own[2 * k + 1];
+      p = lst[2 * k];
+      len = (int)lst[2 * k + 1];
     }
     const int wmax = BACK ? __reduce_max_sync(0xffffffffu, len) : 8;
     if (!valid) continue;
@@ -2577,6 +2581,7 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_mid(Call c) {
     if constexpr (!BACK) m = merge_reg<8>(MT, b, len, dst);
     else m = wmax <= 12 ? merge_reg<12>(MT, b, len, dst) : merge_reg<16>(MT, b, len, dst);
     c.W.cnt[G] = (uint32_t)m;
+    if (!dd) c.W.gsrc[G] = (uint32_t)G;
   }
 }
 
@@ -2605,6 +2610,11 @@ static int cuda_fail(cudaError_t e, const char* what) {
     cudaError_t e_ = (call);                         \
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
+
+// The mid-piece word cache pays for its table clear and extra launches from
+// about this call size on (below it the side stream's latency, not its work,
+// decides).
+constexpr int64_t MID_DEDUP_MIN = 8ll << 20;
 
 // Slots of the mid-piece word cache for a call of n bytes: one per 64 bytes
 // (the serving batch repeats most words), at least 2^10, at most 2^22.
@@ -2713,8 +2723,11 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
   bool ok = cudaStreamCreateWithFlags(&ws->s_h2d, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&ws->s_d2h, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithPriority(&ws->s_side, cudaStreamNonBlocking, prio_hi) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&ws->s_mid, cudaStreamNonBlocking, prio_hi) == cudaSuccess &&
             cudaEventCreateWithFlags(&ws->ev_split, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&ws->ev_long, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&ws->ev_long, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ws->ev_find, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ws->ev_mid, cudaEventDisableTiming) == cudaSuccess;
   cudaEvent_t* evs[2 * tk_workspace::PIPE_MAX + 1];
   int ne = 0;
   evs[ne++] = &ws->ev_start;
@@ -2746,11 +2759,15 @@ extern "C" void tk_workspace_free(tk_workspace* ws) {
   for (int k = 0; k < ws->n_events; k++)
     cudaEventDestroy(k == 0 ? ws->ev_start : ((k - 1) % 2 == 0 ? ws->ev_h2d[(k - 1) / 2] : ws->ev_done[(k - 1) / 2]));
   if (ws->s_side) cudaStreamSynchronize(ws->s_side);
+  if (ws->s_mid) cudaStreamSynchronize(ws->s_mid);
   if (ws->ev_split) cudaEventDestroy(ws->ev_split);
   if (ws->ev_long) cudaEventDestroy(ws->ev_long);
+  if (ws->ev_find) cudaEventDestroy(ws->ev_find);
+  if (ws->ev_mid) cudaEventDestroy(ws->ev_mid);
   if (ws->s_h2d) cudaStreamDestroy(ws->s_h2d);
   if (ws->s_d2h) cudaStreamDestroy(ws->s_d2h);
   if (ws->s_side) cudaStreamDestroy(ws->s_side);
+  if (ws->s_mid) cudaStreamDestroy(ws->s_mid);
   delete ws;
 }
 
@@ -2771,6 +2788,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   c.T = tok->t;
   c.W = ws->w;
   c.W.mtab_log2 = std::min(mtab_log2_for(n), ws->w.mtab_log2_max);
+  c.W.mid_dedup = n >= MID_DEDUP_MIN ? 1 : 0;
   c.W.use_cache = ws->cache ? 1 : 0;
   if (ws->cache) c.W.cache = ws->cache->d;
   const int64_t n_split_tiles = (n + TILE - 1) / TILE;
@@ -2804,6 +2822,21 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     TK_CUDA(cudaStreamWaitEvent(side, ws->ev_split, 0), "fork");
     tk_prof_mark(ws, "k_find_long", side);
     k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 32 / FIND_WPT) + 255) / 256, (int64_t)sms * 16), 256, 0, side>>>(c);
+    // the mid pieces on a third stream, next to the long pieces' chain
+    cudaStream_t mid = ws->s_mid;
+    TK_CUDA(cudaEventRecord(ws->ev_find, side), "fork");
+    TK_CUDA(cudaStreamWaitEvent(mid, ws->ev_find, 0), "fork");
+    if (c.W.mid_dedup) {
+      tk_prof_mark(ws, "k_dedup_mid", mid);
+      k_dedup_mid<false><<<sms * 8, ETHREADS, 0, mid>>>(c);
+      k_dedup_mid<true><<<sms * 4, ETHREADS, 0, mid>>>(c);
+    }
+    tk_prof_mark(ws, "k_merge_mid", mid);
+    k_merge_mid<false><<<sms * 8, ETHREADS, 0, mid>>>(c);
+    tk_prof_mark(ws, "k_merge_mid_long", mid);
+    k_merge_mid<true><<<sms * 4, ETHREADS, 0, mid>>>(c);
+    tk_prof_mark(ws, nullptr, mid);
+    TK_CUDA(cudaEventRecord(ws->ev_mid, mid), "join");
     tk_prof_mark(ws, "k_dedup_medium", side);
     k_dedup_medium<<<sms * 8, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_dedup_big", side);
@@ -2820,13 +2853,6 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), CL_THREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_merge_medium", side);
     k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_dedup_mid", side);
-    k_dedup_mid<false><<<sms * 8, ETHREADS, 0, side>>>(c);
-    k_dedup_mid<true><<<sms * 4, ETHREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_merge_mid", side);
-    k_merge_mid<false><<<sms * 8, ETHREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_merge_mid_long", side);
-    k_merge_mid<true><<<sms * 4, ETHREADS, 0, side>>>(c);
     if (c.W.use_cache) {
       tk_prof_mark(ws, "k_cache_insert", side);
       k_cache_insert<<<sms * 8, ETHREADS, 0, side>>>(c);
@@ -2839,6 +2865,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     k_encode_tiles<<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
     tk_prof_mark(ws, nullptr, st);
     TK_CUDA(cudaStreamWaitEvent(st, ws->ev_long, 0), "join");
+    TK_CUDA(cudaStreamWaitEvent(st, ws->ev_mid, 0), "join");
     tk_prof_mark(ws, "k_long_fixup", st);
     k_long_fixup<<<(int)std::min<int64_t>((n_split_tiles * 32 + ETHREADS - 1) / ETHREADS, (int64_t)sms * 8), ETHREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_scan_u32", st);

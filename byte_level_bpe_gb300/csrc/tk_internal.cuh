@@ -135,6 +135,7 @@ struct Work {
   uint32_t* mid_own;    // the distinct mid pieces, laid out as mid_list
   unsigned long long* mtab;  // dedup table of mid pieces: 4 words per slot (key, key2, owner | len, -)
   uint32_t mtab_log2;        // slots of this call: 2^mtab_log2 (cleared by k_reset)
+  int mid_dedup;             // this call uses the mid-piece word cache (large calls)
   uint32_t mtab_log2_max;
   uint32_t* big_list;   // (start, length) of pre-tokens of MEDIUM_MAX+1 .. CLUSTER_MIN bytes
   uint32_t* cl_list;    // (start, length) of pre-tokens longer than CLUSTER_MIN bytes
@@ -408,7 +409,9 @@ struct tk_workspace {
   static constexpr int PIPE_MAX = 16;
   cudaStream_t s_h2d, s_d2h;
   cudaStream_t s_side;               // the long-piece kernels, next to the tile kernel
+  cudaStream_t s_mid;                // the mid-piece kernels, next to both
   cudaEvent_t ev_split, ev_long;     // fork after the split, join before the fixup
+  cudaEvent_t ev_find, ev_mid;       // fork after the listing, join before the fixup
   cudaEvent_t ev_start, ev_h2d[PIPE_MAX], ev_done[PIPE_MAX];
   int n_events;
   tk::Status* h_pipe_status;  // [PIPE_MAX] pinned

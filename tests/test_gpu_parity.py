@@ -414,19 +414,20 @@ def test_tile_tables_dense_and_ragged(full_gpu, full_enc):
 
 
 def test_mid_word_cache_keys(full_gpu, full_enc):
-    """The mid-piece word cache keys pieces of 5..16 bytes by their bytes,
-    zero-padded, and their length: pieces that differ only by trailing NUL
-    bytes, or whose second key word is zero, must stay apart; hot words
-    repeated thousands of times share one merge."""
+    """The mid-piece word cache (used by calls of 8 MiB or more) keys pieces
+    of 5..16 bytes by their bytes, zero-padded, and their length: pieces that
+    differ only by trailing NUL bytes, or whose second key word is zero, must
+    stay apart; hot words repeated hundreds of thousands of times share one
+    merge.  9 MiB in 1,300 segments."""
     base = ["!!!!!", "!!!!!\0", "!!!!!\0\0", "!!!!!!!!", "!!!!!!!!\0", "!!!!!!!!\0\0",
             "!!!!!!!!\0!", "!!!!!!!!!!!!!!!\0", "\0\0\0\0\0", "\0\0\0\0\0\0\0\0\0",
             "--------", "--------\0", "#$%&#$%&#$%&", "#$%&#$%&#$%&\0"]
     rng = np.random.default_rng(41)
-    words = [" information", " tokenizer", " encodings", "abcdefgh", " merges"]
-    parts = [base[i] for i in rng.integers(0, len(base), size=3000)]
-    parts += [words[i] for i in rng.integers(0, len(words), size=20000)]
+    words = [" information", " tokenizer", " encodings", "abcdefgh", " merges", " the", " of"]
+    parts = [base[i] for i in rng.integers(0, len(base), size=120000)]
+    parts += [words[i] for i in rng.integers(0, len(words), size=900000)]
     rng.shuffle(parts)
     text = "\n".join(parts)
-    segs = [(text[i:i + 7000], False) for i in range(0, len(text), 7000)]
+    assert len(text) >= 8 << 20
+    segs = [(text[i:i + 7300], False) for i in range(0, len(text), 7300)]
     _compare(full_gpu, full_enc, segs, False)
-    _compare(full_gpu, full_enc, segs, True)
