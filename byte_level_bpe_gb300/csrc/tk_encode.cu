@@ -244,12 +244,6 @@ struct SegCountOp {
 
 __global__ void k_reset(Work W, int64_t n_desc_split, int64_t n_desc_scan, int safe,
                         int64_t n_cut_words, int64_t n_tiles, int clear_dtab) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; W.mid_dedup && i < (1ll << W.mtab_log2);
-       i += (int64_t)gridDim.x * blockDim.x)
-  {  // every word: a waiter must never see an owner left by an earlier call
-    reinterpret_cast<uint4*>(W.mtab)[2 * i] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4*>(W.mtab)[2 * i + 1] = make_uint4(0u, 0u, 0u, 0u);
-  }
   const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (tid == 0) {
@@ -2463,7 +2457,7 @@ __global__ void __launch_bounds__(ETHREADS) k_merge_medium(Call c) {
 // zero-padded), so equal keys of equal length are equal pieces and no byte
 // comparison is needed.  Slot: key0 + 1 (0 = empty; claimed by CAS), key1,
 // then (owner G + 1) | len << 32 published with release.  Each word is
-// written once per call (k_reset clears them in an earlier kernel), so a
+// written once per call (k_clear_mtab clears them in an earlier kernel), so a
 // plain load, which may hit a stale L1 line, returns either 0 or the final
 // value: frequent words are then found in L1 without an atomic, and only a
 // slot that reads empty is claimed by CAS (a hot word's slot would otherwise
@@ -2502,6 +2496,17 @@ __device__ int64_t mid_claim(const Call& c, uint64_t k0, uint64_t k1, int len, i
     if (w1 == k1) return owner;
   }
   return G;
+}
+
+// Clears the mid-piece word cache of this call (every word: a waiter must
+// never see an owner left by an earlier call).  Runs on the mid-piece stream,
+// off the split's critical path.
+__global__ void k_clear_mtab(Work W) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (1ll << W.mtab_log2);
+       i += (int64_t)gridDim.x * blockDim.x) {
+    reinterpret_cast<uint4*>(W.mtab)[2 * i] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(W.mtab)[2 * i + 1] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // One thread per listed mid piece: its source (gsrc) from the word cache;
@@ -2827,6 +2832,8 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     TK_CUDA(cudaEventRecord(ws->ev_find, side), "fork");
     TK_CUDA(cudaStreamWaitEvent(mid, ws->ev_find, 0), "fork");
     if (c.W.mid_dedup) {
+      tk_prof_mark(ws, "k_clear_mtab", mid);
+      k_clear_mtab<<<sms * 4, 256, 0, mid>>>(c.W);
       tk_prof_mark(ws, "k_dedup_mid", mid);
       k_dedup_mid<false><<<sms * 8, ETHREADS, 0, mid>>>(c);
       k_dedup_mid<true><<<sms * 4, ETHREADS, 0, mid>>>(c);
