@@ -1411,7 +1411,6 @@ constexpr int MEDIUM_MAX = 1024;
 constexpr int64_t CLUSTER_MIN = 32768;   // longer pieces merge on a CTA cluster
 constexpr int MERGE_CL = 8;              // CTAs per cluster (portable size)
 constexpr int MAX_GP = TILE / MID_MIN + 2;  // table entries of a tile (pieces of >= MID_MIN bytes)
-constexpr int REG_MAX = 16;  // pieces up to this length merge in registers
 constexpr uint32_t NO_START = 0xFFFFFFFFu;
 // Staging slot per tile (u32 entries): the short ids from the front (rounded
 // up to 4), 4 words per table entry from the back.  Pieces starting in the

@@ -253,14 +253,8 @@ __host__ __device__ __forceinline__ uint32_t s34_hash(uint32_t key, uint32_t log
   return (key * 0x9E3779B1u) >> (32 - log2);
 }
 
-// Load that bypasses L1 allocation (streams and big random tables), keeping
-// L1 for the small tables the merge reads on every pre-token.
-__device__ __forceinline__ uint64_t ld_na_u64(const uint64_t* p) {
-  uint64_t v;
-  asm("ld.global.nc.L1::no_allocate.u64 %0, [%1];" : "=l"(v) : "l"(p));
-  return v;
-}
-
+// Load that bypasses L1 allocation (the streamed text), keeping L1 for the
+// small tables the merge reads on every pre-token.
 __device__ __forceinline__ uint4 ld_na_v4(const void* p) {
   uint4 v;
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
