@@ -157,6 +157,17 @@ def captured_traffic(kernel, n):
     return int(k["dram_bytes"] * n / k["input_bytes"])
 
 
+def max_over_ranks(x, world, device="cuda"):
+    """The largest x over the ranks (x itself on one rank): the job's time is
+    its slowest replica's."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -212,13 +223,12 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
         del flush
+    if world > 1:
+        torch.distributed.barrier()
     clk = clocks.stop()
     prof = native.tk_profile_read(tok.workspace)
     native.tk_profile_enable(tok.workspace, False)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     n_pt, _, n_long = native.tk_last_stats(tok.workspace)
     # e2e: host buffers through tk_encode_segments_host (H2D + encode + D2H each step)
     h_text = torch.from_numpy(text).pin_memory().numpy()
@@ -237,16 +247,15 @@ def run_gpu(args, rank, world):
     if not args.no_e2e:
         host_step()
         torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
         t0 = time.perf_counter()
         e2e_steps = max(1, min(args.steps, 5))
         for _ in range(e2e_steps):
             host_step()
         torch.cuda.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     # warm word cache (reported apart from the cold headline): one call fills a
     # cross-call cache, then the same K steps are timed with it attached
     warm = None
@@ -262,7 +271,7 @@ def run_gpu(args, rank, world):
         w1.record(stream)
         torch.cuda.synchronize()
         hits, _ = native.tk_last_cache_stats(tok.workspace)
-        warm = {"ms_per_step": w0.elapsed_time(w1) / args.steps, "cache_hits": hits}
+        warm = {"ms_per_step": max_over_ranks(w0.elapsed_time(w1) / args.steps, world), "cache_hits": hits}
         native.tk_workspace_set_cache(tok.workspace, None)
         native.tk_cache_free(cache)
     return dict(n=n, S=S, n_ids=n_ids, n_pt=n_pt, n_long=n_long, ms=ms, e2e_ms=e2e_ms, prof=prof, clocks=clk,
