@@ -1,5 +1,6 @@
 // tk_encode.cu -- the encode path of libtk: safe chunking, specials, split,
-// byte-pair merge and ordered assembly, all as CUDA kernels on one stream.
+// byte-pair merge and ordered assembly, all as CUDA kernels (the caller's
+// stream, plus two side streams for the longer pieces).
 //
 // Method (what is computed) follows "tiktoken Deep Dive" ("The split
 // pattern", "Inside encode: a parts vector and a linear scan", "Special
@@ -16,15 +17,19 @@
 //    rest of a white-space run holds a CR/LF or reaches the piece end
 //    (clauses 5-7).  The number-run carry crosses tiles through a decoupled
 //    look-back chain; the white-space facts are read by walking the run.
-//  * merge: pre-tokens up to 64 bytes run the parts loop in one thread over
-//    token ids (a pair of pieces merges to the token whose bytes are their
-//    concatenation, looked up in a pair table built at load).  Longer
-//    pre-tokens get one CTA each and merge in rounds: all leftmost-chained
-//    occurrences of the current minimum-rank pair merge at once, stopping
-//    the round at the first merge that creates a pair of lower rank, which is
-//    exactly the sequence the one-at-a-time loop would take.
-//  * assembly: ids are staged at their pre-token's byte offset, the per
-//    pre-token counts are scanned, and a scatter writes the ids in order.
+//  * merge: the parts loop over token ids (a pair of pieces merges to the
+//    token whose bytes are their concatenation, looked up in a pair table
+//    built at load), sized to the piece: 1-4 bytes in the tile kernel from
+//    slice ranks loaded at once, 5-16 bytes one thread each over the whole
+//    grid (k_merge_mid), longer pieces per warp, CTA or CTA cluster, the
+//    longest in exact rounds: all leftmost-chained occurrences of the current
+//    minimum-rank pair merge at once, stopping the round at the first merge
+//    that creates a pair of lower rank, which is exactly the sequence the
+//    one-at-a-time loop would take.  Repeated pieces of 5 bytes or more are
+//    merged once per call (word caches).
+//  * assembly: each 4 KiB tile stages its short ids and a table of its longer
+//    pieces; after the side streams join, the table gets the pieces' counts,
+//    the tile counts are scanned, and each tile's ids are written in order.
 #include <stdarg.h>
 #include <stddef.h>
 #include <stdio.h>
