@@ -7,7 +7,8 @@
  * objects, not a model").  One call encodes a whole prompt of ordered
  * (text, allow_special) segments ("Making Kimi K3 Tokenization 18x Faster For
  * Million Token Agentic Workloads", "One native call for the whole serving
- * path"); every step of the encode runs in CUDA kernels on the caller's stream.
+ * path"); every step of the encode runs in CUDA kernels, ordered on the
+ * caller's stream.
  *
  * Conventions
  *   - "d_" pointers are device pointers, "h_" pointers are host pointers.
@@ -110,9 +111,13 @@ void tk_workspace_free(tk_workspace* ws);
  *       d_out_offsets[s+1]); d_out_offsets[S] is the total.
  *   h_n_ids: receives the total number of ids (also when it exceeds
  *       out_capacity, in which case TK_E_CAPACITY is returned).
- *   cuda_stream: a cudaStream_t (NULL = legacy default stream).  All kernels
- *       and the one 32-byte device->host status read go on this stream; the
- *       call returns after that read completes.
+ *   cuda_stream: a cudaStream_t (NULL = legacy default stream).  The encode
+ *       is ordered on this stream: the kernels of the pre-tokens of 5 bytes
+ *       or more run on the workspace's two side streams, forked from and
+ *       joined back into cuda_stream by events, so work queued on cuda_stream
+ *       before the call is seen and work queued after it waits for the whole
+ *       encode.  The one 32-byte device->host status read goes on cuda_stream;
+ *       the call returns after that read completes.
  *
  * Errors: TK_E_ARG, TK_E_LIMIT (n_bytes or S above the workspace's limits),
  * TK_E_UTF8 (invalid UTF-8; tk_last_error gives the first bad byte offset),
