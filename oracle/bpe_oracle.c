@@ -237,48 +237,47 @@ int orc_new(const uint8_t* rank_bytes, const int64_t* rank_off, const uint32_t* 
 
 /* ------------------------------------------------------------------------- */
 /* Byte-pair merge of one pre-token ([TT] "Inside encode: a parts vector and  */
-/* a linear scan").  parts[i] = (start offset, rank of the pair that starts   */
-/* at that piece); the leftmost minimum is merged by dropping parts[i+1], and */
-/* only the ranks of parts[i] and parts[i-1] are recomputed.  Returns the     */
-/* number of ids written to out (out has room for m ids).                     */
+/* a linear scan").  The rule: start from one piece per byte; as long as some */
+/* two neighbouring pieces concatenate to a token, join the pair whose token  */
+/* has the lowest rank (the leftmost such pair on a tie); then output the     */
+/* rank of every piece.  Only the two pairs that touch the joined piece can   */
+/* change rank, so only those are looked up again.                            */
+/*                                                                            */
+/* Pieces are kept as a singly linked list over byte offsets: piece k covers  */
+/* bytes [k, nxt[k]) and pr[k] is the rank of piece k joined with the piece   */
+/* after it (RANK_MAX when that is not a token or there is no next piece).   */
+/* Returns the number of ids written to out (out has room for m ids).         */
 
 int64_t orc_bpe_piece(const orc_enc* E, const uint8_t* b, int64_t m, int32_t* out) {
   if (m <= 0) return 0;
-  if (m == 1) {
-    out[0] = (int32_t)rank_of(E, b, 1);
-    return 1;
-  }
-  int64_t* start = (int64_t*)malloc(sizeof(int64_t) * (size_t)(m + 1));
-  uint32_t* rank = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)(m + 1));
-  if (!start || !rank) { free(start); free(rank); return -1; }
-  int64_t len = m + 1;
-  for (int64_t i = 0; i < len; i++) {
-    start[i] = i;
-    rank[i] = (i + 2 <= m) ? rank_of(E, b + i, 2) : RANK_MAX;
+  int64_t* nxt = (int64_t*)malloc(sizeof(int64_t) * (size_t)m);
+  uint32_t* pr = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)m);
+  if (!nxt || !pr) { free(nxt); free(pr); return -1; }
+  for (int64_t k = 0; k < m; k++) {
+    nxt[k] = k + 1;
+    pr[k] = (k + 1 < m) ? rank_of(E, b + k, 2) : RANK_MAX;
   }
   for (;;) {
-    int64_t best = -1;
-    uint32_t best_rank = RANK_MAX;
-    for (int64_t i = 0; i + 1 < len; i++)
-      if (rank[i] < best_rank) { best_rank = rank[i]; best = i; }
-    if (best_rank == RANK_MAX) break;
-    /* drop parts[best + 1]: the two halves become one piece */
-    memmove(start + best + 1, start + best + 2, sizeof(int64_t) * (size_t)(len - best - 2));
-    memmove(rank + best + 1, rank + best + 2, sizeof(uint32_t) * (size_t)(len - best - 2));
-    len--;
-    /* only the neighbours change */
-    rank[best] = (best + 2 < len)
-                     ? rank_of(E, b + start[best], start[best + 2] - start[best])
-                     : RANK_MAX;
-    if (best > 0)
-      rank[best - 1] = rank_of(E, b + start[best - 1], start[best + 1] - start[best - 1]);
+    /* walk the pieces left to right: the first piece whose pair rank is the
+     * smallest seen so far wins, so ties go to the leftmost pair */
+    int64_t win = -1, before = -1, prev = -1;
+    uint32_t lo = RANK_MAX;
+    for (int64_t k = 0; k < m; k = nxt[k]) {
+      if (pr[k] < lo) { lo = pr[k]; win = k; before = prev; }
+      prev = k;
+    }
+    if (win < 0) break; /* no neighbouring pair is a token */
+    /* join piece win with its successor */
+    nxt[win] = nxt[nxt[win]];
+    /* the pair (win, its new successor) and the pair (predecessor, win) */
+    pr[win] = (nxt[win] < m) ? rank_of(E, b + win, nxt[nxt[win]] - win) : RANK_MAX;
+    if (before >= 0) pr[before] = rank_of(E, b + before, nxt[win] - before);
   }
-  int64_t k = 0;
-  for (int64_t j = 0; j + 1 < len; j++)
-    out[k++] = (int32_t)rank_of(E, b + start[j], start[j + 1] - start[j]);
-  free(start);
-  free(rank);
-  return k;
+  int64_t cnt = 0;
+  for (int64_t k = 0; k < m; k = nxt[k]) out[cnt++] = (int32_t)rank_of(E, b + k, nxt[k] - k);
+  free(nxt);
+  free(pr);
+  return cnt;
 }
 
 /* ------------------------------------------------------------------------- */
