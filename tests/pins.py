@@ -65,3 +65,45 @@ def closed_form_cuts(is_space, window=400_000, run=25_000):
                 k += run
             r = q
     return cuts
+
+
+def naive_train(corpus, n_merges):
+    """Brute-force BPE trainer: split the corpus with the printed pattern (the
+    regex library), count identical pre-tokens, then n_merges times recount
+    every adjacent pair of every word from scratch, take the most frequent pair
+    whose concatenation is not a token yet (ties: the smallest (left id, right
+    id)), add it as the next id and join its occurrences left to right.
+    Returns the learned token byte strings in id order."""
+    from collections import Counter
+    words = Counter(regex_split(corpus))
+    seqs = [([w[i:i + 1] for i in range(len(w))], c) for w, c in words.items()]
+    ids = {bytes([b]): b for b in range(256)}
+    learned = []
+    for _ in range(n_merges):
+        counts = Counter()
+        for parts, c in seqs:
+            for a, b in zip(parts, parts[1:]):
+                counts[(a, b)] += c
+        best = None
+        for (a, b), c in counts.items():
+            if a + b in ids:
+                continue
+            key = (-c, ids[a], ids[b])
+            if best is None or key < best[0]:
+                best = (key, a, b)
+        if best is None:
+            break
+        _, a, b = best
+        ids[a + b] = 256 + len(learned)
+        learned.append(a + b)
+        for k, (parts, c) in enumerate(seqs):
+            out, i = [], 0
+            while i < len(parts):
+                if i + 1 < len(parts) and parts[i] == a and parts[i + 1] == b:
+                    out.append(a + b)
+                    i += 2
+                else:
+                    out.append(parts[i])
+                    i += 1
+            seqs[k] = (out, c)
+    return learned

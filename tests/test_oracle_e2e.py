@@ -72,3 +72,24 @@ def test_tiny_table_shape(tiny_table):
     for t in tiny_table[256:]:
         assert any(t[:k] in have and t[k:] in have for k in range(1, len(t)))
         have.add(t)
+
+
+def test_trainer_matches_brute_force():
+    """The plain trainer that builds the tiny table, against a brute-force
+    trainer (tests/pins.py) that recounts pairs from the regex library's split:
+    a slice of the tiny corpus and tie-heavy corpora over two- and three-letter
+    alphabets, where the (left id, right id) tie-break decides most rounds."""
+    pytest.importorskip("regex")
+    import numpy as np
+    from pins import naive_train
+    corpora = [workloads.tiny_corpus()[:24_000]]
+    rng = np.random.default_rng(31)
+    for alphabet in (b"ab", b"abc", b"ab1 "):
+        words = [bytes(rng.choice(list(alphabet), size=int(rng.integers(1, 9))).astype(np.uint8))
+                 for _ in range(600)]
+        corpora.append(b" ".join(words))
+    for corpus in corpora:
+        got = oracle.train(corpus, 120)
+        exp = naive_train(corpus, 120)
+        assert got == exp, (corpus[:40], next((i, g, e) for i, (g, e) in enumerate(zip(got, exp)) if g != e)
+                            if got[:len(exp)] != exp[:len(got)] else (len(got), len(exp)))

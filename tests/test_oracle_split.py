@@ -36,14 +36,19 @@ def _check(s):
 
 
 def test_exhaustive_short_strings():
+    """Every string of up to 5 symbols over the 15-symbol alphabet (813,615
+    strings), then a seeded sample of 150,000 strings of 6 symbols."""
     pytest.importorskip("regex")
     alpha = ALPHABET[:15]
     n = 0
-    for L in range(1, 5):
+    for L in range(1, 6):
         for t in itertools.product(alpha, repeat=L):
             _check("".join(t))
             n += 1
-    assert n == sum(15 ** k for k in range(1, 5))
+    assert n == sum(15 ** k for k in range(1, 6))
+    rng = np.random.default_rng(6)
+    for row in rng.integers(0, 15, size=(150_000, 6)):
+        _check("".join(alpha[i] for i in row))
 
 
 def test_random_strings():
