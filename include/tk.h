@@ -212,11 +212,15 @@ int tk_decode_stream(const tk_tokenizer* tok, tk_workspace* ws, tk_decode_state*
  *   GPU that loads it until the process exits.
  *
  *   The first call on a device looks up that array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   that device current) and keeps it for the life of the process; make that
+ *   first call before any stream capture.  The kept address belongs to the
+ *   device's current context: after cudaDeviceReset on that device, do not
+ *   call this entry point again in the same process.
  *   All calls on a device share the array: calls that overlap on the GPU race,
  *   so serialise them (for example on one stream).  Each call clears the part
- *   of the array it uses before its kernel runs, and returns after reading its
- *   32-byte status back (the call synchronises cuda_stream).
+ *   of the array it uses before its kernel runs, then copies its 64-byte
+ *   status back into host memory and waits for cuda_stream to finish (every
+ *   call synchronises cuda_stream).
  */
 int tk_decode_noalloc(const tk_tokenizer* tok, const int32_t* d_ids, int64_t n, uint8_t* d_out,
                       int64_t cap, int64_t* h_len, void* cuda_stream);

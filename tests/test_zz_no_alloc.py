@@ -63,3 +63,20 @@ def test_errors(gpu_tok):
     assert rc == native.TK_E_LIMIT
     rc, m, out = _noalloc(gpu_tok, ids, 16)  # usable again after the errors
     assert rc == native.TK_OK and out[:m].cpu().numpy().tobytes() == b"ABC"
+
+
+def test_exact_limit(gpu_tok, full_table):
+    """The largest call the fixed scratch takes (1,048,576 ids: its look-back
+    descriptors used to the last one) and one that ends in a partial tile,
+    each with multi-byte ids, against tk_decode."""
+    from byte_level_bpe_gb300 import native
+    ids_cjk, _ = gpu_tok.encode_segments([("中文 \U0001F600 don't", False)])
+    pattern = ids_cjk.repeat((1 << 20) // ids_cjk.numel() + 1)
+    for n in (1 << 20, (1 << 20) - 2047):
+        ids = pattern[:n].contiguous()
+        ref = gpu_tok.decode_device(ids).cpu().numpy().tobytes()
+        for _ in range(2):
+            rc, m, out = _noalloc(gpu_tok, ids, len(ref))
+            assert rc == native.TK_OK, native.load().tk_last_error()
+            assert m == len(ref)
+            assert out[:m].cpu().numpy().tobytes() == ref
