@@ -1510,9 +1510,12 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
     const int xb = tid * 16;
     const uint32_t my = (sm.pb[xb >> 5] >> (xb & 31)) & 0xFFFFu;
     // 2a. lengths (exact up to 32 bytes from the start bitmap, specials in
-    //     full): pieces of up to MID_MIN - 1 bytes are listed for the merge
-    //     below, longer ones flagged for the side stream's merges
+    //     full): pieces of one or two bytes are merged right here (one byte:
+    //     its id; two: the dense pair table, else the two byte ids), pieces of
+    //     three or four bytes are listed for the merge below, longer ones
+    //     flagged for the side stream's merges
     uint32_t n_sh = 0;
+    uint32_t lst = 0, is4 = 0;  // bit j: the piece at xb + j is listed; it has four bytes
     for (uint32_t bits = my; bits; bits &= bits - 1) {
       const int x = xb + __ffs(bits) - 1;
       const int wi = x >> 5;  // pb has a word past the tile's last
@@ -1541,8 +1544,24 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
         }
         sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)(e - (t0 + x)));
         sm.cnt[x] = 1;
+      } else if (len == 1) {
+        sm.stage[x] = (int32_t)__ldg(&c.T.byte_id[sm.text[x]]);
+        sm.cnt[x] = 1;
+      } else if (len == 2) {
+        const uint32_t b0 = sm.text[x], b1 = sm.text[x + 1];
+        const uint32_t r = __ldg(&c.T.dense[(b0 << 8) | b1]);
+        if (r != RANK_MAX) {
+          sm.stage[x] = (int32_t)r;
+          sm.cnt[x] = 1;
+        } else {
+          sm.stage[x] = (int32_t)__ldg(&c.T.byte_id[b0]);
+          sm.stage[x + 1] = (int32_t)__ldg(&c.T.byte_id[b1]);
+          sm.cnt[x] = 2;
+        }
       } else if (len < MID_MIN) {
         n_sh++;
+        lst |= 1u << (x - xb);
+        is4 |= (len == 4 ? 1u : 0u) << (x - xb);
       } else {
         // merged on the side stream, which may still be running: the tile
         // records where the piece is; k_long_fixup adds its ids' count
@@ -1570,16 +1589,9 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
         n_list += t;
       }
       uint32_t q = before + a - n_sh;
-      // the same lengths again (specials and longer pieces have their bits)
-      const uint32_t skip = ((sm.sb[xb >> 5] | sm.gb[xb >> 5]) >> (xb & 31)) & 0xFFFFu;
-      for (uint32_t bits = my & ~skip; bits; bits &= bits - 1) {
-        const int x = xb + __ffs(bits) - 1;
-        const int wi = x >> 5;
-        const uint64_t nx = ((((uint64_t)sm.pb[wi + 1] << 32) | sm.pb[wi]) >> (x & 31)) >> 1;
-        int len = nx ? __ffsll((long long)nx) : 64;
-        const int64_t rem = c.n - (t0 + x);
-        if (rem < len) len = (int)rem;
-        sm.list[q++] = (uint16_t)(x | ((len - 1) << 12));
+      for (uint32_t bits = lst; bits; bits &= bits - 1) {
+        const int j = __ffs(bits) - 1;
+        sm.list[q++] = (uint16_t)((xb + j) | ((2 + ((is4 >> j) & 1u)) << 12));
       }
     }
     __syncthreads();
