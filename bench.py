@@ -1,22 +1,35 @@
 """Benchmark: byte-level BPE encode throughput on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload serving|agentic]
+                    [--workload serving|agentic|multilingual|prose] [--no-sub]
 
 One step = one tk_encode_segments call over the whole workload (split,
 specials, safe chunking, merge, ordered assembly), inputs already in HBM.
 Default workload: the serving batch (4,096 requests, 256 MiB; inputs larger
-than L2, so no flush between steps). Prints one JSON line on rank 0.
+than L2, so no flush between steps). The headline is timed with the library's
+per-kernel profiling off, one CUDA-event pair per step (median, p10, p90 and
+mean reported); per-kernel times come from a second, profiled pass of the same
+K steps. The million-token agentic prompt and the multilingual text are timed
+the same way and reported as keyed sub-records of the same JSON line
+("workloads"), each with its own roofline, CPU baseline and end-to-end figure.
+Prints one JSON line on rank 0.
 
---impl reference times the CPU oracle (the plain single-threaded encoder the
-parity tests compare against) on a bounded sample of the same workload, on
-this machine's host cores.
+The CPU baseline is the oracle (the plain single-threaded encoder the parity
+tests compare against) on one stated sample of each workload, in a child
+process pinned to one host core, best of 3; its ids are compared with the
+GPU's ids for the same segments ("ids_match"; a mismatch exits non-zero).
+--impl reference times the same oracle on the same sample (the reference arm:
+there is no reference code to install, the pages hold only prose).
 """
 import argparse
+import hashlib
 import json
+import multiprocessing as mp
 import os
+import platform
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -25,6 +38,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "BPE encode MB/s and tokens/s on 1 GB300 (IDs bit-exact), % of HBM roofline"
+
+# Bytes of the oracle's sample per workload (about 10-30 s of single-core work
+# for three timed runs at the oracle's ~4 MB/s).
+CPU_SAMPLE_BYTES = 12 << 20
 
 
 def _peaks():
@@ -50,8 +67,9 @@ def make_workload(name, rank=0, total_mb=256):
     elif name == "agentic":
         segs = workloads.agentic_segments(table, seed=3 + 1000 * rank)
         text, off, allow = workloads.pack_segments(segs)
-        desc = ("agentic prompt: ~4 M characters in 2,000 typed segments (alternating "
-                "allow_special), prose/JSON/code/white-space runs up to 60k; tiktoken_safe=1")
+        desc = ("million-token agentic prompt: ~4 M characters in 2,000 typed segments "
+                "(alternating allow_special), prose/JSON/code/white-space runs up to 60k; "
+                "tiktoken_safe=1")
         safe = True
     elif name == "prose":
         text = np.frombuffer(workloads.prose_text(table, 1 << 20, seed=2 + 1000 * rank), np.uint8)
@@ -72,21 +90,27 @@ def make_workload(name, rank=0, total_mb=256):
         safe = False
     else:
         raise SystemExit(f"unknown workload {name}")
-    return table, np.ascontiguousarray(text), off, np.ascontiguousarray(allow), safe, desc
+    return table, np.ascontiguousarray(text), np.ascontiguousarray(off, np.int64), \
+        np.ascontiguousarray(allow), safe, desc
+
+
+def input_sha256(text, off, allow):
+    h = hashlib.sha256()
+    for a in (text, off, allow):
+        h.update(np.ascontiguousarray(a).tobytes())
+    return h.hexdigest()
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """nvidia-smi samples during the timed region (written to a temporary file)."""
 
     def __init__(self, gpu_index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            self.f = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
@@ -101,22 +125,23 @@ class Clocks:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        self.f.seek(0)
+        lines = self.f.read().splitlines()
         self.f.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
@@ -140,14 +165,12 @@ def captured_traffic(kernel, n):
     """DRAM bytes per launch of `kernel` from the committed ncu capture
     (profiles/traffic.txt), scaled to n input bytes; None when the kernel
     sources changed after the capture or the kernel was not captured."""
-    import hashlib
-    root = os.path.dirname(os.path.abspath(__file__))
     try:
-        with open(os.path.join(root, "profiles", "traffic.txt")) as f:
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
             rec = json.load(f)
         h = hashlib.sha256()
         for name in ("tk_encode.cu", "tk_internal.cuh"):
-            with open(os.path.join(root, "byte_level_bpe_gb300", "csrc", name), "rb") as f:
+            with open(os.path.join(ROOT, "byte_level_bpe_gb300", "csrc", name), "rb") as f:
                 h.update(f.read())
     except (OSError, ValueError):
         return None
@@ -168,18 +191,116 @@ def max_over_ranks(x, world, device="cuda"):
     return float(t.item())
 
 
-def run_gpu(args, rank, world):
+# ---------------------------------------------------------------------------
+# CPU leg: the oracle in a child process pinned to one host core.
+
+def host_cpu():
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"model": model or platform.processor() or platform.machine(),
+            "arch": platform.machine(), "nproc": os.cpu_count()}
+
+
+def cpu_sample(off, budget=CPU_SAMPLE_BYTES):
+    """The oracle's sample: the workload's first segments, up to `budget` bytes
+    (at least one segment; a segment longer than the budget is taken whole)."""
+    S = len(off) - 1
+    e = 1
+    while e < S and off[e + 1] <= budget:
+        e += 1
+    return 0, e
+
+
+def _oracle_child(table, text, off, allow, safe, warmup, runs, core):
+    """Runs in a spawned process: pins itself to `core`, builds the oracle's
+    tables (untimed), encodes the sample `warmup` times untimed, then `runs`
+    timed times; returns the wall times and the ids of the last run."""
+    try:
+        os.sched_setaffinity(0, {core})
+        pinned = sorted(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        pinned = None
+    import oracle
+    import workloads
+    enc = oracle.Encoding(table, workloads.SPECIALS)
+    S = len(off) - 1
+    for _ in range(warmup):
+        enc.encode_arrays(text, off, allow, S, safe)
+    times, ids = [], None
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        ids, offs = enc.encode_arrays(text, off, allow, S, safe)
+        times.append(time.perf_counter() - t0)
+    return times, ids, offs, pinned
+
+
+def oracle_leg(table, text, off, allow, safe, warmup=1, runs=3):
+    s, e = cpu_sample(off)
+    sub_text = np.ascontiguousarray(text[off[s]:off[e]])
+    sub_off = np.ascontiguousarray(off[s:e + 1] - off[s])
+    sub_allow = np.ascontiguousarray(allow[s:e] if allow.size >= e else np.zeros(e - s, np.uint8))
+    core = max(0, (os.cpu_count() or 1) - 1)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(1) as pool:
+        times, ids, offs, pinned = pool.apply(_oracle_child, (table, sub_text, sub_off, sub_allow, safe,
+                                                              warmup, runs, core))
+    nb = int(sub_off[-1])
+    return {"times": times, "ids": ids, "offs": offs, "bytes": nb, "segments": (s, e), "core": core,
+            "pinned": pinned}
+
+
+def cpu_record(leg, cpu):
+    best = min(leg["times"])
+    return {"value": round(leg["bytes"] / best / 1e6, 3), "unit": "MB/s", "cores": 1, "kind": "oracle",
+            "tokens_per_s": round(len(leg["ids"]) / best, 1),
+            "sample": (f"segments {leg['segments'][0]}..{leg['segments'][1] - 1} "
+                       f"({leg['bytes']:,} bytes, {len(leg['ids']):,} ids): the workload's first segments "
+                       f"up to {CPU_SAMPLE_BYTES >> 20} MiB; best of {len(leg['times'])} runs after "
+                       f"1 untimed run, single thread pinned to core {leg['core']}"),
+            "runs_s": [round(t, 3) for t in leg["times"]],
+            "pinned_cores": leg["pinned"], "host_cpu": cpu}
+
+
+# ---------------------------------------------------------------------------
+# GPU leg.
+
+def time_steps(step, steps, stream, flush):
+    """K steps, one CUDA-event pair each on the launching stream; with `flush`
+    (inputs that fit in L2) 256 MiB is written before each step, outside its
+    events. Returns the per-step milliseconds."""
+    import torch
+    evs = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_gpu(name, args, rank, world, headline):
     import torch
 
     import byte_level_bpe_gb300 as tk
+    import workloads
     from byte_level_bpe_gb300 import native
 
     dev = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev)
-    table, text, off, allow, safe, desc = make_workload(args.workload, rank, args.total_mb)
+    table, text, off, allow, safe, desc = make_workload(name, rank, args.total_mb if name == "serving" else 256)
     n, S = int(text.size), int(off.size - 1)
-    tok = tk.Tokenizer(table, {k: v for k, v in __import__("workloads").SPECIALS.items()},
-                       max_bytes=n, max_segments=S)
+    tok = tk.Tokenizer(table, dict(workloads.SPECIALS), max_bytes=n, max_segments=S)
     d_text = torch.from_numpy(text).cuda()
     d_off = torch.from_numpy(off).cuda()
     d_allow = torch.from_numpy(allow if allow.size else np.zeros(1, np.uint8)).cuda()
@@ -194,42 +315,24 @@ def run_gpu(args, rank, world):
 
     for _ in range(args.warmup):
         n_ids = step()
-    native.tk_profile_enable(tok.workspace, True)
+    flush = None if n > 160e6 else torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    # headline: profiling off
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = Clocks(dev)
-    if n > 160e6:
-        # inputs larger than L2: back-to-back steps, one pair of events
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            n_ids = step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
-    else:
-        # inputs that fit in L2: flush it (write 256 MiB) before each step, outside
-        # that step's events
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-        evs = []
-        for _ in range(args.steps):
-            flush.fill_(1)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            n_ids = step()
-            b.record(stream)
-            evs.append((a, b))
-        torch.cuda.synchronize()
-        ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-        del flush
+    clocks = Clocks(dev) if headline else None
+    step_ms = time_steps(step, args.steps, stream, flush)
     if world > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    n_pt, n_ids, n_long = native.tk_last_stats(tok.workspace)
+    ids_dev, off_dev = out[:n_ids].cpu().numpy(), out_off.cpu().numpy()
+    # per-kernel times: a second pass of K steps with the library's events on
+    native.tk_profile_enable(tok.workspace, True)
+    prof_ms = time_steps(step, args.steps, stream, flush)
     prof = native.tk_profile_read(tok.workspace)
     native.tk_profile_enable(tok.workspace, False)
-    ms = max_over_ranks(ms, world)
-    n_pt, _, n_long = native.tk_last_stats(tok.workspace)
     # e2e: host buffers through tk_encode_segments_host (H2D + encode + D2H each step)
     h_text = torch.from_numpy(text).pin_memory().numpy()
     h_off = torch.from_numpy(off).pin_memory().numpy()
@@ -249,116 +352,53 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        t0 = time.perf_counter()
         e2e_steps = max(1, min(args.steps, 5))
+        t0 = time.perf_counter()
         for _ in range(e2e_steps):
             host_step()
         torch.cuda.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    # warm word cache (reported apart from the cold headline): one call fills a
-    # cross-call cache, then the same K steps are timed with it attached
+        assert np.array_equal(h_out[:n_ids], ids_dev), "host-buffer call differs from the device call"
     warm = None
-    if not args.no_warm_cache:
+    if headline and not args.no_warm_cache:
+        # warm word cache (reported apart from the cold headline): one call fills a
+        # cross-call cache, then the same K steps are timed with it attached
         cache = native.tk_cache_create(tok.handle, max(n, 1 << 20))
         native.tk_workspace_set_cache(tok.workspace, cache)
         step()
-        torch.cuda.synchronize()
-        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        w0.record(stream)
-        for _ in range(args.steps):
-            step()
-        w1.record(stream)
-        torch.cuda.synchronize()
+        warm_ms = time_steps(step, args.steps, stream, flush)
         hits, _ = native.tk_last_cache_stats(tok.workspace)
-        warm = {"ms_per_step": max_over_ranks(w0.elapsed_time(w1) / args.steps, world), "cache_hits": hits}
+        warm = {"ms_per_step": max_over_ranks(float(np.mean(warm_ms)), world), "cache_hits": hits}
         native.tk_workspace_set_cache(tok.workspace, None)
         native.tk_cache_free(cache)
-    return dict(n=n, S=S, n_ids=n_ids, n_pt=n_pt, n_long=n_long, ms=ms, e2e_ms=e2e_ms, prof=prof, clocks=clk,
-                desc=desc, safe=safe, off=off, text=text, table=table, allow=allow, warm=warm)
+    tok.close()
+    del d_text, out, flush
+    torch.cuda.empty_cache()
+    return dict(name=name, n=n, S=S, n_ids=n_ids, n_pt=n_pt, n_long=n_long, step_ms=step_ms,
+                prof_ms=prof_ms, e2e_ms=max_over_ranks(e2e_ms, world), prof=prof, clocks=clk,
+                desc=desc, safe=safe, off=off, text=text, table=table, allow=allow, warm=warm,
+                ids=ids_dev, g_off=off_dev, sha=input_sha256(text, off, allow))
 
 
-def oracle_sample_rate(table, text, off, allow, safe, seconds=12.0):
-    """Times the oracle on consecutive segments until ~`seconds` of CPU work."""
-    import oracle
-    import workloads
-    enc = oracle.Encoding(table, workloads.SPECIALS)
-    done_b, done_ids, t_used, s = 0, 0, 0.0, 0
-    S = len(off) - 1
-    while t_used < seconds and s < S:
-        e = s
-        while e < S and off[e] - off[s] < 2 << 20:
-            e += 1
-        e = max(e, s + 1)
-        sub_text = text[off[s]:off[e]]
-        sub_off = off[s:e + 1] - off[s]
-        sub_allow = allow[s:e] if allow.size else np.zeros(e - s, np.uint8)
-        t0 = time.perf_counter()
-        ids, _ = enc.encode_arrays(sub_text, sub_off, sub_allow, e - s, safe)
-        t_used += time.perf_counter() - t0
-        done_b += int(sub_off[-1])
-        done_ids += len(ids)
-        s = e
-    return done_b / t_used / 1e6, done_ids / t_used, done_b, s, t_used
+def manifest_entry(name, total_mb):
+    try:
+        with open(os.path.join(ROOT, "workloads", "manifest.json")) as f:
+            m = json.load(f)
+    except (OSError, ValueError):
+        return None
+    key = name if name != "serving" or total_mb == 256 else f"serving_{total_mb}MiB"
+    return m.get("inputs", {}).get(key, {}).get("sha256")
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="serving", choices=["serving", "agentic", "prose", "multilingual"])
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--total-mb", type=int, default=256,
-                    help="serving batch size in MiB (256 = the benchmark workload; smaller for profiling)")
-    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
-    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
-    ap.add_argument("--no-warm-cache", action="store_true", help="skip the warm word-cache leg")
-    args = ap.parse_args()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    if world > 1:
-        import torch
-        torch.distributed.init_process_group("nccl" if args.impl == "gb300" else "gloo")
-
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        table, text, off, allow, safe, desc = make_workload(args.workload, 0, args.total_mb)
-        for _ in range(max(0, min(args.warmup, 1))):
-            pass
-        rates = []
-        for _ in range(args.steps):
-            mbs, tps, nb, nseg, secs = oracle_sample_rate(table, text, off, allow, safe,
-                                                          seconds=args.cpu_seconds / max(1, args.steps))
-            rates.append((mbs, tps, nb, nseg, secs))
-        mbs = float(np.median([r[0] for r in rates]))
-        tps = float(np.median([r[1] for r in rates]))
-        sample = f"first {rates[0][3]} segments ({rates[0][2]} bytes) per step, single thread"
-        line = {"impl": "reference", "metric": METRIC, "value": round(mbs, 3), "unit": "MB/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(1e3 * float(np.median([r[4] for r in rates])), 3),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
-                "data": "synthetic", "config": {"workload": desc, "impl_note": "CPU oracle"},
-                "tokens_per_s": round(tps, 1),
-                "cpu_baseline": {"value": round(mbs, 3), "unit": "MB/s", "cores": 1,
-                                 "kind": "oracle", "sample": sample},
-                "e2e": {"value": round(mbs, 3), "unit": "MB/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
-        return
-
-    r = run_gpu(args, rank, world)
-    n, S, n_ids, n_pt, ms = r["n"], r["S"], r["n_ids"], r["n_pt"], r["ms"]
-    peak, peak_kind = _peaks()
-    total_n = n * world
-    value = total_n / (ms * 1e-3) / 1e6
-    tokens_per_s = n_ids * world / (ms * 1e-3)
-    path_bytes = n + 4 * n_ids + 17 * S
-    # dominant kernel of the timed region
-    prof = r["prof"]
+def record(r, args, world, cpu, peak, peak_kind):
+    """The JSON record of one workload (headline fields + roofline + baselines)."""
+    n, S, n_ids, n_pt = r["n"], r["S"], r["n_ids"], r["n_pt"]
     steps = args.steps
+    ms_steps = [max_over_ranks(x, world) for x in r["step_ms"]]
+    ms = float(np.mean(ms_steps))
+    total_n = n * world
+    path_bytes = n + 4 * n_ids + 17 * S
+    prof = r["prof"]
     dom = max((k for k in prof if kernel_bytes(k, n, n_pt, n_ids, S) is not None),
               key=lambda k: prof[k][0], default=None)
     roof = None
@@ -369,52 +409,142 @@ def main():
         roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": captured_traffic(dom, n),
                 "peak_source": peak_kind, "kernel_ms": round(avg_ms, 4),
-                "algorithmic_bytes": int(kb)}
-    launches = int(sum(v[1] for v in prof.values()))
-    if rank != 0:
-        return
-    cpu_mbs = cpu_tps = cpu_s = float("nan")
-    cpu_b = cpu_seg = 0
-    if not args.no_cpu_baseline:
-        cpu_mbs, cpu_tps, cpu_b, cpu_seg, cpu_s = oracle_sample_rate(
-            r["table"], r["text"], r["off"], r["allow"], r["safe"], seconds=args.cpu_seconds)
+                "algorithmic_bytes": int(kb),
+                "timing": "CUDA events on each kernel's own stream, in a profiled pass of the same "
+                          "K steps right after the headline pass"}
+    launches_per_step = int(sum(v[1] for v in prof.values())) / max(1, steps)
+    leg = None if args.no_cpu_baseline else oracle_leg(r["table"], r["text"], r["off"], r["allow"], r["safe"])
+    ids_match = None
+    if leg is not None:
+        s, e = leg["segments"]
+        got = r["ids"][r["g_off"][s]:r["g_off"][e]]
+        ids_match = bool(np.array_equal(got, leg["ids"]) and
+                         np.array_equal(r["g_off"][s:e + 1] - r["g_off"][s], leg["offs"]))
+    exp_sha = manifest_entry(r["name"], args.total_mb)
     e2e_val = total_n / (r["e2e_ms"] * 1e-3) / 1e6
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "MB/s", "n_gpus": world,
+        "metric": METRIC, "value": round(total_n / (ms * 1e-3) / 1e6, 2), "unit": "MB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "step_ms": {"median": round(float(np.median(ms_steps)), 4),
+                    "p10": round(float(np.percentile(ms_steps, 10)), 4),
+                    "p90": round(float(np.percentile(ms_steps, 90)), 4),
+                    "mean": round(ms, 4), "timing": "one CUDA-event pair per step on the launching "
+                                                     "stream, library profiling off; max over ranks"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic",
         "config": {"workload": r["desc"], "bytes": n, "segments": S, "pretokens": n_pt,
-                   "ids": n_ids, "long_pretokens": r["n_long"], "l2": (f"inputs ({n / 2**20:.0f} MiB) larger than L2 (129 MB); no flush" if n > 160e6
+                   "ids": n_ids, "long_pretokens": r["n_long"],
+                   "input_sha256": r["sha"], "manifest_sha256_match": (None if exp_sha is None
+                                                                       else exp_sha == r["sha"]),
+                   "l2": (f"inputs ({n / 2**20:.0f} MiB) larger than L2 (129 MB); no flush" if n > 160e6
                           else f"inputs ({n / 2**20:.1f} MiB) fit in L2 (129 MB): 256 MiB written "
                                "before each timed step, outside its events"),
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_s": round(tokens_per_s, 1),
+        "tokens_per_s": round(n_ids * world / (ms * 1e-3), 1),
         "path_roofline": {"bound": "hbm", "algorithmic_bytes": int(path_bytes),
                           "achieved": round(path_bytes / (ms * 1e-3) / 1e9, 1), "peak": peak,
-                          "unit": "GB/s", "frac": round(path_bytes / (ms * 1e-3) / 1e9 / peak, 4)},
+                          "unit": "GB/s", "frac": round(path_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+                          "peak_source": peak_kind},
         "roofline": roof,
         "kernels_ms_per_step": {k: round(v[0] / steps, 4) for k, v in sorted(prof.items())},
-        "cpu_baseline": {"value": round(cpu_mbs, 3), "unit": "MB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first {cpu_seg} requests ({cpu_b} bytes), single thread, "
-                                   f"{cpu_s:.1f} s", "tokens_per_s": round(cpu_tps, 1)},
+        "profiled_ms_per_step": round(float(np.mean(r["prof_ms"])), 4),
+        "cpu_baseline": None if leg is None else cpu_record(leg, cpu),
+        "ids_match": ids_match,
         "e2e": {"value": round(e2e_val, 2), "unit": "MB/s",
                 "h2d_bytes_per_step": int(n + 8 * (S + 1) + S),
                 "d2h_bytes_per_step": int(4 * n_ids + 8 * (S + 1) + 64)},
-        "gpu_launches": launches,
-        "warm_cache": None if r["warm"] is None else {
+        "gpu_launches": int(round(launches_per_step * steps)),
+    }
+    if r["warm"] is not None:
+        line["warm_cache"] = {
             "value": round(total_n / (r["warm"]["ms_per_step"] * 1e-3) / 1e6, 2), "unit": "MB/s",
             "ms_per_step": round(r["warm"]["ms_per_step"], 4), "cache_hits": r["warm"]["cache_hits"],
-            "note": "cross-call word cache filled by one earlier call; the headline value is cold"},
-        "clocks": r["clocks"],
-    }
+            "note": "cross-call word cache filled by one earlier call; the headline value is cold"}
+    if r["clocks"] is not None:
+        line["clocks"] = r["clocks"]
+    return line
+
+
+def reference_arm(args, rank):
+    """The oracle alone on the same stated sample as the GPU arm's CPU baseline:
+    W untimed runs, then K timed runs in a child pinned to one core."""
+    if rank != 0:
+        return
+    table, text, off, allow, safe, desc = make_workload(args.workload, 0, args.total_mb)
+    leg = oracle_leg(table, text, off, allow, safe, warmup=args.warmup, runs=args.steps)
+    rates = [leg["bytes"] / t / 1e6 for t in leg["times"]]
+    mbs = float(np.median(rates))
+    rec = cpu_record(leg, host_cpu())
+    rec["value"] = round(mbs, 3)
+    rec["sample"] = rec["sample"].replace(f"best of {len(leg['times'])} runs after 1 untimed run",
+                                          f"median of {len(leg['times'])} runs after {args.warmup} "
+                                          "untimed runs")
+    line = {"impl": "reference", "metric": METRIC, "value": round(mbs, 3), "unit": "MB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * float(np.median(leg["times"])), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic",
+            "config": {"workload": desc, "impl_note": "CPU oracle on the stated sample of the workload",
+                       "input_sha256": input_sha256(text, off, allow)},
+            "tokens_per_s": round(len(leg["ids"]) / float(np.median(leg["times"])), 1),
+            "cpu_baseline": rec,
+            "e2e": {"value": round(mbs, 3), "unit": "MB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="serving", choices=["serving", "agentic", "prose", "multilingual"])
+    ap.add_argument("--total-mb", type=int, default=256,
+                    help="serving batch size in MiB (256 = the benchmark workload; smaller for profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing legs")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer legs")
+    ap.add_argument("--no-warm-cache", action="store_true", help="skip the warm word-cache leg")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the agentic and multilingual sub-records")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        raise SystemExit("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+
+    peak, peak_kind = _peaks()
+    cpu = host_cpu()
+    r = run_gpu(args.workload, args, rank, world, headline=True)
+    subs = []
+    if not args.no_sub and args.workload == "serving":
+        subs = [run_gpu(w, args, rank, world, headline=False) for w in ("agentic", "multilingual")]
+    if rank != 0:
+        return
+    line = record(r, args, world, cpu, peak, peak_kind)
+    if subs:
+        line["workloads"] = {s["name"]: record(s, args, world, cpu, peak, peak_kind) for s in subs}
     print(json.dumps(_finite(line)))
+    bad = [k for k, v in [(args.workload, line)] + list(line.get("workloads", {}).items())
+           if v.get("ids_match") is False]
+    if bad:
+        print(f"ids differ from the oracle on the sample of: {', '.join(bad)}", file=sys.stderr)
+        sys.exit(1)
 
 
 def _finite(x):
     """NaN (a skipped leg) -> null, recursively."""
     if isinstance(x, dict):
         return {k: _finite(v) for k, v in x.items()}
+    if isinstance(x, list):
+        return [_finite(v) for v in x]
     if isinstance(x, float) and x != x:
         return None
     return x

@@ -90,9 +90,13 @@ def test_serving_scaled(full_gpu, full_enc, full_table):
     _compare(full_gpu, full_enc, segs, False)
 
 
-def test_serving_full_size_sampled(full_table, full_enc):
-    """The 256 MiB batch in the bench's launch configuration; sampled requests
-    are encoded one by one by the oracle (segments are independent)."""
+def test_serving_full_size(full_table, tmp_path):
+    """The 256 MiB batch (4,096 requests) in the bench's launch configuration,
+    every id compared with the oracle: requests are independent, so the
+    oracle runs over groups of requests in a pool of host processes (spawned,
+    not forked, since this process already holds a CUDA context)."""
+    import multiprocessing as mp
+    import os
     import byte_level_bpe_gb300 as tk
     text, off = workloads.serving_batch(full_table, seed=5)
     gpu = tk.Tokenizer(full_table, workloads.SPECIALS, max_bytes=len(text), max_segments=len(off))
@@ -102,14 +106,31 @@ def test_serving_full_size_sampled(full_table, full_enc):
     ids, g_off = gpu.encode_device(d_text, d_off, d_allow, tiktoken_safe=False)
     ids = ids.cpu().numpy()
     g_off = g_off.cpu().numpy()
-    rng = np.random.default_rng(0)
-    for r in rng.choice(len(off) - 1, size=24, replace=False):
-        seg = text[off[r]:off[r + 1]].tobytes()
-        exp = full_enc.encode(seg)
-        assert np.array_equal(ids[g_off[r]:g_off[r + 1]], exp), r
+    assert g_off[-1] == len(ids) and len(ids) > 100_000_000
     # properties at full size: ids decode back to the text
     assert gpu.decode(torch.from_numpy(ids)) == text.tobytes()
     gpu.close()
+    del d_text
+    path = str(tmp_path / "c5")
+    np.save(path + "_text.npy", text)
+    np.save(path + "_off.npy", off)
+    np.save(path + "_ids.npy", ids)
+    np.save(path + "_goff.npy", g_off)
+    S = len(off) - 1
+    # groups of consecutive requests of about 4 MiB
+    groups, lo = [], 0
+    while lo < S:
+        hi = lo + 1
+        while hi < S and off[hi + 1] - off[lo] <= 4 << 20:
+            hi += 1
+        groups.append((path, lo, hi))
+        lo = hi
+    import oracle_pool
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(max(1, min(32, os.cpu_count() or 1)), initializer=oracle_pool.init,
+                  initargs=(full_table,)) as pool:
+        errors = [e for e in pool.imap_unordered(oracle_pool.check_requests, groups) if e]
+    assert not errors, errors[:5]
 
 
 # ---------------------------------------------------------------------------
@@ -117,6 +138,25 @@ def test_serving_full_size_sampled(full_table, full_enc):
 
 ALPHABET = ["a", "s", "L", "1", " ", "\n", "\r", "\t", "'", ".", "é", "ा", "\U0001F600",
             " ", "\x00", "ſ", "१", "v", "e", "r", "l", "T", "<|endoftext|>", "中"]
+
+
+def test_special_cut_by_chunking_is_text(full_gpu, full_enc):
+    """tiktoken_safe cuts before specials are matched: a special that a 25k-run
+    cut or a 400k window cut falls inside stays ordinary text, while the same
+    special clear of any cut is its id ("One native call for the whole serving
+    path": the legacy path chunked the text, then encoded each chunk)."""
+    eot = "<|endoftext|>"
+    eot_id = workloads.SPECIALS[eot]
+    run_cut = "x" * 24_995 + eot + " tail"            # the run's 25,000th character is inside it
+    prose = ("ab cd " * 70_000)[:399_995]              # runs stay short; character 400,000 is inside it
+    window_cut = prose + eot + " tail"
+    clear = "x" * 100 + eot + " tail"
+    for text in (run_cut, window_cut):
+        g = _compare(full_gpu, full_enc, [(text, True)], True)
+        assert eot_id not in set(g.tolist())
+        _compare(full_gpu, full_enc, [(text, True)], False)  # unchunked: the special is matched
+    g = _compare(full_gpu, full_enc, [(clear, True), (run_cut, True), (clear, True)], True)
+    assert (g == eot_id).sum() == 2
 
 
 def test_random_segments_fuzz(full_gpu, full_enc):

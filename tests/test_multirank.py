@@ -64,7 +64,7 @@ def test_reference_arm_under_torchrun():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
            "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
-           "--workload", "prose", "--cpu-seconds", "0.5"]
+           "--workload", "prose"]
     env = dict(os.environ, OMP_NUM_THREADS="1")
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-3000:]
@@ -73,3 +73,6 @@ def test_reference_arm_under_torchrun():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the sample is stated, and the oracle ran pinned to one core
+    assert d["cpu_baseline"]["pinned_cores"] is not None and len(d["cpu_baseline"]["pinned_cores"]) == 1
+    assert "segments 0..0" in d["cpu_baseline"]["sample"] and d["cpu_baseline"]["host_cpu"]["nproc"] >= 1
