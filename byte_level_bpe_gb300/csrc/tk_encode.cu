@@ -395,21 +395,27 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) 
 // Split kernel: per 4 KiB tile, pre-token starts -> ordered records.
 
 constexpr int WSEG_MAX = 64;
+constexpr int WALK_MAX = 32;
+constexpr uint32_t NRUN_WALK = 32;  // numbers a thread walks back over before the block scan
 struct SplitSmem {
   uint8_t text[WIN + 16];
   uint8_t kc[WIN];
   uint32_t pst[WIN / 32];   // piece starts
   uint32_t insp[WIN / 32];  // bytes inside special spans
   uint32_t sst[WIN / 32];   // special span starts
-  uint32_t outb[TILE / 32]; // pre-token starts of the tile
   // the segments that meet the window (at most WSEG_MAX): their starts
   // relative to the window (-1: before it), one more entry for the end of the
   // last, and their allow_special flags; nwseg = -1 when there are more
   int32_t wseg[WSEG_MAX + 1];
   uint8_t wallow[WSEG_MAX];
   int nwseg;
-  uint32_t scan[SPLIT_THREADS];
-  uint32_t nagg[SPLIT_THREADS];
+  uint32_t scan[SPLIT_THREADS / 32];  // number runs: the warps' aggregates (long runs only)
+  // white-space walks past the window, deferred to a warp each (walk_rest)
+  int nreq;
+  int64_t req_q[WALK_MAX];
+  uint16_t req_owner[WALK_MAX];  // thread << 4 | bit
+  uint8_t req_check[WALK_MAX];
+  uint8_t req_res[WALK_MAX];
   int64_t tile;
   int64_t seg[2];
   uint64_t ncarry;
@@ -497,11 +503,95 @@ __device__ bool g_ws_rest_ends_in_piece(const Call& c, int64_t q, bool check_q) 
   }
 }
 
+// g_ws_rest_ends_in_piece run by one warp (all 32 lanes, same arguments): the
+// bytes up to the next 16-byte boundary one by one (lane 0), then 512 bytes
+// per step, each lane testing 16 bytes for plain white space (space, tab,
+// VT, FF) with no chunk cut; from the first chunk that is not plain, lane 0
+// walks on one by one.  Only when no special starts with those bytes and the
+// text is 16-byte aligned, else lane 0 walks the whole way.
+__device__ bool warp_ws_rest(const Call& c, int64_t q, bool check_q) {
+  const int lane = threadIdx.x & 31;
+  const bool ws_specials = c.T.n_spec && (((c.T.spec_first[0x20 >> 5] >> (0x20 & 31)) |
+                                            (c.T.spec_first[0] >> 0x09) | (c.T.spec_first[0] >> 0x0B) |
+                                            (c.T.spec_first[0] >> 0x0C)) & 1u);
+  const bool vec = !ws_specials && (((uintptr_t)c.text & 15) == 0);
+  int res = -1;  // lane 0: the answer once known
+  int64_t a0 = (q + 16) & ~(int64_t)15;
+  int64_t lim = 0;
+  if (lane == 0) {
+    lim = min(c.n, c.seg_off[seg_of(c, q) + 1]);
+    if (!vec || a0 + 16 > lim) {
+      res = g_ws_rest_ends_in_piece(c, q, check_q) ? 1 : 0;
+    } else {
+      // the bytes before a0, one by one: an answer there ends the walk
+      int64_t p = q;
+      for (bool first = true; p < a0; first = false) {
+        if (!first || check_q) {
+          if (g_chunk_cut(c, p)) { res = 0; break; }
+          if (c.T.n_spec && g_special_at(c, p, nullptr)) { res = 0; break; }
+        }
+        const uint32_t b = gbyte(c, p);
+        if (b == 0x0A || b == 0x0D) { res = 0; break; }
+        if (b == 0x20 || b == 0x09 || b == 0x0B || b == 0x0C) { p++; continue; }
+        if (b < 0x80) { res = 1; break; }
+        // a multi-byte code point: the serial walk from here
+        res = g_ws_rest_ends_in_piece(c, p, !first || check_q) ? 1 : 0;
+        break;
+      }
+    }
+  }
+  res = __shfl_sync(0xffffffffu, res, 0);
+  if (res >= 0) return res != 0;
+  lim = __shfl_sync(0xffffffffu, lim, 0);
+  int64_t b = lim;
+  for (int64_t p = a0; p < lim; p += 512) {
+    const int64_t mine = p + 16 * lane;
+    bool plain = false;
+    if (mine + 16 <= lim) {
+      const uint4 v = *reinterpret_cast<const uint4*>(c.text + mine);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      plain = true;
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const uint32_t e = __vcmpeq4(wv[k], 0x20202020u) | __vcmpeq4(wv[k], 0x09090909u) |
+                           __vcmpeq4(wv[k], 0x0B0B0B0Bu) | __vcmpeq4(wv[k], 0x0C0C0C0Cu);
+        plain &= e == 0xFFFFFFFFu;
+      }
+      if (plain && c.safe)
+        plain = (((c.W.win_cut[mine >> 5] | c.W.run_cut[mine >> 5]) >> (mine & 31)) & 0xFFFFu) == 0;
+    }
+    const uint32_t np = __ballot_sync(0xffffffffu, !plain);
+    if (np) {
+      b = p + 16 * (__ffs(np) - 1);
+      break;
+    }
+  }
+  // [a0, b) is plain white space inside the piece: walk on from b
+  if (lane == 0) res = (b < lim && g_ws_rest_ends_in_piece(c, b, true)) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, res, 0) != 0;
+}
+
 // Accessors that read the window when the position is trusted, else global.
 struct Win {
   const Call& c;
-  const SplitSmem& sm;
+  SplitSmem& sm;
   int64_t wlo;
+  int owner;  // thread << 4 | bit of the code point under test (for deferred walks)
+  int* ndef;  // this thread's count of deferred walks
+  // The rest of a white-space run past the window (g_ws_rest_ends_in_piece):
+  // queued for a warp (provisional answer false, fixed after the queue runs),
+  // or walked here when the queue is full.
+  __device__ bool walk(int64_t q, bool check_q) const {
+    const int k = atomicAdd(&sm.nreq, 1);
+    if (k < WALK_MAX) {
+      (*ndef)++;
+      sm.req_q[k] = q;
+      sm.req_owner[k] = (uint16_t)owner;
+      sm.req_check[k] = check_q ? 1 : 0;
+      return false;
+    }
+    return g_ws_rest_ends_in_piece(c, q, check_q);
+  }
   __device__ bool trusted(int64_t p) const {
     return p >= wlo + TRUST && p < wlo + WIN - TRUST;
   }
@@ -594,7 +684,7 @@ __device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) 
         int64_t q = x;
         bool check_q = false;
         for (;;) {
-          if (!w.trusted(q) || !w.trusted(q + 4)) return g_ws_rest_ends_in_piece(w.c, q, check_q);
+          if (!w.trusted(q) || !w.trusted(q + 4)) return w.walk(q, check_q);
           const uint8_t kq = w.kc(q) & 7;
           if (kq == K_NL) return false;
           if (kq != K_SP && kq != K_WSO) return true;
@@ -673,6 +763,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
     if (tid == 0) {
       sm.tile = atomicAdd(&c.W.status->tile_ctr[0], 1u);
       s_any_allow = 0;
+      sm.nreq = 0;
     }
     __syncthreads();
     const int64_t tile = sm.tile;
@@ -696,7 +787,6 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       if (c.safe && word >= 0 && (word << 5) < c.n) v = c.W.win_cut[word] | c.W.run_cut[word];
       sm.pst[i] = v;
     }
-    for (int i = tid; i < TILE / 32; i += SPLIT_THREADS) sm.outb[i] = 0;
     const int64_t seg_lo = c.W.tile_segs[4 * tile], seg_hi = c.W.tile_segs[4 * tile + 3];
     __syncthreads();
     // 2. segment starts (and the text end) are piece starts; note whether any
@@ -785,95 +875,116 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       }
     }
     __syncthreads();
-    // 5. number-run aggregate of this thread's 16 bytes
+    // 5. number runs.  The start test needs, for this thread's first code
+    //    point, how many numbers of the same run precede it (mod 3): a walk
+    //    back over the numbers before it (runs are short), stopping at a reset
+    //    (a code point that is not a number, a number inside a special, or a
+    //    number that starts a piece) or at the tile start.  A walk that reaches
+    //    the tile start adds the tile's carry: the run that ends before t0,
+    //    counted in the window if it starts there, else taken from the
+    //    look-back chain over the tiles' aggregates.  Every tile publishes its
+    //    aggregate (NRunOp: the numbers at its end since its last reset, and
+    //    whether nothing in it resets) before anything waits on the chain.
     const int xb = HALO + tid * 16;
-    uint32_t nreset = 0, ncount = 0;
-    {
-      // bit-parallel when the 16 bytes hold no continuation byte and no text
-      // end: D = numbers, reset at every non-number (or number inside a
-      // special), restart at every number that starts a piece
-      const uint32_t* kw = reinterpret_cast<const uint32_t*>(&sm.kc[xb]);
-      uint32_t D = 0, CO = 0;
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        const uint32_t wv = kw[j];
-        const uint32_t p0 = gather_plane(wv, 0), p1 = gather_plane(wv, 1), p2 = gather_plane(wv, 2);
-        D |= (p0 & ~p1 & ~p2 & 0xFu) << (4 * j);
-        CO |= (p1 & p2 & 0xFu) << (4 * j);
+    int unres = 0;  // a walk gave up (a long run of numbers): block scan below
+    if (tid == SPLIT_THREADS - 1) {
+      int p = HALO + (int)min((int64_t)TILE, c.n - t0) - 1;
+      while (p >= HALO && (sm.kc[p] & 7) == K_CONT) p--;
+      uint32_t cnt = 0, unbroken = 1;
+      while (p >= HALO) {
+        if ((sm.kc[p] & 7) != K_N || bit_get(sm.insp, p)) { unbroken = 0; break; }
+        cnt++;
+        if (bit_get(sm.pst, p)) { unbroken = 0; break; }
+        if (cnt == NRUN_WALK) { unres = 1; break; }  // published after the block scan
+        const int q = p;
+        p--;
+        while (p > q - 4 && (sm.kc[p] & 7) == K_CONT) p--;
       }
-      if (CO == 0) {
-        const uint32_t I = (sm.insp[xb >> 5] >> (xb & 31)) & 0xFFFFu;
-        const uint32_t Pm = (sm.pst[xb >> 5] >> (xb & 31)) & 0xFFFFu;
-        const uint32_t non_run = (~D | (D & I)) & 0xFFFFu;
-        const uint32_t restart = D & ~I & Pm;
-        nreset = (non_run | restart) != 0;
-        const int a = non_run ? 31 - __clz(non_run) : -1;
-        const int b = restart ? 31 - __clz(restart) : -1;
-        const int start = max(a + 1, max(b, 0));
-        ncount = (uint32_t)__popc(D & ~I & (0xFFFFu << start) & 0xFFFFu) % 3u;
-      } else {
-        for (int j = 0; j < 16; j++) {
-          const int x = xb + j;
-          const uint8_t k = sm.kc[x] & 7;
-          if (k == K_CONT) continue;
-          if (k == K_OUT) break;
-          if (k != K_N || bit_get(sm.insp, x)) { nreset = 1; ncount = 0; continue; }
-          if (bit_get(sm.pst, x)) { nreset = 1; ncount = 0; }
-          ncount = (ncount + 1) % 3;
+      if (!unres) st_release_u64(&c.W.desc_a[tile], DESC_AGG | (unbroken ? 4u : 0u) | (cnt % 3u));
+    }
+    const int agg_late = unres;
+    uint32_t r = 0;
+    int reach_t0 = 0;  // the walk ran past the tile start without a reset
+    {
+      int q = xb;
+      while (q < xb + 16 && (sm.kc[q] & 7) == K_CONT) q++;
+      int p = q - 1;
+      while (p > q - 4 && (sm.kc[p] & 7) == K_CONT) p--;
+      uint32_t cnt = 0;
+      for (;;) {
+        if (p < HALO) { reach_t0 = 1; break; }
+        if ((sm.kc[p] & 7) != K_N || bit_get(sm.insp, p)) break;
+        cnt++;
+        if (bit_get(sm.pst, p)) break;
+        if (cnt == NRUN_WALK) { unres = 1; break; }
+        const int q2 = p;
+        p--;
+        while (p > q2 - 4 && (sm.kc[p] & 7) == K_CONT) p--;
+      }
+      r = cnt;
+    }
+    // the tile's carry (warp 0; thread 0 of every tile needs it)
+    if (tid < 32) {
+      int resolved = 0;
+      uint32_t cnt = 0;
+      if (tid == 0) {
+        int p = HALO - 1;
+        while (p > HALO - 5 && (sm.kc[p] & 7) == K_CONT) p--;
+        for (;;) {
+          if (p < TRUST) break;
+          if ((sm.kc[p] & 7) != K_N || bit_get(sm.insp, p)) { resolved = 1; break; }
+          cnt++;
+          if (bit_get(sm.pst, p)) { resolved = 1; break; }
+          const int q = p;
+          p--;
+          while (p > q - 5 && (sm.kc[p] & 7) == K_CONT) p--;
         }
       }
+      resolved = __shfl_sync(0xffffffffu, resolved, 0);
+      uint64_t carry;
+      if (resolved) carry = cnt % 3;
+      else carry = carry_walk_warp<NRunOp>(c.W.desc_a, tile, 0, c.W.status, 4);
+      if (tid == 0) sm.ncarry = carry;
     }
-    {
-      // exclusive block scan of the number-run aggregates (warp shuffles)
-      uint32_t x = (nreset ? 0u : 4u) | ncount;
+    if (__syncthreads_or(unres)) {
+      // a run of numbers longer than the walks: every thread's aggregate of
+      // its 16 bytes, an inclusive warp scan, the warps before it
+      uint32_t nreset = 0, ncount = 0;
+      for (int j = 0; j < 16; j++) {
+        const int x = xb + j;
+        const uint8_t k = sm.kc[x] & 7;
+        if (k == K_CONT) continue;
+        if (k == K_OUT) break;
+        if (k != K_N || bit_get(sm.insp, x)) { nreset = 1; ncount = 0; continue; }
+        if (bit_get(sm.pst, x)) { nreset = 1; ncount = 0; }
+        ncount = (ncount + 1) % 3;
+      }
+      const uint32_t mine = (nreset ? 0u : 4u) | ncount;
+      uint32_t x = mine;
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if ((tid & 31) >= o) x = (uint32_t)NRunOp::comb(y, x);
       }
       if ((tid & 31) == 31) sm.scan[tid >> 5] = x;
       __syncthreads();
-      if (tid < 32) {
-        uint64_t run = NRunOp::id();
-        int resolved = 0;
-        uint32_t cnt = 0;
-        if (tid == 0) {
-          for (int w = 0; w < SPLIT_THREADS / 32; w++) {
-            const uint64_t a = sm.scan[w];
-            sm.scan[w] = (uint32_t)run;
-            run = NRunOp::comb(run, a);
-          }
-          st_release_u64(&c.W.desc_a[tile], DESC_AGG | run);
-          // the number run that ends before t0, counted in the window if it
-          // starts there (it almost always does)
-          int p = HALO - 1;
-          while (p > HALO - 5 && (sm.kc[p] & 7) == K_CONT) p--;
-          for (;;) {
-            if (p < TRUST) break;
-            if ((sm.kc[p] & 7) != K_N || bit_get(sm.insp, p)) { resolved = 1; break; }
-            cnt++;
-            if (bit_get(sm.pst, p)) { resolved = 1; break; }
-            const int q = p;
-            p--;
-            while (p > q - 5 && (sm.kc[p] & 7) == K_CONT) p--;
-          }
-        }
-        resolved = __shfl_sync(0xffffffffu, resolved, 0);
-        uint64_t carry;
-        if (resolved) carry = cnt % 3;
-        else carry = carry_walk_warp<NRunOp>(c.W.desc_a, tile, 0, c.W.status, 4);
-        if (tid == 0) sm.ncarry = carry;
+      if (agg_late) {
+        uint64_t agg = NRunOp::id();
+        for (int w = 0; w < SPLIT_THREADS / 32; w++) agg = NRunOp::comb(agg, sm.scan[w]);
+        st_release_u64(&c.W.desc_a[tile], DESC_AGG | agg);
       }
-      __syncthreads();
+      uint64_t pre = sm.ncarry;
+      for (int w = 0; w < (tid >> 5); w++) pre = NRunOp::comb(pre, sm.scan[w]);
       uint32_t e = __shfl_up_sync(0xffffffffu, x, 1);
       if ((tid & 31) == 0) e = (uint32_t)NRunOp::id();
-      sm.nagg[tid] = (uint32_t)NRunOp::comb(sm.scan[tid >> 5], e);
+      r = (uint32_t)(NRunOp::comb(pre, e) & 3);
+    } else if (reach_t0) {
+      r += (uint32_t)(sm.ncarry & 3);
     }
-    __syncthreads();
+    r %= 3u;
     // 6. the start test: 16 ASCII bytes at once where possible, else per code point
     {
-      const Win w{c, sm, wlo};
-      const uint64_t pre = NRunOp::comb(sm.ncarry, sm.nagg[tid]);
-      uint32_t r = (uint32_t)(pre & 3);
+      int ndef = 0;
+      Win w{c, sm, wlo, 0, &ndef};
       uint32_t bits = 0;
       bool fast = wlo + xb + 20 <= c.n;
       uint32_t P[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -898,6 +1009,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
         bits = starts_ascii16(P, r, &slow, c.T.pattern == TK_PATTERN_R50K_DIGITS);
         for (; slow; slow &= slow - 1) {
           const int j = __ffs(slow) - 1;
+          w.owner = (tid << 4) | j;
           if (starts_here(w, wlo + xb + j, sm.kc[xb + j], 0)) bits |= 1u << j;
         }
       } else {
@@ -920,24 +1032,37 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
           bool s;
           if (in_sp) s = bit_get(sm.sst, x);
           else if (bit_get(sm.pst, x)) s = true;
-          else s = starts_here(w, pos, k, nidx);
+          else {
+            w.owner = (tid << 4) | j;
+            s = starts_here(w, pos, k, nidx);
+          }
           if (s) bits |= 1u << j;
         }
       }
-      // 16 bits per thread: two threads share one 32-bit word
-      atomicOr(&sm.outb[tid >> 1], bits << (16 * (tid & 1)));
-    }
-    __syncthreads();
-    // 7. start bitmaps of the tile and the position of its first start
-    //    (tile_first starts at NO_START, set by k_reset).  No barrier after:
-    //    the next tile writes shared memory only after the loop's first one.
-    static_assert(TILE / 32 <= SPLIT_THREADS && (TILE / 32) % 32 == 0, "one bitmap word per thread");
-    if (tid < TILE / 32) {
-      const int64_t word = (t0 >> 5) + tid;
-      const uint32_t w = sm.outb[tid];
-      c.W.pbits[word] = w;
-      if (c.T.n_spec) c.W.sbits[word] = w & sm.sst[(HALO >> 5) + tid];
-      const uint32_t f = __reduce_min_sync(0xffffffffu, w ? (uint32_t)(32 * tid + __ffs(w) - 1) : 0xFFFFFFFFu);
+      // deferred white-space walks: one warp each, then their start bits
+      if (__syncthreads_or(ndef)) {
+        const int nr = min(sm.nreq, WALK_MAX);
+        for (int k = tid >> 5; k < nr; k += SPLIT_THREADS / 32) {
+          const bool res = warp_ws_rest(c, sm.req_q[k], sm.req_check[k] != 0);
+          if ((tid & 31) == 0) sm.req_res[k] = res ? 1 : 0;
+        }
+        __syncthreads();
+        if (ndef)
+          for (int k = 0; k < nr; k++)
+            if ((sm.req_owner[k] >> 4) == tid && sm.req_res[k]) bits |= 1u << (sm.req_owner[k] & 15);
+      }
+      // 7. start bitmaps of the tile (two threads' 16 bits per word) and the
+      //    position of its first start (tile_first starts at NO_START, set by
+      //    k_reset).  No barrier after: the next tile writes shared memory
+      //    only after the loop's first one.
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, bits, 1);
+      if (!(tid & 1)) {
+        const int64_t word = (t0 >> 5) + (tid >> 1);
+        const uint32_t wv = bits | (hi << 16);
+        c.W.pbits[word] = wv;
+        if (c.T.n_spec) c.W.sbits[word] = wv & sm.sst[(HALO >> 5) + (tid >> 1)];
+      }
+      const uint32_t f = __reduce_min_sync(0xffffffffu, bits ? (uint32_t)(16 * tid + __ffs(bits) - 1) : 0xFFFFFFFFu);
       if ((tid & 31) == 0 && f != 0xFFFFFFFFu) atomicMin(&c.W.tile_first[tile], f);
     }
   }
@@ -1509,66 +1634,73 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
     // 2. each thread: its pre-tokens (starts in bytes [16 tid, 16 tid + 16))
     const int xb = tid * 16;
     const uint32_t my = (sm.pb[xb >> 5] >> (xb & 31)) & 0xFFFFu;
-    // 2a. lengths (exact up to 32 bytes from the start bitmap, specials in
-    //     full): pieces of one or two bytes are merged right here (one byte:
-    //     its id; two: the dense pair table, else the two byte ids), pieces of
-    //     three or four bytes are listed for the merge below, longer ones
-    //     flagged for the side stream's merges
-    uint32_t n_sh = 0;
-    uint32_t lst = 0, is4 = 0;  // bit j: the piece at xb + j is listed; it has four bytes
-    for (uint32_t bits = my; bits; bits &= bits - 1) {
+    // 2a. lengths, as bit masks over a 48-bit window of the start bitmap (a
+    //     virtual start at the text end): a start whose next start is k bytes
+    //     on begins a piece of k bytes.  Pieces of one byte are their id, of
+    //     two bytes the dense pair table or the two byte ids; pieces of three
+    //     or four bytes are listed for the merge below; longer ones are
+    //     flagged for the side streams' merges; specials (their exact end
+    //     found one by one) are their id.
+    uint64_t win = (((uint64_t)sm.pb[(xb >> 5) + 1] << 32) | sm.pb[xb >> 5]) >> (xb & 31);
+    {
+      const int64_t e = c.n - (t0 + xb);
+      if (e >= 0 && e < 48) win |= 1ull << e;
+    }
+    const uint32_t n1 = (uint32_t)(win >> 1), n2 = (uint32_t)(win >> 2), n3 = (uint32_t)(win >> 3),
+                   n4 = (uint32_t)(win >> 4);
+    const uint32_t spc = my & ((sm.sb[xb >> 5] >> (xb & 31)) & 0xFFFFu);
+    const uint32_t ord = my & ~spc;
+    const uint32_t m1 = ord & n1, m2 = ord & ~n1 & n2, m3 = ord & ~n1 & ~n2 & n3;
+    const uint32_t m4 = ord & ~n1 & ~n2 & ~n3 & n4, mg = ord & ~(n1 | n2 | n3 | n4);
+    uint32_t inl = (uint32_t)__popc(m1 | spc);  // short ids of the pieces resolved here
+    for (uint32_t bits = m1; bits; bits &= bits - 1) {
       const int x = xb + __ffs(bits) - 1;
-      const int wi = x >> 5;  // pb has a word past the tile's last
-      const uint64_t nx = ((((uint64_t)sm.pb[wi + 1] << 32) | sm.pb[wi]) >> (x & 31)) >> 1;
-      int64_t len = nx ? __ffsll((long long)nx) : 64;  // 33 or more bytes: "long"
-      const int64_t rem = c.n - (t0 + x);               // the text end ends a piece
-      if (rem < len) len = rem;
-      if ((sm.sb[x >> 5] >> (x & 31)) & 1u) {
-        // a special: its exact end (the next start bit, else the first start
-        // of a later tile, else n)
-        int64_t e = -1;
-        int y = x + 1;
-        while (y < TILE + EPAD) {
-          const uint32_t w = sm.pb[y >> 5] >> (y & 31);
-          if (w) { y += __ffs(w) - 1; break; }
-          y = (y | 31) + 1;
-        }
-        if (y < TILE + EPAD) e = t0 + y;
-        else if (t0 + TILE + EPAD >= c.n) e = c.n;
-        else {
-          for (int64_t k = tile + 1; k < ntiles && e < 0; k++) {
-            const uint32_t f = c.W.tile_first[k];
-            if (f != NO_START) e = k * TILE + f;
-          }
-          if (e < 0) e = c.n;
-        }
-        sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)(e - (t0 + x)));
+      sm.stage[x] = (int32_t)__ldg(&c.T.byte_id[sm.text[x]]);
+      sm.cnt[x] = 1;
+    }
+    for (uint32_t bits = m2; bits; bits &= bits - 1) {
+      const int x = xb + __ffs(bits) - 1;
+      const uint32_t b0 = sm.text[x], b1 = sm.text[x + 1];
+      const uint32_t r = __ldg(&c.T.dense[(b0 << 8) | b1]);
+      if (r != RANK_MAX) {
+        sm.stage[x] = (int32_t)r;
         sm.cnt[x] = 1;
-      } else if (len == 1) {
-        sm.stage[x] = (int32_t)__ldg(&c.T.byte_id[sm.text[x]]);
-        sm.cnt[x] = 1;
-      } else if (len == 2) {
-        const uint32_t b0 = sm.text[x], b1 = sm.text[x + 1];
-        const uint32_t r = __ldg(&c.T.dense[(b0 << 8) | b1]);
-        if (r != RANK_MAX) {
-          sm.stage[x] = (int32_t)r;
-          sm.cnt[x] = 1;
-        } else {
-          sm.stage[x] = (int32_t)__ldg(&c.T.byte_id[b0]);
-          sm.stage[x + 1] = (int32_t)__ldg(&c.T.byte_id[b1]);
-          sm.cnt[x] = 2;
-        }
-      } else if (len < MID_MIN) {
-        n_sh++;
-        lst |= 1u << (x - xb);
-        is4 |= (len == 4 ? 1u : 0u) << (x - xb);
+        inl += 1;
       } else {
-        // merged on the side stream, which may still be running: the tile
-        // records where the piece is; k_long_fixup adds its ids' count
-        atomicOr(&sm.gb[x >> 5], 1u << (x & 31));
-        sm.cnt[x] = 0;
+        sm.stage[x] = (int32_t)__ldg(&c.T.byte_id[b0]);
+        sm.stage[x + 1] = (int32_t)__ldg(&c.T.byte_id[b1]);
+        sm.cnt[x] = 2;
+        inl += 2;
       }
     }
+    for (uint32_t bits = spc; bits; bits &= bits - 1) {
+      const int x = xb + __ffs(bits) - 1;
+      // a special: its exact end (the next start bit, else the first start
+      // of a later tile, else n)
+      int64_t e = -1;
+      int y = x + 1;
+      while (y < TILE + EPAD) {
+        const uint32_t w = sm.pb[y >> 5] >> (y & 31);
+        if (w) { y += __ffs(w) - 1; break; }
+        y = (y | 31) + 1;
+      }
+      if (y < TILE + EPAD) e = t0 + y;
+      else if (t0 + TILE + EPAD >= c.n) e = c.n;
+      else {
+        for (int64_t k = tile + 1; k < ntiles && e < 0; k++) {
+          const uint32_t f = c.W.tile_first[k];
+          if (f != NO_START) e = k * TILE + f;
+        }
+        if (e < 0) e = c.n;
+      }
+      sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)(e - (t0 + x)));
+      sm.cnt[x] = 1;
+    }
+    // merged on the side streams, which may still be running: the tile
+    // records where the pieces are; k_long_fixup adds their ids' count
+    if (mg) atomicOr(&sm.gb[xb >> 5], mg << (xb & 31));
+    const uint32_t lst = m3 | m4, is4 = m4;  // bit j: the piece at xb + j is listed; it has four bytes
+    const uint32_t n_sh = (uint32_t)__popc(lst);
     // the list of short pieces: x | (len - 1) << 12, in text order (a block
     // scan of the per-thread counts)
     uint32_t n_list;
@@ -1615,10 +1747,13 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
       }
     }
     __syncthreads();
-    uint32_t my_short = 0;
-    const uint32_t my_g = my & ((sm.gb[xb >> 5] >> (xb & 31)) & 0xFFFFu);
-    for (uint32_t bits = my & ~my_g; bits; bits &= bits - 1) my_short += sm.cnt[xb + __ffs(bits) - 1];
-    atomicAdd(&sm.n_starts, (uint32_t)__popc(my));
+    uint32_t my_short = inl;
+    const uint32_t my_g = mg;
+    for (uint32_t bits = lst; bits; bits &= bits - 1) my_short += sm.cnt[xb + __ffs(bits) - 1];
+    {
+      const uint32_t ns = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(my));
+      if (lane == 0) atomicAdd(&sm.n_starts, ns);
+    }
     __syncthreads();
     if (tid == 0) atomicAdd((unsigned long long*)&c.W.status->n_ptok, (unsigned long long)sm.n_starts);
     // 4. per-thread counts (short ids | table entries << 16; a tile has fewer
@@ -2668,7 +2803,8 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
   const int64_t nbp = nb + 16 * (tk_workspace::PIPE_MAX + 2) + 2;
   const int64_t n_split_tiles = (nb + TILE - 1) / TILE + 1;
   const int64_t n_scan_tiles = (nb + 1 + SCAN_TILE - 1) / SCAN_TILE + 1;
-  const int64_t cut_words = (nb + 64) / 32 + 1;
+  // bitmaps: the split writes whole tiles of the start bitmaps
+  const int64_t cut_words = std::max<int64_t>((nb + 64) / 32 + 1, n_split_tiles * (TILE / 32) + 1);
   Work& w = ws->w;
   w.max_bytes = max_bytes;
   w.max_segments = max_segments;
