@@ -95,10 +95,8 @@ def make_workload(name, rank=0, total_mb=256):
 
 
 def input_sha256(text, off, allow):
-    h = hashlib.sha256()
-    for a in (text, off, allow):
-        h.update(np.ascontiguousarray(a).tobytes())
-    return h.hexdigest()
+    import workloads
+    return workloads.input_sha256(text, off, allow)
 
 
 class Clocks:
@@ -380,14 +378,17 @@ def run_gpu(name, args, rank, world, headline):
                 ids=ids_dev, g_off=off_dev, sha=input_sha256(text, off, allow))
 
 
-def manifest_entry(name, total_mb):
+def manifest_entry(name, total_mb, rank=0):
+    """The recorded sha256 of a workload input (workloads/manifest.json), or
+    None (a serving batch of another size, another rank's seed, or prose)."""
     try:
         with open(os.path.join(ROOT, "workloads", "manifest.json")) as f:
             m = json.load(f)
     except (OSError, ValueError):
         return None
-    key = name if name != "serving" or total_mb == 256 else f"serving_{total_mb}MiB"
-    return m.get("inputs", {}).get(key, {}).get("sha256")
+    if rank != 0 or (name == "serving" and total_mb != 256):
+        return None
+    return m.get("inputs", {}).get(name, {}).get("sha256")
 
 
 def record(r, args, world, cpu, peak, peak_kind):

@@ -612,6 +612,24 @@ struct Win {
     }
     return g_prev(c, p);
   }
+  // From q (a trusted position whose window index is a multiple of 4), past
+  // every 16-byte block that holds only ASCII space, tab, VT or FF (class
+  // bytes K_SP / K_WSO, no flags) with no piece start at the 16 positions
+  // after q's first byte; returns the first position not skipped.
+  __device__ int64_t skip_plain_ws(int64_t q) const {
+    for (;;) {
+      const int i = (int)(q - wlo);
+      if ((i & 3) || !trusted(q) || !trusted(q + 20)) return q;
+      const uint32_t* kw = reinterpret_cast<const uint32_t*>(&sm.kc[i]);
+      const bool ws = ((kw[0] & 0xFEFEFEFEu) == 0x04040404u) & ((kw[1] & 0xFEFEFEFEu) == 0x04040404u) &
+                      ((kw[2] & 0xFEFEFEFEu) == 0x04040404u) & ((kw[3] & 0xFEFEFEFEu) == 0x04040404u);
+      if (!ws) return q;
+      const int j = i + 1;  // piece starts at i + 1 .. i + 16
+      const uint64_t pw = ((uint64_t)sm.pst[(j >> 5) + 1] << 32) | sm.pst[j >> 5];
+      if ((pw >> (j & 31)) & 0xFFFFu) return q;
+      q += 16;
+    }
+  }
   __device__ int64_t next(int64_t p) const {
     if (trusted(p) && trusted(p + 4)) {
       for (int k = 1; k <= 4; k++)
@@ -684,6 +702,7 @@ __device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) 
         int64_t q = x;
         bool check_q = false;
         for (;;) {
+          q = w.skip_plain_ws(q);
           if (!w.trusted(q) || !w.trusted(q + 4)) return w.walk(q, check_q);
           const uint8_t kq = w.kc(q) & 7;
           if (kq == K_NL) return false;

@@ -23,4 +23,7 @@ from .gen import (  # noqa: F401
     tiny_corpus,
     tiny_input,
     pack_segments,
+    input_sha256,
+    table_sha256,
+    manifest_inputs,
 )

@@ -606,3 +606,42 @@ def pack_segments(segments):
         np.cumsum([len(p) for p in parts], out=off[1:])
     allow = np.asarray([1 if a else 0 for _, a in segments], np.uint8)
     return text, off, allow
+
+
+def input_sha256(text, seg_off, allow):
+    """sha256 of one workload input: its text, segment offsets (int64) and
+    allow_special flags (uint8), in that order, as raw bytes."""
+    import hashlib
+    h = hashlib.sha256()
+    for a in (np.ascontiguousarray(text, np.uint8), np.ascontiguousarray(seg_off, np.int64),
+              np.ascontiguousarray(allow, np.uint8)):
+        h.update(a.tobytes())
+    return h.hexdigest()
+
+
+def table_sha256(ranks):
+    """sha256 of a rank table: for each token in rank order its id (int64) and
+    its length (int64), then the token's bytes."""
+    import hashlib
+    h = hashlib.sha256()
+    for i, t in enumerate(ranks):
+        tok, tid = (t if isinstance(t, tuple) else (t, i))
+        h.update(np.array([tid, len(tok)], np.int64).tobytes())
+        h.update(tok)
+    return h.hexdigest()
+
+
+def manifest_inputs(serving_total=256 * MiB):
+    """The inputs the manifest records: name -> (text, seg_off, allow)."""
+    table = full_table()
+    tiny = np.frombuffer(tiny_input(), np.uint8)
+    prose = np.frombuffer(prose_text(table, 1 * MiB, seed=2), np.uint8)
+    one = lambda t: (t, np.array([0, t.size], np.int64), np.zeros(1, np.uint8))  # noqa: E731
+    ag = pack_segments(agentic_segments(table, seed=3))
+    ml = multilingual_text(table, seed=4)
+    ml = np.frombuffer(ml.tobytes() if isinstance(ml, np.ndarray) else bytes(ml), np.uint8)
+    out = {"tiny": one(tiny), "prose": one(prose), "agentic": ag, "multilingual": one(ml)}
+    if serving_total:
+        text, off = serving_batch(table, seed=5, total=serving_total)
+        out["serving"] = (text, off, np.zeros(len(off) - 1, np.uint8))
+    return out
