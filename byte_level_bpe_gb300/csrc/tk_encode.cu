@@ -919,7 +919,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
         p--;
         while (p > q - 4 && (sm.kc[p] & 7) == K_CONT) p--;
       }
-      if (!unres) st_release_u64(&c.W.desc_a[tile], DESC_AGG | (unbroken ? 4u : 0u) | (cnt % 3u));
+      if (!unres) st_relaxed_u64(&c.W.desc_a[tile], DESC_AGG | (unbroken ? 4u : 0u) | (cnt % 3u));
     }
     const int agg_late = unres;
     uint32_t r = 0;
@@ -989,7 +989,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       if (agg_late) {
         uint64_t agg = NRunOp::id();
         for (int w = 0; w < SPLIT_THREADS / 32; w++) agg = NRunOp::comb(agg, sm.scan[w]);
-        st_release_u64(&c.W.desc_a[tile], DESC_AGG | agg);
+        st_relaxed_u64(&c.W.desc_a[tile], DESC_AGG | agg);
       }
       uint64_t pre = sm.ncarry;
       for (int w = 0; w < (tid >> 5); w++) pre = NRunOp::comb(pre, sm.scan[w]);

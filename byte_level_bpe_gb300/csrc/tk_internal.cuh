@@ -176,6 +176,13 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// A self-contained descriptor (state and value in one 64-bit word) needs no
+// ordering with other data: a relaxed store publishes it without the fence a
+// release store implies.
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ void set_error(Status* st, int code, int kind) {
   if (atomicCAS(&st->code, 0, code) == 0) st->err_kind = kind;
 }
