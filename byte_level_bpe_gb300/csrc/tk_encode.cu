@@ -728,13 +728,17 @@ __device__ __forceinline__ uint32_t gather_plane(uint32_t w, int i) {
 }
 
 // The start test for 16 ASCII code points at once (window bytes x0 .. x0+15,
-// no piece start or special byte within 4 before and 4 after).  Bit k of each
-// mask is window byte x0 - 4 + k; the rules are those of starts_here, with the
-// number groups found by propagating run starts in steps of 3.  r is the
-// index in its number run of the code point at x0.  Returns the start bits of
-// the 16 bytes; *slow receives the bytes whose test needs the white-space
-// walks (CR/LF followed by other white space).
-__device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t r, uint32_t* slow,
+// no special span byte within 4 before and 4 after).  Bit k of each mask is
+// window byte x0 - 4 + k; PS holds the piece starts (segment starts, chunk
+// cuts) of those 24 bytes.  The rules are those of starts_here, with the number
+// groups found by propagating run starts in steps of 3, and a piece start as a
+// barrier: it is a start itself, no look-back reaches past it (a run of
+// numbers restarts there, the other-prefix and contraction rules stop at it)
+// and white space whose next code point starts another piece reaches its
+// piece's end.  r is the index in its number run of the code point at x0.
+// Returns the start bits of the 16 bytes; *slow receives the bytes whose test
+// needs the white-space walks (CR/LF followed by other white space).
+__device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t r, uint32_t PS, uint32_t* slow,
                                                    bool r50k_digits) {
   const uint32_t p0 = P[0], p1 = P[1], p2 = P[2];
   const uint32_t L = ~p0 & ~p1 & ~p2, N = p0 & ~p1 & ~p2, O = ~p0 & p1 & ~p2, NL = p0 & p1 & ~p2;
@@ -746,28 +750,31 @@ __device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t
     // one start per digit run, on the space before it if there is one
     S_N = N & ~(N << 1) & ~(SP << 1);
   } else {
-    // numbers: group starts at run start + 3k
-    const uint32_t N1 = N << 1, N2 = N << 2;
-    uint32_t G = N & ~N1 & ~1u;
-    if ((N >> 4) & (N >> 3) & 1u) {  // the run at x0 began earlier: its index there is r
+    // numbers: group starts at run start + 3k; a number that starts a piece
+    // starts a run, and only numbers that are no piece start continue one
+    const uint32_t NR = N & ~PS;
+    uint32_t G = (N & ~(N << 1) & ~1u) | (N & PS);
+    if ((N >> 4) & (N >> 3) & ~(PS >> 4) & 1u) {  // the run at x0 began earlier: its index there is r
       const int first = 4 + (int)((3u - r) % 3u);
       const uint32_t span = ((2u << first) - 1u) & ~0xFu;  // bits 4..first
-      if ((N & span) == span) G |= 1u << first;
+      if ((NR & span) == span) G |= 1u << first;
     }
 #pragma unroll
-    for (int it = 0; it < 7; it++) G |= (G << 3) & N & N1 & N2;
+    for (int it = 0; it < 7; it++) G |= (G << 3) & NR & (NR << 1) & (NR << 2);
     S_N = G & N;
   }
+  const uint32_t nps1 = ~(PS << 1);
   const uint32_t S_L =
-      L & ((N << 1) | (NL << 1) | ((O << 1) & (OS << 2)) |
-           ((L << 1) & (C1 << 1) & (APOS << 2) & ~(OS << 3)) |
-           ((L << 1) & (APOS << 3) & (((LLf << 2) & (LLf << 1)) | ((VR << 2) & (E << 1))) & ~(OS << 4)));
+      L & ((N << 1) | (NL << 1) | ((O << 1) & (OS << 2) & nps1) |
+           ((L << 1) & (C1 << 1) & (APOS << 2) & nps1 & (~(OS << 3) | (PS << 2))) |
+           ((L << 1) & (APOS << 3) & (((LLf << 2) & (LLf << 1)) | ((VR << 2) & (E << 1))) & nps1 & ~(PS << 2) &
+            (~(OS << 4) | (PS << 3))));
   const uint32_t S_O = O & ((L | N | NL | WSO) << 1);
   const uint32_t S_NL = NL & ((L | N) << 1);
-  const uint32_t S_W = SPW & (((L | N | O) << 1) | ((SPW << 1) & ~(WS >> 1)));
-  const uint32_t sl = SPW & (NL << 1);
+  const uint32_t S_W = SPW & (((L | N | O) << 1) | ((SPW << 1) & ~(WS >> 1) & ~(PS >> 1)));
+  const uint32_t sl = SPW & (NL << 1) & ~PS;
   *slow = (sl >> 4) & 0xFFFFu;
-  return ((S_N | S_L | S_O | S_NL | S_W) & ~sl) >> 4 & 0xFFFFu;
+  return (((S_N | S_L | S_O | S_NL | S_W) & ~sl) | PS) >> 4 & 0xFFFFu;
 }
 
 __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
@@ -1007,11 +1014,13 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       uint32_t bits = 0;
       bool fast = wlo + xb + 20 <= c.n;
       uint32_t P[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      uint32_t PS = 0;  // piece starts of bytes xb - 4 .. xb + 19
       if (fast) {
         const int b0 = xb - 4;
-        const uint64_t both = ((uint64_t)(sm.pst[(b0 >> 5) + 1] | sm.insp[(b0 >> 5) + 1]) << 32) |
-                              (sm.pst[b0 >> 5] | sm.insp[b0 >> 5]);
-        fast = ((both >> (b0 & 31)) & 0xFFFFFFu) == 0;
+        const uint64_t ins = ((uint64_t)sm.insp[(b0 >> 5) + 1] << 32) | sm.insp[b0 >> 5];
+        fast = ((ins >> (b0 & 31)) & 0xFFFFFFu) == 0;
+        const uint64_t ps = ((uint64_t)sm.pst[(b0 >> 5) + 1] << 32) | sm.pst[b0 >> 5];
+        PS = (uint32_t)(ps >> (b0 & 31)) & 0xFFFFFFu;
       }
       if (fast) {
         const uint32_t* kw = reinterpret_cast<const uint32_t*>(&sm.kc[xb - 4]);
@@ -1025,7 +1034,7 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       }
       if (fast) {
         uint32_t slow;
-        bits = starts_ascii16(P, r, &slow, c.T.pattern == TK_PATTERN_R50K_DIGITS);
+        bits = starts_ascii16(P, r, PS, &slow, c.T.pattern == TK_PATTERN_R50K_DIGITS);
         for (; slow; slow &= slow - 1) {
           const int j = __ffs(slow) - 1;
           w.owner = (tid << 4) | j;
