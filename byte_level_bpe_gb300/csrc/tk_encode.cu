@@ -772,9 +772,38 @@ __device__ __forceinline__ uint32_t starts_ascii16(const uint32_t P[8], uint32_t
   const uint32_t S_O = O & ((L | N | NL | WSO) << 1);
   const uint32_t S_NL = NL & ((L | N) << 1);
   const uint32_t S_W = SPW & (((L | N | O) << 1) | ((SPW << 1) & ~(WS >> 1) & ~(PS >> 1)));
+  // white space right after CR/LF: a start iff the CR/LF run before it (no
+  // piece start in it) follows an "other" byte (clause 4 took it), else iff
+  // the first byte after it that is not space / other white space, or is a
+  // piece start, is neither a piece start nor CR/LF (the run ends inside the
+  // piece without another CR/LF).  Decided here when both facts lie inside
+  // the 24 bytes (segmented propagations by doubling); the rest is left to
+  // starts_here.
   const uint32_t sl = SPW & (NL << 1) & ~PS;
-  *slow = (sl >> 4) & 0xFFFFu;
-  return (((S_N | S_L | S_O | S_NL | S_W) & ~sl) | PS) >> 4 & 0xFFFFu;
+  uint32_t nl_start = 0, nl_known = 0;
+  if (sl & 0xFFFF0u) {
+    const uint32_t M = NL & ~PS;
+    uint32_t R = M & (O << 1), U = M & 1u, Mk = M;  // runs after "other"; runs reaching bit 0
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      R |= (R << d) & Mk;
+      U |= (U << d) & Mk;
+      Mk &= Mk << d;
+    }
+    const uint32_t absorbed = R << 1, unknown = U << 1;
+    const uint32_t Z = (~SPW | PS) & 0xFFFFFFu;   // stops
+    const uint32_t V = Z & ~WS & ~PS;             // stops that make a start
+    uint32_t Y = (V >> 1) & (Z >> 1), K = Z >> 1;  // the first stop after each byte: known, value
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      Y |= ~K & (Y >> d);
+      K |= K >> d;
+    }
+    nl_known = sl & ~unknown & (absorbed | K);
+    nl_start = nl_known & (absorbed | Y);
+  }
+  *slow = ((sl & ~nl_known) >> 4) & 0xFFFFu;
+  return ((((S_N | S_L | S_O | S_NL | S_W) & ~sl) | PS | nl_start) >> 4) & 0xFFFFu;
 }
 
 __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
