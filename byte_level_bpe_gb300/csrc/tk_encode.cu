@@ -2938,6 +2938,11 @@ extern "C" int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, i
             cudaStreamCreateWithFlags(&ws->s_d2h, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithPriority(&ws->s_side, cudaStreamNonBlocking, prio_hi) == cudaSuccess &&
             cudaStreamCreateWithPriority(&ws->s_mid, cudaStreamNonBlocking, prio_hi) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&ws->s_cl, cudaStreamNonBlocking, prio_hi) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&ws->s_med, cudaStreamNonBlocking, prio_hi) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ws->ev_dedup, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ws->ev_cl, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ws->ev_med, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&ws->ev_split, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&ws->ev_long, cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&ws->ev_find, cudaEventDisableTiming) == cudaSuccess &&
@@ -2974,6 +2979,13 @@ extern "C" void tk_workspace_free(tk_workspace* ws) {
     cudaEventDestroy(k == 0 ? ws->ev_start : ((k - 1) % 2 == 0 ? ws->ev_h2d[(k - 1) / 2] : ws->ev_done[(k - 1) / 2]));
   if (ws->s_side) cudaStreamSynchronize(ws->s_side);
   if (ws->s_mid) cudaStreamSynchronize(ws->s_mid);
+  if (ws->s_cl) cudaStreamSynchronize(ws->s_cl);
+  if (ws->s_med) cudaStreamSynchronize(ws->s_med);
+  if (ws->ev_dedup) cudaEventDestroy(ws->ev_dedup);
+  if (ws->ev_cl) cudaEventDestroy(ws->ev_cl);
+  if (ws->ev_med) cudaEventDestroy(ws->ev_med);
+  if (ws->s_cl) cudaStreamDestroy(ws->s_cl);
+  if (ws->s_med) cudaStreamDestroy(ws->s_med);
   if (ws->ev_split) cudaEventDestroy(ws->ev_split);
   if (ws->ev_long) cudaEventDestroy(ws->ev_long);
   if (ws->ev_find) cudaEventDestroy(ws->ev_find);
@@ -3063,12 +3075,24 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
       tk_prof_mark(ws, "k_cache_lookup_big", side);
       k_cache_lookup_big<<<sms, 1024, 0, side>>>(c);
     }
+    // the three merge tiers take disjoint lists: the cluster and medium
+    // merges run on streams of their own next to the big merges
+    TK_CUDA(cudaEventRecord(ws->ev_dedup, side), "fork");
+    TK_CUDA(cudaStreamWaitEvent(ws->s_cl, ws->ev_dedup, 0), "fork");
+    TK_CUDA(cudaStreamWaitEvent(ws->s_med, ws->ev_dedup, 0), "fork");
+    tk_prof_mark(ws, "k_merge_cluster", ws->s_cl);
+    k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), CL_THREADS, 0, ws->s_cl>>>(c);
+    tk_prof_mark(ws, nullptr, ws->s_cl);
+    TK_CUDA(cudaEventRecord(ws->ev_cl, ws->s_cl), "join");
+    tk_prof_mark(ws, "k_merge_medium", ws->s_med);
+    k_merge_medium<<<sms * 4, ETHREADS, 0, ws->s_med>>>(c);
+    tk_prof_mark(ws, nullptr, ws->s_med);
+    TK_CUDA(cudaEventRecord(ws->ev_med, ws->s_med), "join");
     tk_prof_mark(ws, "k_merge_big", side);
     k_merge_big<<<sms, BIG_THREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_merge_cluster", side);
-    k_merge_cluster<<<MERGE_CL * std::max(1, sms / MERGE_CL), CL_THREADS, 0, side>>>(c);
-    tk_prof_mark(ws, "k_merge_medium", side);
-    k_merge_medium<<<sms * 4, ETHREADS, 0, side>>>(c);
+    tk_prof_mark(ws, nullptr, side);
+    TK_CUDA(cudaStreamWaitEvent(side, ws->ev_cl, 0), "join");
+    TK_CUDA(cudaStreamWaitEvent(side, ws->ev_med, 0), "join");
     if (c.W.use_cache) {
       tk_prof_mark(ws, "k_cache_insert", side);
       k_cache_insert<<<sms * 8, ETHREADS, 0, side>>>(c);

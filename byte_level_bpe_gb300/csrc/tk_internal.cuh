@@ -370,7 +370,7 @@ struct tk_tokenizer {
 };
 
 struct tk_profile {
-  static constexpr int MAXK = 40;
+  static constexpr int MAXK = 64;
   int on;
   int n;                        // kernels with totals
   const char* names[MAXK];
@@ -411,6 +411,8 @@ struct tk_workspace {
   cudaStream_t s_h2d, s_d2h;
   cudaStream_t s_side;               // the long-piece kernels, next to the tile kernel
   cudaStream_t s_mid;                // the mid-piece kernels, next to both
+  cudaStream_t s_cl, s_med;          // the cluster and medium merges, next to the big merges
+  cudaEvent_t ev_dedup, ev_cl, ev_med;  // fork after the long pieces' word cache, joins
   cudaEvent_t ev_split, ev_long;     // fork after the split, join before the fixup
   cudaEvent_t ev_find, ev_mid;       // fork after the listing, join before the fixup
   cudaEvent_t ev_start, ev_h2d[PIPE_MAX], ev_done[PIPE_MAX];
