@@ -1607,6 +1607,7 @@ constexpr int64_t STG = TILE + SHORT_MAX + 8;
 static_assert(MID_MIN >= 5 && TILE + MID_MIN - 1 + 3 <= STG, "staging slot bound");
 constexpr uint32_t DTAB_LOG2 = 20;                  // dedup table of long pieces: 2^20 slots
 
+constexpr int LIST_END = TILE + SHORT_MAX;  // the mid pieces' list ends here
 struct EncSmem {
   uint8_t text[TILE + EPAD + 16];
   uint32_t pb[(TILE + EPAD) / 32 + 1];  // pre-token starts in [t0, t0 + TILE + EPAD)
@@ -1615,7 +1616,8 @@ struct EncSmem {
   uint8_t cnt[TILE];                    // ids of the short piece starting at each byte
   int32_t stage[TILE + SHORT_MAX];      // ids of short pieces, at their start byte
   union {
-    uint16_t list[TILE + SHORT_MAX];    // work list: x | (len - 1) << 12 (until the merges end)
+    uint16_t list[TILE + SHORT_MAX];    // work lists: x | (len - 1) << 12 (until the merges end):
+                                        // 3-4-byte pieces from the front, mid pieces from the back
     __align__(16) int32_t outs[TILE + SHORT_MAX + 4];  // then the tile's short ids in order
   };
   uint32_t th_full[ETHREADS];           // short ids before each thread's 16 bytes
@@ -1652,6 +1654,7 @@ __device__ uint32_t ids_before(const EncSmem& sm, int x) {
   return r | (g << 16);
 }
 
+template <bool MIDS>
 __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   EncSmem& sm = *reinterpret_cast<EncSmem*>(smem_raw);
@@ -1753,14 +1756,29 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
       sm.stage[x] = special_id_smem(c.T, &sm.text[x], (int)(e - (t0 + x)));
       sm.cnt[x] = 1;
     }
-    // merged on the side streams, which may still be running: the tile
-    // records where the pieces are; k_long_fixup adds their ids' count
-    if (mg) atomicOr(&sm.gb[xb >> 5], mg << (xb & 31));
+    // with MIDS, pieces of 5..SHORT_MAX bytes (the next start within 16
+    // bytes) are merged here too, after the short ones; longer pieces (and
+    // without MIDS the mid pieces) are merged on the side streams, which may
+    // still be running: the tile records where they are, k_long_fixup adds
+    // their ids' count
+    uint32_t mid = 0, mlen = 0;  // mid pieces; their lengths - 1, 4 bits each, in start order
+    for (uint32_t bits = MIDS ? mg : 0u; bits; bits &= bits - 1) {
+      const int j = __ffs(bits) - 1;
+      const uint32_t nx = (uint32_t)(win >> (j + 1)) & 0xFFFFu;
+      if (nx) {
+        mid |= 1u << j;
+        mlen = (mlen >> 4) | ((uint32_t)(__ffs(nx) - 1) << 28);
+      }
+    }
+    const uint32_t lng = mg & ~mid;
+    if (lng) atomicOr(&sm.gb[xb >> 5], lng << (xb & 31));
     const uint32_t lst = m3 | m4, is4 = m4;  // bit j: the piece at xb + j is listed; it has four bytes
-    const uint32_t n_sh = (uint32_t)__popc(lst);
-    // the list of short pieces: x | (len - 1) << 12, in text order (a block
-    // scan of the per-thread counts)
-    uint32_t n_list;
+    const uint32_t n_mid = (uint32_t)__popc(mid);
+    const uint32_t n_sh = (uint32_t)__popc(lst) | (n_mid << 16);
+    // the lists: pieces of 3-4 bytes from the front, mid pieces from the
+    // back, x | (len - 1) << 12, in text order (a block scan of the
+    // per-thread counts, both packed in one word)
+    uint32_t n_list, n_mids;
     {
       uint32_t a = n_sh;
       for (int o = 1; o < 32; o <<= 1) {
@@ -1769,18 +1787,26 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
       }
       if (lane == 31) sm.warp_tot[ETHREADS / 32 + warp] = a;
       __syncthreads();
-      uint32_t before = 0;
-      n_list = 0;
+      uint32_t before = 0, all = 0;
 #pragma unroll
       for (int w = 0; w < ETHREADS / 32; w++) {
         const uint32_t t = sm.warp_tot[ETHREADS / 32 + w];
         before += w < warp ? t : 0u;
-        n_list += t;
+        all += t;
       }
-      uint32_t q = before + a - n_sh;
+      n_list = all & 0xFFFFu;
+      n_mids = all >> 16;
+      const uint32_t ex = before + a - n_sh;
+      uint32_t q = ex & 0xFFFFu;
       for (uint32_t bits = lst; bits; bits &= bits - 1) {
         const int j = __ffs(bits) - 1;
         sm.list[q++] = (uint16_t)((xb + j) | ((2 + ((is4 >> j) & 1u)) << 12));
+      }
+      uint32_t qm = ex >> 16;
+      uint32_t ml = n_mid ? mlen >> (32 - 4 * n_mid) : 0u;  // the first mid piece's length in the low bits
+      for (uint32_t bits = mid; bits; bits &= bits - 1, ml >>= 4) {
+        const int j = __ffs(bits) - 1;
+        sm.list[LIST_END - 1 - qm++] = (uint16_t)((xb + j) | ((ml & 15u) << 12));
       }
     }
     __syncthreads();
@@ -1802,11 +1828,28 @@ __global__ void __launch_bounds__(ETHREADS, 5) k_encode_tiles(Call c) {
         for (int u = 0; u < MERGE_U; u++)
           if (xs[u] >= 0) sm.cnt[xs[u]] = (uint8_t)le4_finish(MT, L[u], &sm.stage[xs[u]]);
       }
+      // 2c. mid pieces, one per thread, the parts loop in registers at the
+      //     width of the warp's longest piece
+      if constexpr (MIDS)
+      for (uint32_t b0 = warp * 32; b0 < n_mids; b0 += ETHREADS) {
+        const uint32_t i = b0 + lane;
+        const bool valid = i < n_mids;
+        const uint32_t e = valid ? sm.list[LIST_END - 1 - i] : 0u;
+        const int len = valid ? (int)(e >> 12) + 1 : 0;
+        const int wmax = __reduce_max_sync(0xffffffffu, len);
+        if (!valid) continue;
+        const int x = (int)(e & 0xFFF);
+        int m;
+        if (wmax <= 8) m = merge_reg<8>(MT, &sm.text[x], len, &sm.stage[x]);
+        else if (wmax <= 12) m = merge_reg<12>(MT, &sm.text[x], len, &sm.stage[x]);
+        else m = merge_reg<16>(MT, &sm.text[x], len, &sm.stage[x]);
+        sm.cnt[x] = (uint8_t)m;
+      }
     }
     __syncthreads();
     uint32_t my_short = inl;
-    const uint32_t my_g = mg;
-    for (uint32_t bits = lst; bits; bits &= bits - 1) my_short += sm.cnt[xb + __ffs(bits) - 1];
+    const uint32_t my_g = lng;
+    for (uint32_t bits = lst | mid; bits; bits &= bits - 1) my_short += sm.cnt[xb + __ffs(bits) - 1];
     {
       const uint32_t ns = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(my));
       if (lane == 0) atomicAdd(&sm.n_starts, ns);
@@ -2149,8 +2192,10 @@ __device__ __forceinline__ void list_long(const Call& c, int64_t p, int64_t len)
 }
 
 // The pre-tokens of MID_MIN bytes or more: mid pieces (up to SHORT_MAX
-// bytes) -> mid_list, up to 8 bytes from the front and longer ones from the
-// back (k_merge_mid gives a warp one of the two); longer ones -> list_long.
+// bytes) -> mid_list when they are merged on the side streams (mid_side; up
+// to 8 bytes from the front and longer ones from the back: k_merge_mid gives
+// a warp one of the two), else the tile kernel merges them; longer ones ->
+// list_long.
 // Each thread reads FIND_WPT words of the start bitmap; a start's length is
 // the distance to the next start bit (the next word is in reach of every
 // start of the word; the text end counts as a start), else piece_end.  The
@@ -2207,6 +2252,7 @@ __global__ void __launch_bounds__(256) k_find_long(Call c) {
           const uint64_t nxt = w >> (x + 1);
           const int d = nxt ? __ffsll((long long)nxt) : 0;  // length, if the next start is in w
           if (d >= MID_MIN && d <= SHORT_MAX) {
+            if (!c.W.mid_side) continue;
             if (pass == 0) {
               if (d <= 8) ia++;
               else ib++;
@@ -2828,6 +2874,13 @@ static int cuda_fail(cudaError_t e, const char* what) {
 // about this call size on (below it the side stream's latency, not its work,
 // decides).
 constexpr int64_t MID_DEDUP_MIN = 8ll << 20;
+// Calls of at least this size merge their mid pieces (5..SHORT_MAX bytes) on
+// a side stream with the mid-piece word cache, next to the tile kernel;
+// smaller calls merge them inside the tile kernel (measured: the 256 MiB
+// serving batch, whose requests repeat, is 0.57 ms faster per call with the
+// word cache; the 4 MB agentic prompt and the 8 MiB multilingual text are
+// 0.04-0.07 ms faster in the tile kernel).
+constexpr int64_t MID_SIDE_MIN = 16ll << 20;
 
 // Slots of the mid-piece word cache for a call of n bytes: one per 64 bytes
 // (the serving batch repeats most words), at least 2^10, at most 2^22.
@@ -3014,7 +3067,8 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   c.T = tok->t;
   c.W = ws->w;
   c.W.mtab_log2 = std::min(mtab_log2_for(n), ws->w.mtab_log2_max);
-  c.W.mid_dedup = n >= MID_DEDUP_MIN ? 1 : 0;
+  c.W.mid_side = n >= MID_SIDE_MIN ? 1 : 0;
+  c.W.mid_dedup = (c.W.mid_side && n >= MID_DEDUP_MIN) ? 1 : 0;
   c.W.use_cache = ws->cache ? 1 : 0;
   if (ws->cache) c.W.cache = ws->cache->d;
   const int64_t n_split_tiles = (n + TILE - 1) / TILE;
@@ -3048,23 +3102,26 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     TK_CUDA(cudaStreamWaitEvent(side, ws->ev_split, 0), "fork");
     tk_prof_mark(ws, "k_find_long", side);
     k_find_long<<<(int)std::min<int64_t>((n_split_tiles * (TILE / 32 / FIND_WPT) + 255) / 256, (int64_t)sms * 16), 256, 0, side>>>(c);
-    // the mid pieces on a third stream, next to the long pieces' chain
+    // the mid pieces of large calls on a third stream, next to the long
+    // pieces' chain
     cudaStream_t mid = ws->s_mid;
-    TK_CUDA(cudaEventRecord(ws->ev_find, side), "fork");
-    TK_CUDA(cudaStreamWaitEvent(mid, ws->ev_find, 0), "fork");
-    if (c.W.mid_dedup) {
-      tk_prof_mark(ws, "k_clear_mtab", mid);
-      k_clear_mtab<<<sms * 4, 256, 0, mid>>>(c.W);
-      tk_prof_mark(ws, "k_dedup_mid", mid);
-      k_dedup_mid<false><<<sms * 8, ETHREADS, 0, mid>>>(c);
-      k_dedup_mid<true><<<sms * 4, ETHREADS, 0, mid>>>(c);
+    if (c.W.mid_side) {
+      TK_CUDA(cudaEventRecord(ws->ev_find, side), "fork");
+      TK_CUDA(cudaStreamWaitEvent(mid, ws->ev_find, 0), "fork");
+      if (c.W.mid_dedup) {
+        tk_prof_mark(ws, "k_clear_mtab", mid);
+        k_clear_mtab<<<sms * 4, 256, 0, mid>>>(c.W);
+        tk_prof_mark(ws, "k_dedup_mid", mid);
+        k_dedup_mid<false><<<sms * 8, ETHREADS, 0, mid>>>(c);
+        k_dedup_mid<true><<<sms * 4, ETHREADS, 0, mid>>>(c);
+      }
+      tk_prof_mark(ws, "k_merge_mid", mid);
+      k_merge_mid<false><<<sms * 8, ETHREADS, 0, mid>>>(c);
+      tk_prof_mark(ws, "k_merge_mid_long", mid);
+      k_merge_mid<true><<<sms * 4, ETHREADS, 0, mid>>>(c);
+      tk_prof_mark(ws, nullptr, mid);
+      TK_CUDA(cudaEventRecord(ws->ev_mid, mid), "join");
     }
-    tk_prof_mark(ws, "k_merge_mid", mid);
-    k_merge_mid<false><<<sms * 8, ETHREADS, 0, mid>>>(c);
-    tk_prof_mark(ws, "k_merge_mid_long", mid);
-    k_merge_mid<true><<<sms * 4, ETHREADS, 0, mid>>>(c);
-    tk_prof_mark(ws, nullptr, mid);
-    TK_CUDA(cudaEventRecord(ws->ev_mid, mid), "join");
     tk_prof_mark(ws, "k_dedup_medium", side);
     k_dedup_medium<<<sms * 8, ETHREADS, 0, side>>>(c);
     tk_prof_mark(ws, "k_dedup_big", side);
@@ -3099,13 +3156,16 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     }
     tk_prof_mark(ws, nullptr, side);
     TK_CUDA(cudaEventRecord(ws->ev_long, side), "join");
-    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(EncSmem)), "smem attribute");
+    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(EncSmem)), "smem attribute");
     tk_prof_mark(ws, "k_encode_tiles", st);
-    k_encode_tiles<<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
+    if (c.W.mid_side) k_encode_tiles<false><<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
+    else k_encode_tiles<true><<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
     tk_prof_mark(ws, nullptr, st);
     TK_CUDA(cudaStreamWaitEvent(st, ws->ev_long, 0), "join");
-    TK_CUDA(cudaStreamWaitEvent(st, ws->ev_mid, 0), "join");
+    if (c.W.mid_side) TK_CUDA(cudaStreamWaitEvent(st, ws->ev_mid, 0), "join");
     tk_prof_mark(ws, "k_long_fixup", st);
     k_long_fixup<<<(int)std::min<int64_t>((n_split_tiles * 32 + ETHREADS - 1) / ETHREADS, (int64_t)sms * 8), ETHREADS, 0, st>>>(c);
     tk_prof_mark(ws, "k_scan_u32", st);

@@ -135,6 +135,7 @@ struct Work {
   uint32_t* mid_own;    // the distinct mid pieces, laid out as mid_list
   unsigned long long* mtab;  // dedup table of mid pieces: 4 words per slot (key, key2, owner | len, -)
   uint32_t mtab_log2;        // slots of this call: 2^mtab_log2 (cleared by k_clear_mtab)
+  int mid_side;              // mid pieces are merged on a side stream (large calls), else in the tile kernel
   int mid_dedup;             // this call uses the mid-piece word cache (large calls)
   uint32_t mtab_log2_max;
   uint32_t* big_list;   // (start, length) of pre-tokens of MEDIUM_MAX+1 .. CLUSTER_MIN bytes
