@@ -471,3 +471,24 @@ def test_mid_word_cache_keys(full_gpu, full_enc):
     assert len(text) >= 8 << 20
     segs = [(text[i:i + 7300], False) for i in range(0, len(text), 7300)]
     _compare(full_gpu, full_enc, segs, False)
+
+
+def test_big_mixed_white_space_pieces(full_gpu, full_enc):
+    """Pre-tokens of 1,025-26,000 bytes of mixed white space (spaces, tabs and
+    their boundaries, which no token of the table holds), runs ending in CR/LF
+    and a long letter/white-space mix: the exact rounds of the big-piece merge
+    against the oracle's parts loop."""
+    rng = np.random.default_rng(23)
+    segs = []
+    for n in (1030, 1500, 4000, 9000, 17000, 26000):
+        for mix in ((" ", "\t"), (" ", " ", " ", "\t", "\t\t"), (" ", "\t", " \t ")):
+            parts = []
+            while sum(len(p) for p in parts) < n:
+                parts.append(mix[int(rng.integers(0, len(mix)))] * int(rng.integers(1, 40)))
+            run = "".join(parts)[:n]
+            segs.append(("x" + run + "y", False))
+            segs.append((run + "\n", False))
+    segs.append(("a" + " \t" * 5 + " " * 2000 + "b", False))
+    segs.append(("q" + "ab" * 900 + " " + "\t" * 1200, False))
+    _compare(full_gpu, full_enc, segs, False)
+    _compare(full_gpu, full_enc, segs, True)
