@@ -83,8 +83,11 @@ void tk_free(tk_tokenizer* tok);
  * max_bytes bytes in up to max_segments segments ("tokenizers v1: encode,
  * decode and scaling, measured", "Key Technical Improvements": the merge
  * working set lives in a caller-owned scratch buffer, so an encode never
- * touches an allocator).  About 22 bytes of device memory per byte of
- * max_bytes.  A workspace serves one encode at a time.
+ * touches an allocator).  About 44 bytes of device memory per byte of
+ * max_bytes (11.9 GB for max_bytes = 256 MiB: seven 4-byte arrays indexed
+ * by byte position for the long-piece merges, the per-tile staging of the
+ * ids, the host-call staging, the mid-piece lists and the bitmaps).  A
+ * workspace serves one encode at a time.
  */
 int tk_workspace_create(const tk_tokenizer* tok, int64_t max_bytes, int64_t max_segments,
                         tk_workspace** out);
