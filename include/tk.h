@@ -148,8 +148,9 @@ int tk_encode_segments_host(const tk_tokenizer* tok, tk_workspace* ws, const uin
 
 /*
  * tk_decode -- ids -> bytes on the device ("tiktoken Deep Dive", "The byte
- * floor": round trips are exact at the byte level; "Pitfalls that bite in
- * production": decode the bytes, not the pieces).
+ * floor": a round trip reproduces the input byte for byte; "Pitfalls that
+ * bite in production": the output is the concatenated bytes of all ids, since
+ * one character's bytes may be spread over several ids).
  *
  *   d_ids[n]: ids (ranks or specials).  d_out[cap]: receives the bytes of each
  *   id in turn.  h_len: the total byte length (also when it exceeds cap, then

@@ -568,9 +568,10 @@ int64_t orc_safe_chunks_bytes(const uint8_t* s, int64_t n, int64_t* byte_starts)
 }
 
 /* ------------------------------------------------------------------------- */
-/* Decode ([TT] "The byte floor": round trips are exact at the byte level;    */
-/* "Pitfalls": decode bytes, not pieces).  Writes the bytes of each id in     */
-/* turn; *len receives the total even if it exceeds cap.                      */
+/* Decode ([TT] "The byte floor": a round trip reproduces the input byte for */
+/* byte; "Pitfalls that bite in production": a character's bytes may span     */
+/* several ids, so the output is all ids' bytes concatenated).  Writes the    */
+/* bytes of each id in turn; *len receives the total even if it exceeds cap.  */
 
 int orc_decode(const orc_enc* E, const int32_t* ids, int64_t n, uint8_t* out, int64_t cap,
                int64_t* len) {
