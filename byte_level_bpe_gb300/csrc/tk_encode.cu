@@ -304,13 +304,15 @@ __global__ void k_tile_segs(Call c) {
 // Tiles of 4 KiB, 256 threads x 16 bytes, persistent with dynamic tiles.
 
 __global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) {
-  __shared__ uint8_t s_text[TILE + 8];
-  __shared__ uint64_t s_agg[SPLIT_THREADS];
+  constexpr int CB = 16;  // bytes loaded before the tile (a 16-byte aligned window)
+  __shared__ __align__(16) uint8_t s_text[TILE + 2 * CB];
+  __shared__ uint32_t s_head[TILE / 32];  // segment starts (and window cuts in mode 1)
+  __shared__ uint64_t s_wtot[SPLIT_THREADS / 32];
   __shared__ int64_t s_tile;
   __shared__ uint64_t s_carry;
-  __shared__ int64_t s_seg[2];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
+  const bool aligned = ((uintptr_t)c.text & 15) == 0;
   uint64_t* desc = mode == 0 ? c.W.desc_w : c.W.desc_r;
   uint32_t* out = mode == 0 ? c.W.win_cut : c.W.run_cut;
   const int64_t M = mode == 0 ? CHUNK_CHARS : RUN_CHARS;
@@ -320,67 +322,84 @@ __global__ void __launch_bounds__(SPLIT_THREADS) k_chunk_scan(Call c, int mode) 
     const int64_t tile = s_tile;
     if (tile >= ntiles) break;
     const int64_t t0 = tile * TILE;
-    // bytes [t0 - 4, t0 + TILE + 4)
-    for (int x = tid; x < TILE + 8; x += SPLIT_THREADS) s_text[x] = gbyte(c, t0 - 4 + x);
-    if (tid == 0) {
-      s_seg[0] = c.W.tile_segs[4 * tile + 1];
-      s_seg[1] = c.W.tile_segs[4 * tile + 2];
+    // bytes [t0 - CB, t0 + TILE + CB), 16 at a time where they lie in the text
+    for (int v = tid; v < (TILE + 2 * CB) / 16; v += SPLIT_THREADS) {
+      const int64_t p = t0 - CB + 16 * v;
+      if (aligned && p >= 0 && p + 16 <= c.n) {
+        *reinterpret_cast<uint4*>(&s_text[16 * v]) = ld_na_v4(c.text + p);
+      } else {
+        for (int j = 0; j < 16; j++) s_text[16 * v + j] = gbyte(c, p + j);
+      }
+    }
+    // heads known before the scan: segment starts (the text start among
+    // them), and in mode 1 the window cuts
+    for (int i = tid; i < TILE / 32; i += SPLIT_THREADS) {
+      uint32_t v = 0;
+      if (mode == 1 && t0 + 32 * i < c.n) v = c.W.win_cut[(t0 >> 5) + i];
+      s_head[i] = v;
     }
     __syncthreads();
-    const int64_t slo = s_seg[0], shi = s_seg[1];
+    {
+      const int64_t slo = c.W.tile_segs[4 * tile + 1], shi = c.W.tile_segs[4 * tile + 2];
+      for (int64_t sg = slo + tid; sg < shi; sg += SPLIT_THREADS) {
+        const int64_t x = c.seg_off[sg] - t0;
+        if (x >= 0 && x < TILE) atomicOr(&s_head[x >> 5], 1u << (x & 31));
+      }
+      if (tid == 0 && t0 == 0) atomicOr(&s_head[0], 1u);
+    }
+    __syncthreads();
     // per-thread aggregate over its 16 bytes
-    const int xb = 4 + tid * 16;
+    const int xb = CB + tid * 16;
     uint64_t agg = 0;
-    uint64_t heads = 0, starts = 0;  // bit j: byte xb + j is a head / code-point start
+    uint32_t heads = (s_head[tid >> 1] >> (16 * (tid & 1))) & 0xFFFFu;
+    uint32_t starts = 0;  // bit j: byte xb + j is a head / code-point start
     for (int j = 0; j < 16; j++) {
       const int x = xb + j;
       const int64_t pos = t0 + tid * 16 + j;
       if (pos >= c.n) break;
       const uint32_t b = s_text[x];
       if ((b & 0xC0) == 0x80) continue;
-      starts |= 1ull << j;
-      bool head = false;
-      // segment start?
-      for (int64_t s = slo; s < shi && !head; s++) head = c.seg_off[s] == pos;
-      if (!head && pos == 0) head = true;
+      starts |= 1u << j;
+      bool head = (heads >> j) & 1u;
       if (mode == 1 && !head) {
-        if (bit_get(c.W.win_cut, pos)) head = true;
-        else {
-          uint32_t cp, pcp;
-          bool ok;
-          utf8_seq(b, s_text[x + 1], s_text[x + 2], s_text[x + 3], cp, ok);
-          int px = x - 1;
-          while (px > x - 4 && (s_text[px] & 0xC0) == 0x80) px--;
-          utf8_seq(s_text[px], s_text[px + 1], s_text[px + 2], s_text[px + 3], pcp, ok);
-          head = py_isspace(cp) != py_isspace(pcp);
-        }
+        uint32_t cp, pcp;
+        bool ok;
+        utf8_seq(b, s_text[x + 1], s_text[x + 2], s_text[x + 3], cp, ok);
+        int px = x - 1;
+        while (px > x - 4 && (s_text[px] & 0xC0) == 0x80) px--;
+        utf8_seq(s_text[px], s_text[px + 1], s_text[px + 2], s_text[px + 3], pcp, ok);
+        head = py_isspace(cp) != py_isspace(pcp);
+        if (head) heads |= 1u << j;
       }
-      if (head) { heads |= 1ull << j; agg = 1ull << 40; }
+      if (head) agg = 1ull << 40;
       agg += 1;
     }
-    s_agg[tid] = agg;
+    heads &= starts;
+    // exclusive scan of the thread aggregates: warp shuffles, then the warps
+    uint64_t inc = agg;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc = SegCountOp::comb(y, inc);
+    }
+    if (lane == 31) s_wtot[warp] = inc;
     __syncthreads();
     if (tid < 32) {
       uint64_t run = SegCountOp::id();
-      if (tid == 0) {
-        // exclusive combine over the 256 thread aggregates
-        for (int t = 0; t < SPLIT_THREADS; t++) {
-          const uint64_t a = s_agg[t];
-          s_agg[t] = run;
-          run = SegCountOp::comb(run, a);
-        }
-      }
-      run = __shfl_sync(0xffffffffu, run, 0);
+      for (int w = 0; w < SPLIT_THREADS / 32; w++) run = SegCountOp::comb(run, s_wtot[w]);
       if (tid == 0) st_release_u64(&desc[tile], DESC_AGG | run);
       const uint64_t carry = carry_walk_warp<SegCountOp>(desc, tile, run, c.W.status, 2 + mode);
       if (tid == 0) s_carry = carry;
     }
     __syncthreads();
-    uint64_t v = SegCountOp::comb(s_carry, s_agg[tid]);
+    uint64_t pre = s_carry;
+    for (int w = 0; w < warp; w++) pre = SegCountOp::comb(pre, s_wtot[w]);
+    uint64_t e = __shfl_up_sync(0xffffffffu, inc, 1);
+    if (lane == 0) e = SegCountOp::id();
+    const uint64_t v = SegCountOp::comb(pre, e);
     int64_t idx = (int64_t)(v & ((1ull << 40) - 1));
-    for (int j = 0; j < 16; j++) {
-      if (!((starts >> j) & 1)) continue;
-      if ((heads >> j) & 1) idx = 0;
+    for (uint32_t bits = starts; bits; bits &= bits - 1) {
+      const int j = __ffs(bits) - 1;
+      if ((heads >> j) & 1u) idx = 0;
       if (idx > 0 && idx % M == 0) {
         const int64_t pos = t0 + tid * 16 + j;
         atomicOr(&out[pos >> 5], 1u << (pos & 31));
@@ -722,9 +741,18 @@ __device__ bool starts_here(const Win& w, int64_t x, uint8_t kx, uint32_t nidx) 
   }
 }
 
-// Eight bit-planes of four class bytes: bit j of the result is bit i of byte j.
-__device__ __forceinline__ uint32_t gather_plane(uint32_t w, int i) {
-  return (((w >> i) & 0x01010101u) * 0x10204080u) >> 28;
+// The 8x8 bit matrix of eight bytes (byte k = row k) transposed by three
+// delta swaps: afterwards byte i holds bit i of every byte (bit k from byte
+// k), i.e. the eight bit-planes of the eight bytes at once.
+__device__ __forceinline__ uint64_t transpose8x8(uint64_t x) {
+  uint64_t t;
+  t = (x ^ (x >> 7)) & 0x00AA00AA00AA00AAull;
+  x = x ^ t ^ (t << 7);
+  t = (x ^ (x >> 14)) & 0x0000CCCC0000CCCCull;
+  x = x ^ t ^ (t << 14);
+  t = (x ^ (x >> 28)) & 0x00000000F0F0F0F0ull;
+  x = x ^ t ^ (t << 28);
+  return x;
 }
 
 // The start test for 16 ASCII code points at once (window bytes x0 .. x0+15,
@@ -1053,12 +1081,13 @@ __global__ void __launch_bounds__(SPLIT_THREADS, 6) k_split(Call c) {
       }
       if (fast) {
         const uint32_t* kw = reinterpret_cast<const uint32_t*>(&sm.kc[xb - 4]);
+        const uint64_t y0 = transpose8x8(((uint64_t)kw[1] << 32) | kw[0]);
+        const uint64_t y1 = transpose8x8(((uint64_t)kw[3] << 32) | kw[2]);
+        const uint64_t y2 = transpose8x8(((uint64_t)kw[5] << 32) | kw[4]);
 #pragma unroll
-        for (int j = 0; j < 6; j++) {
-          const uint32_t wv = kw[j];
-#pragma unroll
-          for (int i = 0; i < 8; i++) P[i] |= gather_plane(wv, i) << (4 * j);
-        }
+        for (int i = 0; i < 8; i++)
+          P[i] = (uint32_t)((y0 >> (8 * i)) & 0xFFu) | ((uint32_t)((y1 >> (8 * i)) & 0xFFu) << 8) |
+                 ((uint32_t)((y2 >> (8 * i)) & 0xFFu) << 16);
         fast = (P[1] & P[2] & 0xFFFFFFu) == 0;  // no continuation bytes or text end
       }
       if (fast) {
