@@ -1613,6 +1613,326 @@ __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t 
   return n;
 }
 
+// The same rounds over warp-owned chunks, for one CTA of NW warps.  Warp w
+// owns chunk w: its parts sit at the front of a fixed window of cw slots, in
+// text order, and the pair rank of a part is the rank with the next part in
+// text order (the first part of the next non-empty chunk for the last one).
+// A round merges every other pair of rank rs from the start of each run of
+// rs-pairs, up to the first merge that creates a lower-ranked neighbour pair,
+// as above; but each chunk compacts in place (no scan over the CTA), and the
+// chunks without an rs-pair (most of them, in the late rounds of a long
+// piece, which merge a few pairs each) do nothing but keep their minimum
+// rank.  A run of rs-pairs entering a chunk from the chunks before it flips
+// the choices in the chunk's leading run when its length there is odd.
+// Works in the workspace at the piece's byte offset until the parts fit in
+// the CTA's shared memory `sm` (scap parts, CHUNK_PART bytes each), then
+// there; the ids end in arena[s ..].  Returns the number of ids.
+constexpr int CHUNK_PART = 10;  // ids and ranks (4 + 4 bytes), selection and change flags
+template <int NW>
+struct ChunkSh {
+  int cnt[NW], cnt2[NW];   // parts in each chunk (at the round's start / after it)
+  uint32_t mn[NW];         // each chunk's minimum pair rank
+  int lead[NW], tail[NW];  // the chunk's rs-pairs before its first / after its last other pair
+  uint32_t bad[NW];        // the chunk's first merge that stops the round
+  int off[NW + 1];         // chunk offsets in text order
+};
+
+// The part d places after (d > 0) or before (d < 0) part j of chunk w, in
+// text order over the non-empty chunks; false if there is none.
+template <int NW>
+__device__ __forceinline__ bool chunk_step(const int* cnt, int& w, int& j, int d) {
+  for (; d > 0; d--) {
+    if (j + 1 < cnt[w]) { j++; continue; }
+    int v = w + 1;
+    while (v < NW && cnt[v] == 0) v++;
+    if (v >= NW) return false;
+    w = v; j = 0;
+  }
+  for (; d < 0; d++) {
+    if (j > 0) { j--; continue; }
+    int v = w - 1;
+    while (v >= 0 && cnt[v] == 0) v--;
+    if (v < 0) return false;
+    w = v; j = cnt[v] - 1;
+  }
+  return true;
+}
+
+template <int NW>
+__device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm, int64_t scap, ChunkSh<NW>& S) {
+  constexpr int U = 4;
+  constexpr uint32_t NONE = 0xFFFFFFFFu;
+  const int lane = threadIdx.x & 31, w = (int)(threadIdx.x >> 5);
+  const uint32_t lt = (1u << lane) - 1u;
+  const int64_t G = c.gb + s;
+  uint32_t* const out = reinterpret_cast<uint32_t*>(c.W.arena + G);
+  bool on_chip = scap > 0 && n <= scap;
+  uint32_t* ids = on_chip ? reinterpret_cast<uint32_t*>(sm) : c.W.lids2 + G;
+  uint32_t* rk = on_chip ? ids + scap : c.W.lrk + G;
+  uint8_t* sel = on_chip ? reinterpret_cast<uint8_t*>(rk + scap) : c.W.lsel + G;
+  uint8_t* chg = on_chip ? sel + scap : c.W.lchg + G;
+  int cw = (int)((((n + NW - 1) / NW) + 31) & ~(int64_t)31);
+  // chunk minimum of the pair ranks, into S.mn[w]
+  auto chunk_min = [&](int cnt) {
+    uint32_t m = RANK_MAX;
+    for (int j = lane; j < cnt; j += 32) m = min(m, rk[w * cw + j]);
+    m = __reduce_min_sync(0xffffffffu, m);
+    if (lane == 0) S.mn[w] = m;
+  };
+  {
+    const int cnt = (int)max((int64_t)0, min((int64_t)cw, n - (int64_t)w * cw));
+    for (int j = lane; j < cnt; j += 32) {
+      const int64_t i = (int64_t)w * cw + j;
+      const uint32_t b = gbyte(c, s + i);
+      ids[w * cw + j] = __ldg(&c.T.byte_id[b]);
+      rk[w * cw + j] = (i + 1 < n) ? __ldg(&c.T.dense[(b << 8) | gbyte(c, s + i + 1)]) : RANK_MAX;
+    }
+    __syncwarp();
+    chunk_min(cnt);
+    if (lane == 0) S.cnt[w] = cnt;
+  }
+  __syncthreads();
+  for (int64_t round = 0;; round++) {
+    uint32_t rs = RANK_MAX;
+#pragma unroll 8
+    for (int k = 0; k < NW; k++) rs = min(rs, S.mn[k]);
+    if (rs == RANK_MAX) break;
+    const int cnt = S.cnt[w];
+    const bool act = S.mn[w] == rs;
+    const int base = w * cw;
+    // (1) choose every other rs-pair from the start of each run, counting
+    //     runs as if they started in this chunk
+    if (act) {
+      int carry = -1, first_nc = cnt;
+      for (int b0 = 0; b0 < cnt; b0 += 32 * U) {
+        uint32_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int j = b0 + 32 * u + lane;
+          v[u] = j < cnt ? rk[base + j] : rs;
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int b = b0 + 32 * u, j = b + lane;
+          const bool in = j < cnt, cand = in && v[u] == rs;
+          const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
+          const uint32_t before = nm & lt;
+          const int ln = before ? b + 31 - __clz(before) : carry;
+          if (in) sel[base + j] = cand && (((j - ln - 1) & 1) == 0);
+          if (nm) {
+            if (first_nc == cnt) first_nc = b + __ffs(nm) - 1;
+            carry = b + 31 - __clz(nm);
+          }
+        }
+      }
+      if (lane == 0) {
+        S.lead[w] = first_nc;
+        S.tail[w] = cnt - 1 - carry;
+      }
+    }
+    __syncthreads();
+    // (2) a run entering the chunk with an odd length flips its leading run
+    if (act && S.lead[w] > 0) {
+      int run_in = 0;
+      for (int v = w - 1; v >= 0; v--) {
+        if (S.cnt[v] == 0) continue;  // empty chunks are transparent
+        if (S.mn[v] != rs) break;     // no rs-pair there: its last pair ends the run
+        run_in += S.tail[v];
+        if (S.lead[v] != S.cnt[v]) break;
+      }
+      if (run_in & 1) {
+        __syncwarp();
+        for (int j = lane; j < S.lead[w]; j += 32) sel[base + j] ^= 1;
+      }
+    }
+    __syncthreads();
+    // (3) the chunk's first chosen merge that creates a neighbour pair of a
+    //     rank below rs (the one-at-a-time loop would take that pair next)
+    if (act) {
+      uint32_t fb = NONE;
+      for (int b0 = 0; b0 < cnt && fb == NONE; b0 += 32 * U) {
+        uint8_t sv[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int j = b0 + 32 * u + lane;
+          sv[u] = j < cnt ? sel[base + j] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int j = b0 + 32 * u + lane;
+          bool bad = false;
+          if (sv[u]) {
+            uint32_t rl = RANK_MAX, rr = RANK_MAX;
+            if (j >= 2) {
+              rl = pair_rank(c.T, sel[base + j - 2] ? rs : ids[base + j - 1], rs);
+            } else {
+              int pw = w, pj = j;
+              if (chunk_step<NW>(S.cnt, pw, pj, -1)) {
+                int qw = pw, qj = pj;
+                const bool ql = chunk_step<NW>(S.cnt, qw, qj, -1) && S.mn[qw] == rs && sel[qw * cw + qj];
+                rl = pair_rank(c.T, ql ? rs : ids[pw * cw + pj], rs);
+              }
+            }
+            if (j + 2 < cnt) {
+              rr = pair_rank(c.T, rs, ids[base + j + 2]);
+            } else {
+              int qw = w, qj = j;
+              if (chunk_step<NW>(S.cnt, qw, qj, 2)) rr = pair_rank(c.T, rs, ids[qw * cw + qj]);
+            }
+            bad = rl < rs || rr < rs;
+          }
+          const uint32_t bm = __ballot_sync(0xffffffffu, bad);
+          if (bm && fb == NONE) fb = (uint32_t)(b0 + 32 * u + __ffs(bm) - 1);
+        }
+      }
+      if (lane == 0) S.bad[w] = fb;
+    }
+    __syncthreads();
+    // the round's limit: merges at (chunk, index) <= (lw, lj) go ahead
+    int lw = NW;
+    uint32_t lj = 0;
+    for (int k = 0; k < NW; k++)
+      if (S.mn[k] == rs && S.bad[k] != NONE) {
+        lw = k;
+        lj = S.bad[k];
+        break;
+      }
+    auto allowed = [&](int v, int j) { return v < lw || (v == lw && (uint32_t)j <= lj); };
+    // (4) merge: each chunk compacts in place.  A chunk changes when it holds
+    //     a chosen merge or its first part is taken by the chunk before it.
+    bool first_gone = false;
+    if (cnt > 0) {
+      int pw = w, pj = 0;
+      if (chunk_step<NW>(S.cnt, pw, pj, -1))
+        first_gone = S.mn[pw] == rs && sel[pw * cw + pj] && allowed(pw, pj);
+    }
+    const bool moves = act || first_gone;
+    int cnt2 = cnt;
+    if (moves) {
+      int dst = 0;
+      uint8_t prev = first_gone ? 1 : 0;  // chosen flag of the pair before the strip's lane 0
+      for (int b0 = 0; b0 < cnt; b0 += 32 * U) {
+        uint32_t iv[U], rv[U];
+        uint8_t sv[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int j = b0 + 32 * u + lane;
+          const bool in = j < cnt;
+          iv[u] = in ? ids[base + j] : 0u;
+          rv[u] = in ? rk[base + j] : 0u;
+          sv[u] = (in && act) ? sel[base + j] : 0;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int j = b0 + 32 * u + lane;
+          const bool in = j < cnt;
+          // the pair before part j merged: part j is taken into it
+          const uint8_t up = (uint8_t)__shfl_up_sync(0xffffffffu, (uint32_t)sv[u], 1);
+          const bool gone = lane == 0 ? (j == 0 ? first_gone : (prev && allowed(w, j - 1)))
+                                      : (up && allowed(w, j - 1));
+          const bool kp = in && !gone;
+          const uint32_t km = __ballot_sync(0xffffffffu, kp);
+          if (kp) {
+            const int pos = dst + __popc(km & lt);
+            const bool merged = sv[u] && allowed(w, j);
+            ids[base + pos] = merged ? rs : iv[u];
+            rk[base + pos] = rv[u];
+            chg[base + pos] = merged;
+          }
+          dst += __popc(km);
+          prev = (uint8_t)__shfl_sync(0xffffffffu, (uint32_t)sv[u], 31);
+        }
+        __syncwarp();
+      }
+      cnt2 = dst;
+    }
+    if (lane == 0) S.cnt2[w] = cnt2;
+    __syncthreads();
+    // (5) re-rank the pairs of merged parts and of the parts before them
+    if (moves) {
+      for (int j = lane; j < cnt2; j += 32) {
+        if (!chg[base + j]) continue;
+        const uint32_t x = ids[base + j];
+        int qw = w, qj = j;
+        rk[base + j] = chunk_step<NW>(S.cnt2, qw, qj, 1) ? pair_rank(c.T, x, ids[qw * cw + qj]) : RANK_MAX;
+        int pw = w, pj = j;
+        if (chunk_step<NW>(S.cnt2, pw, pj, -1)) rk[pw * cw + pj] = pair_rank(c.T, ids[pw * cw + pj], x);
+      }
+    }
+    __syncthreads();
+    // (6) new minima: the chunks that moved and the non-empty chunk before each
+    //     (only a chunk with a chosen pair writes ranks: its merged parts')
+    bool dirty = moves;
+    if (!dirty && cnt2 > 0) {
+      for (int v = w + 1; v < NW; v++) {
+        if (S.cnt2[v] == 0) continue;
+        dirty = S.mn[v] == rs;
+        break;
+      }
+    }
+    __syncthreads();  // every warp has read the old minima and counts
+    if (dirty) chunk_min(cnt2);
+    if (lane == 0) S.cnt[w] = cnt2;
+    if (round > n) {  // every round merges at least one pair
+      if (threadIdx.x == 0) set_error(c.W.status, TK_E_LIMIT, 6);
+      __syncthreads();
+      break;
+    }
+    __syncthreads();
+    // once the parts fit, the rest of the rounds run in shared memory
+    if (!on_chip && scap > 0) {
+      if (threadIdx.x == 0) {
+        int t = 0;
+        for (int k = 0; k < NW; k++) {
+          S.off[k] = t;
+          t += S.cnt[k];
+        }
+        S.off[NW] = t;
+      }
+      __syncthreads();
+      const int tot = S.off[NW];
+      if (tot <= scap) {
+        uint32_t* ids2 = reinterpret_cast<uint32_t*>(sm);
+        uint32_t* rk2 = ids2 + scap;
+        const int c0 = S.cnt[w], o0 = S.off[w];
+        for (int j = lane; j < c0; j += 32) {
+          ids2[o0 + j] = ids[base + j];
+          rk2[o0 + j] = rk[base + j];
+        }
+        on_chip = true;
+        ids = ids2;
+        rk = rk2;
+        sel = reinterpret_cast<uint8_t*>(rk + scap);
+        chg = sel + scap;
+        cw = (((tot + NW - 1) / NW) + 31) & ~31;
+        __syncthreads();
+        const int cn = max(0, min(cw, tot - w * cw));
+        chunk_min(cn);
+        if (lane == 0) S.cnt[w] = cn;
+        __syncthreads();
+      }
+    }
+  }
+  // the chunks in text order to arena[s ..]
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int k = 0; k < NW; k++) {
+      S.off[k] = t;
+      t += S.cnt[k];
+    }
+    S.off[NW] = t;
+  }
+  __syncthreads();
+  {
+    const int c0 = S.cnt[w], o0 = S.off[w];
+    for (int j = lane; j < c0; j += 32) out[o0 + j] = ids[w * cw + j];
+  }
+  const int64_t total = S.off[NW];
+  __syncthreads();
+  return total;
+}
+
 // --------------------------------------------------------------------------
 // Fused encode of one 4 KiB tile: the pre-tokens of up to MID_MIN - 1 bytes
 // that start in the tile are merged here (one thread each), their ids
@@ -2660,10 +2980,14 @@ __device__ int merge_warp(const Call& c, int64_t s, int n, uint32_t* dst) {
 // ids -> arena[start ..], count -> cnt[start].
 constexpr int BIG_THREADS = 1024;
 constexpr int64_t BIG_FIRST = 8192;
+// Parts a big merge holds in shared memory: its rounds move there once the
+// piece has shrunk to this many parts (at once for pieces this short).
+constexpr int64_t BIG_SCAP = 23000;
+constexpr int BIG_SMEM = (int)(BIG_SCAP * CHUNK_PART);
 __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
-  __shared__ int64_t red64[BIG_THREADS / 32];
-  __shared__ uint32_t red32[BIG_THREADS / 32];
+  __shared__ ChunkSh<BIG_THREADS / 32> s_ch;
   __shared__ uint32_t s_idx;
+  extern __shared__ __align__(16) uint8_t s_parts[];
   const int tid = threadIdx.x;
   const uint32_t n_big = c.W.status->n_biglong;
   // two passes over the list, pieces over BIG_FIRST bytes first, so that no
@@ -2679,7 +3003,7 @@ __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
       const int64_t p = c.W.big_list[2 * k], len = c.W.big_list[2 * k + 1];
       if ((len > BIG_FIRST) != (pass == 0)) continue;
       if (c.W.gsrc[c.gb + p] != (uint32_t)(c.gb + p)) continue;  // a copy: uses its owner's ids
-      const int64_t m = merge_rounds(c, RGroup<BIG_THREADS / 32>{red64, red32}, p, len);
+      const int64_t m = merge_chunks<BIG_THREADS / 32>(c, p, len, s_parts, BIG_SCAP, s_ch);
       if (tid == 0) c.W.cnt[c.gb + p] = (uint32_t)m;
     }
   }
@@ -3175,7 +3499,9 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     tk_prof_mark(ws, nullptr, ws->s_med);
     TK_CUDA(cudaEventRecord(ws->ev_med, ws->s_med), "join");
     tk_prof_mark(ws, "k_merge_big", side);
-    k_merge_big<<<sms, BIG_THREADS, 0, side>>>(c);
+    TK_CUDA(cudaFuncSetAttribute(k_merge_big, cudaFuncAttributeMaxDynamicSharedMemorySize, BIG_SMEM),
+            "smem attribute");
+    k_merge_big<<<sms, BIG_THREADS, BIG_SMEM, side>>>(c);
     tk_prof_mark(ws, nullptr, side);
     TK_CUDA(cudaStreamWaitEvent(side, ws->ev_cl, 0), "join");
     TK_CUDA(cudaStreamWaitEvent(side, ws->ev_med, 0), "join");

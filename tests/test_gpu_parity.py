@@ -492,3 +492,22 @@ def test_big_mixed_white_space_pieces(full_gpu, full_enc):
     segs.append(("q" + "ab" * 900 + " " + "\t" * 1200, False))
     _compare(full_gpu, full_enc, segs, False)
     _compare(full_gpu, full_enc, segs, True)
+
+
+def test_big_pieces_chunk_edges(full_gpu, full_enc):
+    """Pre-tokens of 1,025-32,768 bytes merged by one CTA over warp-owned
+    chunks: lengths around the chunk and shared-memory sizes (one repeated
+    letter), runs of pairs of one rank crossing chunk ends ("ab..."), and
+    random letters of a small alphabet, whose rounds merge a few pairs each
+    and stop early at lower-ranked neighbour pairs."""
+    rng = np.random.default_rng(29)
+    segs = []
+    for n in (1025, 1056, 1057, 2049, 4097, 22990, 23010, 32768):
+        segs.append((" " + "a" * (n - 1), False))
+    for n in (1100, 3001, 7777):
+        segs.append(("ab" * (n // 2) + "a", False))
+        segs.append(("abc" * (n // 3), False))
+    for alpha, n in (("etaoin", 1100), ("etaoin", 3000), ("ab", 4000), ("aeiost", 9000)):
+        letters = np.array(list(alpha))
+        segs.append(("".join(letters[rng.integers(0, len(letters), n)]), False))
+    _compare(full_gpu, full_enc, segs, False)
