@@ -1508,8 +1508,10 @@ __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t 
     }
     g.sync();
     // (3) the first selected merge that creates a neighbour pair of lower rank
+    //     (only possible when the token rs has an extension ranked below it)
+    const uint32_t xf = __ldg(&c.T.ext_low[rs]);
     uint32_t fb = 0xFFFFFFFFu;
-    for (int64_t b0 = wlo; b0 < whi && fb == 0xFFFFFFFFu; b0 += 32 * U) {
+    for (int64_t b0 = wlo; xf && b0 < whi && fb == 0xFFFFFFFFu; b0 += 32 * U) {
       uint8_t sv[U];
 #pragma unroll
       for (int u = 0; u < U; u++) {
@@ -1531,7 +1533,7 @@ __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t 
         if (bm && fb == 0xFFFFFFFFu) fb = (uint32_t)(b0 + 32 * u + __ffs(bm) - 1);
       }
     }
-    const uint32_t limit = g.gmin(fb);
+    const uint32_t limit = xf ? g.gmin(fb) : 0xFFFFFFFFu;
     // (4) merge the selected pairs up to limit, compacting into B
     int64_t keep_w = 0;
     for (int64_t b0 = wlo; b0 < whi; b0 += 32 * U) {
@@ -1627,7 +1629,7 @@ __device__ int64_t merge_rounds(const Call& c, const Grp& g, int64_t s, int64_t 
 // Works in the workspace at the piece's byte offset until the parts fit in
 // the CTA's shared memory `sm` (scap parts, CHUNK_PART bytes each), then
 // there; the ids end in arena[s ..].  Returns the number of ids.
-constexpr int CHUNK_PART = 10;  // ids and ranks (4 + 4 bytes), selection and change flags
+constexpr int CHUNK_PART = 9;  // id and rank (4 + 4 bytes), chosen / merged flag
 template <int NW>
 struct ChunkSh {
   int cnt[NW], cnt2[NW];   // parts in each chunk (at the round's start / after it)
@@ -1670,7 +1672,6 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
   uint32_t* ids = on_chip ? reinterpret_cast<uint32_t*>(sm) : c.W.lids2 + G;
   uint32_t* rk = on_chip ? ids + scap : c.W.lrk + G;
   uint8_t* sel = on_chip ? reinterpret_cast<uint8_t*>(rk + scap) : c.W.lsel + G;
-  uint8_t* chg = on_chip ? sel + scap : c.W.lchg + G;
   int cw = (int)((((n + NW - 1) / NW) + 31) & ~(int64_t)31);
   // chunk minimum of the pair ranks, into S.mn[w]
   auto chunk_min = [&](int cnt) {
@@ -1747,8 +1748,13 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
     }
     __syncthreads();
     // (3) the chunk's first chosen merge that creates a neighbour pair of a
-    //     rank below rs (the one-at-a-time loop would take that pair next)
-    if (act) {
+    //     rank below rs (the one-at-a-time loop would take that pair next);
+    //     the neighbours' first probes of a batch are loaded together.  Only
+    //     a token rs with an extension that ranks below it can do that.
+    const uint32_t xf = __ldg(&c.T.ext_low[rs]);
+    int lw = NW;
+    uint32_t lj = 0;
+    if (xf && act) {
       uint32_t fb = NONE;
       for (int b0 = 0; b0 < cnt && fb == NONE; b0 += 32 * U) {
         uint8_t sv[U];
@@ -1757,55 +1763,71 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
           const int j = b0 + 32 * u + lane;
           sv[u] = j < cnt ? sel[base + j] : 0;
         }
+        PairProbe pl[U], pq[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
           const int j = b0 + 32 * u + lane;
-          bool bad = false;
+          uint32_t left = 0, right = 0;
+          bool hl = false, hr = false;
           if (sv[u]) {
-            uint32_t rl = RANK_MAX, rr = RANK_MAX;
+            // the part before j, or rs when the pair before that one is chosen
+            // (it merges first); the part two after j
             if (j >= 2) {
-              rl = pair_rank(c.T, sel[base + j - 2] ? rs : ids[base + j - 1], rs);
+              hl = true;
+              left = sel[base + j - 2] ? rs : ids[base + j - 1];
             } else {
               int pw = w, pj = j;
               if (chunk_step<NW>(S.cnt, pw, pj, -1)) {
                 int qw = pw, qj = pj;
                 const bool ql = chunk_step<NW>(S.cnt, qw, qj, -1) && S.mn[qw] == rs && sel[qw * cw + qj];
-                rl = pair_rank(c.T, ql ? rs : ids[pw * cw + pj], rs);
+                hl = true;
+                left = ql ? rs : ids[pw * cw + pj];
               }
             }
             if (j + 2 < cnt) {
-              rr = pair_rank(c.T, rs, ids[base + j + 2]);
+              hr = true;
+              right = ids[base + j + 2];
             } else {
               int qw = w, qj = j;
-              if (chunk_step<NW>(S.cnt, qw, qj, 2)) rr = pair_rank(c.T, rs, ids[qw * cw + qj]);
+              if (chunk_step<NW>(S.cnt, qw, qj, 2)) {
+                hr = true;
+                right = ids[qw * cw + qj];
+              }
             }
-            bad = rl < rs || rr < rs;
           }
+          pl[u] = pair_first(c.T, left, rs, hl);
+          pq[u] = pair_first(c.T, rs, right, hr);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const bool bad = sv[u] && (pair_finish(c.T, pl[u]) < rs || pair_finish(c.T, pq[u]) < rs);
           const uint32_t bm = __ballot_sync(0xffffffffu, bad);
           if (bm && fb == NONE) fb = (uint32_t)(b0 + 32 * u + __ffs(bm) - 1);
         }
       }
       if (lane == 0) S.bad[w] = fb;
     }
-    __syncthreads();
     // the round's limit: merges at (chunk, index) <= (lw, lj) go ahead
-    int lw = NW;
-    uint32_t lj = 0;
-    for (int k = 0; k < NW; k++)
-      if (S.mn[k] == rs && S.bad[k] != NONE) {
-        lw = k;
-        lj = S.bad[k];
-        break;
-      }
+    if (xf) {
+      __syncthreads();
+      for (int k = 0; k < NW; k++)
+        if (S.mn[k] == rs && S.bad[k] != NONE) {
+          lw = k;
+          lj = S.bad[k];
+          break;
+        }
+    }
     auto allowed = [&](int v, int j) { return v < lw || (v == lw && (uint32_t)j <= lj); };
-    // (4) merge: each chunk compacts in place.  A chunk changes when it holds
-    //     a chosen merge or its first part is taken by the chunk before it.
+    // (4) merge: each chunk compacts in place, the merged flags replacing
+    //     the chosen ones in sel.  A chunk changes when it holds a chosen
+    //     merge or its first part is taken by the chunk before it.
     bool first_gone = false;
     if (cnt > 0) {
       int pw = w, pj = 0;
       if (chunk_step<NW>(S.cnt, pw, pj, -1))
         first_gone = S.mn[pw] == rs && sel[pw * cw + pj] && allowed(pw, pj);
     }
+    __syncthreads();  // every chunk's last chosen flag is read
     const bool moves = act || first_gone;
     int cnt2 = cnt;
     if (moves) {
@@ -1838,7 +1860,7 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
             const bool merged = sv[u] && allowed(w, j);
             ids[base + pos] = merged ? rs : iv[u];
             rk[base + pos] = rv[u];
-            chg[base + pos] = merged;
+            sel[base + pos] = merged;
           }
           dst += __popc(km);
           prev = (uint8_t)__shfl_sync(0xffffffffu, (uint32_t)sv[u], 31);
@@ -1850,14 +1872,45 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
     if (lane == 0) S.cnt2[w] = cnt2;
     __syncthreads();
     // (5) re-rank the pairs of merged parts and of the parts before them
+    //     (first probes of a batch loaded together)
     if (moves) {
-      for (int j = lane; j < cnt2; j += 32) {
-        if (!chg[base + j]) continue;
-        const uint32_t x = ids[base + j];
-        int qw = w, qj = j;
-        rk[base + j] = chunk_step<NW>(S.cnt2, qw, qj, 1) ? pair_rank(c.T, x, ids[qw * cw + qj]) : RANK_MAX;
-        int pw = w, pj = j;
-        if (chunk_step<NW>(S.cnt2, pw, pj, -1)) rk[pw * cw + pj] = pair_rank(c.T, ids[pw * cw + pj], x);
+      for (int j0 = 0; j0 < cnt2; j0 += 32 * U) {
+        bool mg[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int j = j0 + 32 * u + lane;
+          mg[u] = j < cnt2 && sel[base + j];
+        }
+        PairProbe pn[U], pp[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int j = j0 + 32 * u + lane;
+          uint32_t x = 0, nxt = 0, prv = 0;
+          bool hn = false, hp = false;
+          if (mg[u]) {
+            x = ids[base + j];
+            int qw = w, qj = j;
+            if (chunk_step<NW>(S.cnt2, qw, qj, 1)) {
+              hn = true;
+              nxt = ids[qw * cw + qj];
+            }
+            int pw = w, pj = j;
+            if (chunk_step<NW>(S.cnt2, pw, pj, -1)) {
+              hp = true;
+              prv = ids[pw * cw + pj];
+            }
+          }
+          pn[u] = pair_first(c.T, x, nxt, hn);  // unused probes resolve to RANK_MAX
+          pp[u] = pair_first(c.T, prv, x, hp);
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          if (!mg[u]) continue;
+          const int j = j0 + 32 * u + lane;
+          rk[base + j] = pair_finish(c.T, pn[u]);
+          int pw = w, pj = j;
+          if (chunk_step<NW>(S.cnt2, pw, pj, -1)) rk[pw * cw + pj] = pair_finish(c.T, pp[u]);
+        }
       }
     }
     __syncthreads();
@@ -1904,7 +1957,6 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
         ids = ids2;
         rk = rk2;
         sel = reinterpret_cast<uint8_t*>(rk + scap);
-        chg = sel + scap;
         cw = (((tot + NW - 1) / NW) + 31) & ~31;
         __syncthreads();
         const int cn = max(0, min(cw, tot - w * cw));
@@ -2982,7 +3034,7 @@ constexpr int BIG_THREADS = 1024;
 constexpr int64_t BIG_FIRST = 8192;
 // Parts a big merge holds in shared memory: its rounds move there once the
 // piece has shrunk to this many parts (at once for pieces this short).
-constexpr int64_t BIG_SCAP = 23000;
+constexpr int64_t BIG_SCAP = 25600;
 constexpr int BIG_SMEM = (int)(BIG_SCAP * CHUNK_PART);
 __global__ void __launch_bounds__(BIG_THREADS) k_merge_big(Call c) {
   __shared__ ChunkSh<BIG_THREADS / 32> s_ch;

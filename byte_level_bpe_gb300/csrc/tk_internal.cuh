@@ -78,6 +78,8 @@ struct Tables {
   const uint64_t* pair_slots;  // open addressing: (a << 40) | (b << 20) | rank; empty = ~0
   uint32_t pair_log2;          // log2(number of slots)
   uint32_t pair_max_probe;     // longest probe sequence present in the table
+  const uint8_t* ext_low;      // [max_id + 1] bit 0: a token a||x ranks below x; bit 1:
+                               // a token x||b does (x = the id; a, b tokens)
   const uint64_t* s34_slots;   // open addressing over the 3- and 4-byte tokens:
                                // (bytes << 21) | (len == 4) << 20 | rank; empty = ~0
   uint32_t s34_log2;
@@ -333,6 +335,34 @@ __device__ __forceinline__ uint32_t pair_rank(const TT& T, uint32_t a, uint32_t 
     if (s == ~0ull) return RANK_MAX;
     if ((s >> 20) == key) return (uint32_t)(s & 0xFFFFF);
     h = (h + 1) & mask;
+  }
+  return RANK_MAX;
+}
+
+// The same lookup in two steps, so that a thread can have several first
+// probes in flight: pair_first loads the first slot (none when `use` is
+// false), pair_finish resolves it, probing on past a collision.
+struct PairProbe {
+  uint64_t s, key;
+};
+template <class TT>
+__device__ __forceinline__ PairProbe pair_first(const TT& T, uint32_t a, uint32_t b, bool use) {
+  PairProbe p;
+  p.key = ((uint64_t)a << 20) | b;
+  p.s = use ? __ldg(&T.pair_slots[(p.key * 0x9E3779B97F4A7C15ull) >> (64 - T.pair_log2)]) : ~0ull;
+  return p;
+}
+template <class TT>
+__device__ __forceinline__ uint32_t pair_finish(const TT& T, PairProbe p) {
+  if (p.s == ~0ull) return RANK_MAX;
+  if ((p.s >> 20) == p.key) return (uint32_t)(p.s & 0xFFFFF);
+  const uint64_t mask = (1ull << T.pair_log2) - 1;
+  uint64_t h = (p.key * 0x9E3779B97F4A7C15ull) >> (64 - T.pair_log2);
+  for (uint32_t probe = 1; probe <= T.pair_max_probe; probe++) {
+    h = (h + 1) & mask;
+    const uint64_t s = __ldg(&T.pair_slots[h]);
+    if (s == ~0ull) return RANK_MAX;
+    if ((s >> 20) == p.key) return (uint32_t)(s & 0xFFFFF);
   }
   return RANK_MAX;
 }

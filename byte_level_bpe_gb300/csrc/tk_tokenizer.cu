@@ -199,6 +199,14 @@ extern "C" int tk_load(const uint8_t* rank_bytes, const int64_t* rank_off, const
       pairs.emplace_back(((uint64_t)a->second << 20) | b->second, rank_ids[i]);
     }
   }
+  // tokens with an extension that ranks below them: only a merge into such a
+  // token can create a neighbour pair below the round's rank
+  std::vector<uint8_t> ext_low((size_t)max_id + 1, 0);
+  for (auto& kv : pairs) {
+    const uint32_t a = (uint32_t)(kv.first >> 20), b = (uint32_t)(kv.first & 0xFFFFF);
+    if (kv.second < b) ext_low[b] |= 1;
+    if (kv.second < a) ext_low[a] |= 2;
+  }
   uint32_t log2cap = 10;
   while ((1ull << log2cap) < 2 * pairs.size() + 16) log2cap++;
   std::vector<uint64_t> slots(1ull << log2cap, ~0ull);
@@ -269,6 +277,7 @@ extern "C" int tk_load(const uint8_t* rank_bytes, const int64_t* rank_off, const
   rc = rc ? rc : upload(tok, byte_id, 256, &t.byte_id);
   rc = rc ? rc : upload(tok, dense.data(), dense.size(), &t.dense);
   rc = rc ? rc : upload(tok, slots.data(), slots.size(), &t.pair_slots);
+  rc = rc ? rc : upload(tok, ext_low.data(), ext_low.size(), &t.ext_low);
   rc = rc ? rc : upload(tok, s34.data(), s34.size(), &t.s34_slots);
   rc = rc ? rc : upload(tok, sbytes.data(), sbytes.size(), &t.spec_bytes);
   rc = rc ? rc : upload(tok, soff.data(), soff.size(), &t.spec_off);

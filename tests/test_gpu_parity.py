@@ -511,3 +511,44 @@ def test_big_pieces_chunk_edges(full_gpu, full_enc):
         letters = np.array(list(alpha))
         segs.append(("".join(letters[rng.integers(0, len(letters), n)]), False))
     _compare(full_gpu, full_enc, segs, False)
+
+
+def _shuffled_ab_table(seed):
+    """The 256 bytes, then tokens over {a, b} of 2-8 bytes built from pairs of
+    earlier tokens, in a shuffled rank order: many tokens then have an
+    extension (a token a||x or x||b) ranked below them, so the exact rounds'
+    stop rule fires."""
+    rng = np.random.default_rng(seed)
+    toks = [b"a", b"b"]
+    seen = set(toks)
+    while len(toks) < 300:
+        t = toks[int(rng.integers(0, len(toks)))] + toks[int(rng.integers(0, len(toks)))]
+        if len(t) <= 8 and t not in seen:
+            seen.add(t)
+            toks.append(t)
+    multi = toks[2:]
+    order = rng.permutation(len(multi))
+    return [bytes([i]) for i in range(256)] + [multi[k] for k in order]
+
+
+def test_long_pieces_stop_rule():
+    """Pre-tokens of random a/b letters over a table with shuffled ranks, at
+    the lengths of every round-merge path (a warp: 129-1,024 bytes; a CTA over
+    chunks: 1,025-32,768; an 8-CTA cluster: longer): rounds stop at merges that
+    create lower-ranked neighbour pairs."""
+    import byte_level_bpe_gb300 as tk
+    table = _shuffled_ab_table(31)
+    rank = {t: i for i, t in enumerate(table)}
+    low = sum(1 for t, r in rank.items() for k in range(1, len(t))
+              if t[:k] in rank and t[k:] in rank and (r < rank[t[k:]] or r < rank[t[:k]]))
+    assert low > 20  # the table exercises the stop rule
+    enc = oracle.Encoding(table, {})
+    gpu = tk.Tokenizer(table, {}, max_bytes=1 << 18, max_segments=64)
+    rng = np.random.default_rng(37)
+    segs = []
+    for n in (200, 700, 1100, 2500, 6000, 23500, 33000):
+        segs.append(("".join(np.array(["a", "b"])[rng.integers(0, 2, n)]), False))
+    segs.append(("ab" * 3000, False))
+    segs.append(("a" * 5000 + "b" * 3000, False))
+    _compare(gpu, enc, segs, False)
+    gpu.close()
