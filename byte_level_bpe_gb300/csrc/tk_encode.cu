@@ -3487,16 +3487,29 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
   tk_prof_mark(ws, "k_check_segments", st);
   k_check_segments<<<seg_grid, 256, 0, st>>>(c);
   if (n > 0) {
-    int split_per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&split_per_sm, k_split, SPLIT_THREADS, 0);
-    const int split_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(split_per_sm, 1));
+    if (ws->split_per_sm == 0) {  // once per workspace: launch shapes and shared-memory limits
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ws->split_per_sm, k_split, SPLIT_THREADS, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ws->scan_per_sm, k_chunk_scan, SPLIT_THREADS, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ws->copy_per_sm, k_copy_out, COPY_THREADS, 0);
+      TK_CUDA(cudaFuncSetAttribute(k_merge_big, cudaFuncAttributeMaxDynamicSharedMemorySize, BIG_SMEM),
+              "smem attribute");
+      TK_CUDA(cudaFuncSetAttribute(k_encode_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)sizeof(EncSmem)), "smem attribute");
+      TK_CUDA(cudaFuncSetAttribute(k_encode_tiles<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)sizeof(EncSmem)), "smem attribute");
+      ws->split_per_sm = std::max(ws->split_per_sm, 1);
+      ws->scan_per_sm = std::max(ws->scan_per_sm, 1);
+      ws->copy_per_sm = std::max(ws->copy_per_sm, 1);
+    }
+    const int split_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * ws->split_per_sm);
+    const int scan_grid = (int)std::min<int64_t>(n_split_tiles, (int64_t)sms * ws->scan_per_sm);
     tk_prof_mark(ws, "k_tile_segs", st);
     k_tile_segs<<<(int)std::min<int64_t>((4 * n_split_tiles + 255) / 256, (int64_t)sms * 8), 256, 0, st>>>(c);
     if (c.safe) {
       tk_prof_mark(ws, "k_chunk_scan_windows", st);
-      k_chunk_scan<<<split_grid, SPLIT_THREADS, 0, st>>>(c, 0);
+      k_chunk_scan<<<scan_grid, SPLIT_THREADS, 0, st>>>(c, 0);
       tk_prof_mark(ws, "k_chunk_scan_runs", st);
-      k_chunk_scan<<<split_grid, SPLIT_THREADS, 0, st>>>(c, 1);
+      k_chunk_scan<<<scan_grid, SPLIT_THREADS, 0, st>>>(c, 1);
     }
     tk_prof_mark(ws, "k_split", st);
     k_split<<<split_grid, SPLIT_THREADS, 0, st>>>(c);
@@ -3551,8 +3564,6 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     tk_prof_mark(ws, nullptr, ws->s_med);
     TK_CUDA(cudaEventRecord(ws->ev_med, ws->s_med), "join");
     tk_prof_mark(ws, "k_merge_big", side);
-    TK_CUDA(cudaFuncSetAttribute(k_merge_big, cudaFuncAttributeMaxDynamicSharedMemorySize, BIG_SMEM),
-            "smem attribute");
     k_merge_big<<<sms, BIG_THREADS, BIG_SMEM, side>>>(c);
     tk_prof_mark(ws, nullptr, side);
     TK_CUDA(cudaStreamWaitEvent(side, ws->ev_cl, 0), "join");
@@ -3563,10 +3574,6 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     }
     tk_prof_mark(ws, nullptr, side);
     TK_CUDA(cudaEventRecord(ws->ev_long, side), "join");
-    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sizeof(EncSmem)), "smem attribute");
-    TK_CUDA(cudaFuncSetAttribute(k_encode_tiles<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sizeof(EncSmem)), "smem attribute");
     tk_prof_mark(ws, "k_encode_tiles", st);
     if (c.W.mid_side) k_encode_tiles<false><<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
     else k_encode_tiles<true><<<(int)n_split_tiles, ETHREADS, sizeof(EncSmem), st>>>(c);
@@ -3579,9 +3586,7 @@ static int encode_launch(const tk_tokenizer* tok, tk_workspace* ws, const uint8_
     int rc = tk_scan_u32(ws, ws->w.tile_count, ws->w.tile_base, &ws->w.status->n_tiles, n_split_tiles, 3, st);
     if (rc) return rc;
     tk_prof_mark(ws, "k_copy_out", st);
-    int copy_per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&copy_per_sm, k_copy_out, COPY_THREADS, 0);
-    k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * std::max(copy_per_sm, 1)), COPY_THREADS, 0,
+    k_copy_out<<<(int)std::min<int64_t>(n_split_tiles, (int64_t)sms * ws->copy_per_sm), COPY_THREADS, 0,
                  st>>>(c, d_out, cap);
     tk_prof_mark(ws, "k_copy_huge", st);
     k_copy_huge<<<sms * 4, ETHREADS, 0, st>>>(c, d_out, cap);

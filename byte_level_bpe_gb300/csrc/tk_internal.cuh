@@ -431,6 +431,7 @@ struct tk_workspace {
   void* dev_mem[MAX_DEV];
   int n_dev;
   tk::Status* h_status;     // pinned host copy of the status block
+  int split_per_sm, scan_per_sm, copy_per_sm;  // resident CTAs per SM (0: not queried yet)
   uint8_t* d_stage_text;    // staging for tk_encode_segments_host
   int64_t* d_stage_off;
   uint8_t* d_stage_allow;
