@@ -1673,12 +1673,40 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
   uint32_t* rk = on_chip ? ids + scap : c.W.lrk + G;
   uint8_t* sel = on_chip ? reinterpret_cast<uint8_t*>(rk + scap) : c.W.lsel + G;
   int cw = (int)((((n + NW - 1) / NW) + 31) & ~(int64_t)31);
-  // chunk minimum of the pair ranks, into S.mn[w]
-  auto chunk_min = [&](int cnt) {
+  // the chunk's minimum pair rank and its pairs of that rank before the first
+  // and after the last other pair, into S.mn / S.lead / S.tail
+  auto chunk_stats = [&](int cnt) {
     uint32_t m = RANK_MAX;
     for (int j = lane; j < cnt; j += 32) m = min(m, rk[w * cw + j]);
     m = __reduce_min_sync(0xffffffffu, m);
-    if (lane == 0) S.mn[w] = m;
+    int first = cnt, last = -1;
+    if (m != RANK_MAX) {
+      for (int b0 = 0; b0 < cnt; b0 += 32) {
+        const int j = b0 + lane;
+        const uint32_t ne = __ballot_sync(0xffffffffu, j < cnt && rk[w * cw + j] != m);
+        if (ne) {
+          if (first == cnt) first = b0 + __ffs(ne) - 1;
+          last = b0 + 31 - __clz(ne);
+        }
+      }
+    }
+    if (lane == 0) {
+      S.mn[w] = m;
+      S.lead[w] = first;
+      S.tail[w] = cnt - 1 - last;
+    }
+  };
+  // length of the run of rs-pairs that ends just before chunk v (rs: the
+  // minimum of every chunk it crosses; empty chunks are transparent)
+  auto run_into = [&](int v, uint32_t rs) {
+    int r = 0;
+    for (int u = v - 1; u >= 0; u--) {
+      if (S.cnt[u] == 0) continue;
+      if (S.mn[u] != rs) break;
+      r += S.tail[u];
+      if (S.lead[u] != S.cnt[u]) break;
+    }
+    return r;
   };
   {
     const int cnt = (int)max((int64_t)0, min((int64_t)cw, n - (int64_t)w * cw));
@@ -1689,126 +1717,177 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
       rk[w * cw + j] = (i + 1 < n) ? __ldg(&c.T.dense[(b << 8) | gbyte(c, s + i + 1)]) : RANK_MAX;
     }
     __syncwarp();
-    chunk_min(cnt);
+    chunk_stats(cnt);
     if (lane == 0) S.cnt[w] = cnt;
   }
   __syncthreads();
   for (int64_t round = 0;; round++) {
-    uint32_t rs = RANK_MAX;
-#pragma unroll 8
-    for (int k = 0; k < NW; k++) rs = min(rs, S.mn[k]);
+    static_assert(NW <= 32, "one chunk minimum per lane");
+    const uint32_t rs = __reduce_min_sync(0xffffffffu, lane < NW ? S.mn[lane] : RANK_MAX);
     if (rs == RANK_MAX) break;
     const int cnt = S.cnt[w];
     const bool act = S.mn[w] == rs;
     const int base = w * cw;
-    // (1) choose every other rs-pair from the start of each run, counting
-    //     runs as if they started in this chunk
-    if (act) {
-      int carry = -1, first_nc = cnt;
-      for (int b0 = 0; b0 < cnt; b0 += 32 * U) {
-        uint32_t v[U];
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-          const int j = b0 + 32 * u + lane;
-          v[u] = j < cnt ? rk[base + j] : rs;
-        }
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-          const int b = b0 + 32 * u, j = b + lane;
-          const bool in = j < cnt, cand = in && v[u] == rs;
-          const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
-          const uint32_t before = nm & lt;
-          const int ln = before ? b + 31 - __clz(before) : carry;
-          if (in) sel[base + j] = cand && (((j - ln - 1) & 1) == 0);
-          if (nm) {
-            if (first_nc == cnt) first_nc = b + __ffs(nm) - 1;
-            carry = b + 31 - __clz(nm);
-          }
-        }
-      }
-      if (lane == 0) {
-        S.lead[w] = first_nc;
-        S.tail[w] = cnt - 1 - carry;
-      }
-    }
-    __syncthreads();
-    // (2) a run entering the chunk with an odd length flips its leading run
-    if (act && S.lead[w] > 0) {
-      int run_in = 0;
-      for (int v = w - 1; v >= 0; v--) {
-        if (S.cnt[v] == 0) continue;  // empty chunks are transparent
-        if (S.mn[v] != rs) break;     // no rs-pair there: its last pair ends the run
-        run_in += S.tail[v];
-        if (S.lead[v] != S.cnt[v]) break;
-      }
-      if (run_in & 1) {
-        __syncwarp();
-        for (int j = lane; j < S.lead[w]; j += 32) sel[base + j] ^= 1;
-      }
-    }
-    __syncthreads();
-    // (3) the chunk's first chosen merge that creates a neighbour pair of a
-    //     rank below rs (the one-at-a-time loop would take that pair next);
-    //     the neighbours' first probes of a batch are loaded together.  Only
-    //     a token rs with an extension that ranks below it can do that.
+    // Only a token rs with an extension that ranks below it can stop a round
+    // early; without one, a round chooses and merges in one pass per chunk.
     const uint32_t xf = __ldg(&c.T.ext_low[rs]);
-    int lw = NW;
-    uint32_t lj = 0;
-    if (xf && act) {
-      uint32_t fb = NONE;
-      for (int b0 = 0; b0 < cnt && fb == NONE; b0 += 32 * U) {
-        uint8_t sv[U];
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-          const int j = b0 + 32 * u + lane;
-          sv[u] = j < cnt ? sel[base + j] : 0;
-        }
-        PairProbe pl[U], pq[U];
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-          const int j = b0 + 32 * u + lane;
-          uint32_t left = 0, right = 0;
-          bool hl = false, hr = false;
-          if (sv[u]) {
-            // the part before j, or rs when the pair before that one is chosen
-            // (it merges first); the part two after j
-            if (j >= 2) {
-              hl = true;
-              left = sel[base + j - 2] ? rs : ids[base + j - 1];
-            } else {
-              int pw = w, pj = j;
-              if (chunk_step<NW>(S.cnt, pw, pj, -1)) {
-                int qw = pw, qj = pj;
-                const bool ql = chunk_step<NW>(S.cnt, qw, qj, -1) && S.mn[qw] == rs && sel[qw * cw + qj];
-                hl = true;
-                left = ql ? rs : ids[pw * cw + pj];
-              }
-            }
-            if (j + 2 < cnt) {
-              hr = true;
-              right = ids[base + j + 2];
-            } else {
-              int qw = w, qj = j;
-              if (chunk_step<NW>(S.cnt, qw, qj, 2)) {
-                hr = true;
-                right = ids[qw * cw + qj];
-              }
-            }
-          }
-          pl[u] = pair_first(c.T, left, rs, hl);
-          pq[u] = pair_first(c.T, rs, right, hr);
-        }
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-          const bool bad = sv[u] && (pair_finish(c.T, pl[u]) < rs || pair_finish(c.T, pq[u]) < rs);
-          const uint32_t bm = __ballot_sync(0xffffffffu, bad);
-          if (bm && fb == NONE) fb = (uint32_t)(b0 + 32 * u + __ffs(bm) - 1);
+    bool moves = act;
+    int cnt2 = cnt;
+    if (!xf) {
+      // whether the chunk's first part is taken by the last pair before it:
+      // that pair is an rs-pair at an even place in its run
+      bool first_gone = false;
+      if (cnt > 0) {
+        int v = w - 1;
+        while (v >= 0 && S.cnt[v] == 0) v--;
+        if (v >= 0 && S.mn[v] == rs && S.tail[v] > 0) {
+          const int at = (S.lead[v] == S.cnt[v] ? run_into(v, rs) : 0) + S.tail[v] - 1;
+          first_gone = (at & 1) == 0;
         }
       }
-      if (lane == 0) S.bad[w] = fb;
-    }
-    // the round's limit: merges at (chunk, index) <= (lw, lj) go ahead
-    if (xf) {
+      moves = act || first_gone;
+      if (moves) {
+        // choose every other rs-pair of each run (counting the run entering
+        // the chunk) and compact in place, the merged flags into sel
+        int carry = -1 - (act && S.lead[w] > 0 ? run_into(w, rs) : 0);
+        int dst = 0;
+        bool prev = first_gone;  // chosen flag of the pair before the strip's lane 0
+        for (int b0 = 0; b0 < cnt; b0 += 32 * U) {
+          uint32_t iv[U], rv[U];
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int j = b0 + 32 * u + lane;
+            const bool in = j < cnt;
+            iv[u] = in ? ids[base + j] : 0u;
+            rv[u] = in ? rk[base + j] : 0u;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int b = b0 + 32 * u, j = b + lane;
+            const bool in = j < cnt, cand = in && rv[u] == rs;
+            const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
+            const uint32_t before = nm & lt;
+            const int ln = before ? b + 31 - __clz(before) : carry;
+            const bool chosen = cand && (((j - ln - 1) & 1) == 0);
+            const bool up = __shfl_up_sync(0xffffffffu, (uint32_t)chosen, 1) != 0;
+            const bool gone = lane == 0 ? prev : up;  // taken into the pair before it
+            const bool kp = in && !gone;
+            const uint32_t km = __ballot_sync(0xffffffffu, kp);
+            if (kp) {
+              const int pos = dst + __popc(km & lt);
+              ids[base + pos] = chosen ? rs : iv[u];
+              rk[base + pos] = rv[u];
+              sel[base + pos] = chosen;
+            }
+            dst += __popc(km);
+            prev = __shfl_sync(0xffffffffu, (uint32_t)chosen, 31) != 0;
+            if (nm) carry = b + 31 - __clz(nm);
+          }
+          __syncwarp();
+        }
+        cnt2 = dst;
+      }
+    } else {
+      // (1) choose every other rs-pair from the start of each run, counting
+      //     runs as if they started in this chunk
+      if (act) {
+        int carry = -1, first_nc = cnt;
+        for (int b0 = 0; b0 < cnt; b0 += 32 * U) {
+          uint32_t v[U];
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int j = b0 + 32 * u + lane;
+            v[u] = j < cnt ? rk[base + j] : rs;
+          }
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int b = b0 + 32 * u, j = b + lane;
+            const bool in = j < cnt, cand = in && v[u] == rs;
+            const uint32_t nm = __ballot_sync(0xffffffffu, in && !cand);
+            const uint32_t before = nm & lt;
+            const int ln = before ? b + 31 - __clz(before) : carry;
+            if (in) sel[base + j] = cand && (((j - ln - 1) & 1) == 0);
+            if (nm) {
+              if (first_nc == cnt) first_nc = b + __ffs(nm) - 1;
+              carry = b + 31 - __clz(nm);
+            }
+          }
+        }
+        if (lane == 0) {
+          S.lead[w] = first_nc;
+          S.tail[w] = cnt - 1 - carry;
+        }
+      }
+      __syncthreads();
+      // (2) a run entering the chunk with an odd length flips its leading run
+      if (act && S.lead[w] > 0) {
+        const int run_in = run_into(w, rs);
+        if (run_in & 1) {
+          __syncwarp();
+          for (int j = lane; j < S.lead[w]; j += 32) sel[base + j] ^= 1;
+        }
+      }
+      __syncthreads();
+      // (3) the chunk's first chosen merge that creates a neighbour pair of a
+      //     rank below rs (the one-at-a-time loop would take that pair next);
+      //     the neighbours' first probes of a batch are loaded together
+      int lw = NW;
+      uint32_t lj = 0;
+      if (act) {
+        uint32_t fb = NONE;
+        for (int b0 = 0; b0 < cnt && fb == NONE; b0 += 32 * U) {
+          uint8_t sv[U];
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int j = b0 + 32 * u + lane;
+            sv[u] = j < cnt ? sel[base + j] : 0;
+          }
+          PairProbe pl[U], pq[U];
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int j = b0 + 32 * u + lane;
+            uint32_t left = 0, right = 0;
+            bool hl = false, hr = false;
+            if (sv[u]) {
+              // the part before j, or rs when the pair before that one is chosen
+              // (it merges first); the part two after j
+              if (j >= 2) {
+                hl = true;
+                left = sel[base + j - 2] ? rs : ids[base + j - 1];
+              } else {
+                int pw = w, pj = j;
+                if (chunk_step<NW>(S.cnt, pw, pj, -1)) {
+                  int qw = pw, qj = pj;
+                  const bool ql = chunk_step<NW>(S.cnt, qw, qj, -1) && S.mn[qw] == rs && sel[qw * cw + qj];
+                  hl = true;
+                  left = ql ? rs : ids[pw * cw + pj];
+                }
+              }
+              if (j + 2 < cnt) {
+                hr = true;
+                right = ids[base + j + 2];
+              } else {
+                int qw = w, qj = j;
+                if (chunk_step<NW>(S.cnt, qw, qj, 2)) {
+                  hr = true;
+                  right = ids[qw * cw + qj];
+                }
+              }
+            }
+            pl[u] = pair_first(c.T, left, rs, hl);
+            pq[u] = pair_first(c.T, rs, right, hr);
+          }
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const bool bad = sv[u] && (pair_finish(c.T, pl[u]) < rs || pair_finish(c.T, pq[u]) < rs);
+            const uint32_t bm = __ballot_sync(0xffffffffu, bad);
+            if (bm && fb == NONE) fb = (uint32_t)(b0 + 32 * u + __ffs(bm) - 1);
+          }
+        }
+        if (lane == 0) S.bad[w] = fb;
+      }
+      // the round's limit: merges at (chunk, index) <= (lw, lj) go ahead
       __syncthreads();
       for (int k = 0; k < NW; k++)
         if (S.mn[k] == rs && S.bad[k] != NONE) {
@@ -1816,58 +1895,57 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
           lj = S.bad[k];
           break;
         }
-    }
-    auto allowed = [&](int v, int j) { return v < lw || (v == lw && (uint32_t)j <= lj); };
-    // (4) merge: each chunk compacts in place, the merged flags replacing
-    //     the chosen ones in sel.  A chunk changes when it holds a chosen
-    //     merge or its first part is taken by the chunk before it.
-    bool first_gone = false;
-    if (cnt > 0) {
-      int pw = w, pj = 0;
-      if (chunk_step<NW>(S.cnt, pw, pj, -1))
-        first_gone = S.mn[pw] == rs && sel[pw * cw + pj] && allowed(pw, pj);
-    }
-    __syncthreads();  // every chunk's last chosen flag is read
-    const bool moves = act || first_gone;
-    int cnt2 = cnt;
-    if (moves) {
-      int dst = 0;
-      uint8_t prev = first_gone ? 1 : 0;  // chosen flag of the pair before the strip's lane 0
-      for (int b0 = 0; b0 < cnt; b0 += 32 * U) {
-        uint32_t iv[U], rv[U];
-        uint8_t sv[U];
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-          const int j = b0 + 32 * u + lane;
-          const bool in = j < cnt;
-          iv[u] = in ? ids[base + j] : 0u;
-          rv[u] = in ? rk[base + j] : 0u;
-          sv[u] = (in && act) ? sel[base + j] : 0;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-          const int j = b0 + 32 * u + lane;
-          const bool in = j < cnt;
-          // the pair before part j merged: part j is taken into it
-          const uint8_t up = (uint8_t)__shfl_up_sync(0xffffffffu, (uint32_t)sv[u], 1);
-          const bool gone = lane == 0 ? (j == 0 ? first_gone : (prev && allowed(w, j - 1)))
-                                      : (up && allowed(w, j - 1));
-          const bool kp = in && !gone;
-          const uint32_t km = __ballot_sync(0xffffffffu, kp);
-          if (kp) {
-            const int pos = dst + __popc(km & lt);
-            const bool merged = sv[u] && allowed(w, j);
-            ids[base + pos] = merged ? rs : iv[u];
-            rk[base + pos] = rv[u];
-            sel[base + pos] = merged;
-          }
-          dst += __popc(km);
-          prev = (uint8_t)__shfl_sync(0xffffffffu, (uint32_t)sv[u], 31);
-        }
-        __syncwarp();
+      auto allowed = [&](int v, int j) { return v < lw || (v == lw && (uint32_t)j <= lj); };
+      // (4) merge: each chunk compacts in place, the merged flags replacing
+      //     the chosen ones in sel.  A chunk changes when it holds a chosen
+      //     merge or its first part is taken by the chunk before it.
+      bool first_gone = false;
+      if (cnt > 0) {
+        int pw = w, pj = 0;
+        if (chunk_step<NW>(S.cnt, pw, pj, -1))
+          first_gone = S.mn[pw] == rs && sel[pw * cw + pj] && allowed(pw, pj);
       }
-      cnt2 = dst;
+      __syncthreads();  // every chunk's last chosen flag is read
+      moves = act || first_gone;
+      if (moves) {
+        int dst = 0;
+        uint8_t prev = first_gone ? 1 : 0;  // chosen flag of the pair before the strip's lane 0
+        for (int b0 = 0; b0 < cnt; b0 += 32 * U) {
+          uint32_t iv[U], rv[U];
+          uint8_t sv[U];
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int j = b0 + 32 * u + lane;
+            const bool in = j < cnt;
+            iv[u] = in ? ids[base + j] : 0u;
+            rv[u] = in ? rk[base + j] : 0u;
+            sv[u] = (in && act) ? sel[base + j] : 0;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int j = b0 + 32 * u + lane;
+            const bool in = j < cnt;
+            // the pair before part j merged: part j is taken into it
+            const uint8_t up = (uint8_t)__shfl_up_sync(0xffffffffu, (uint32_t)sv[u], 1);
+            const bool gone = lane == 0 ? (j == 0 ? first_gone : (prev && allowed(w, j - 1)))
+                                        : (up && allowed(w, j - 1));
+            const bool kp = in && !gone;
+            const uint32_t km = __ballot_sync(0xffffffffu, kp);
+            if (kp) {
+              const int pos = dst + __popc(km & lt);
+              const bool merged = sv[u] && allowed(w, j);
+              ids[base + pos] = merged ? rs : iv[u];
+              rk[base + pos] = rv[u];
+              sel[base + pos] = merged;
+            }
+            dst += __popc(km);
+            prev = (uint8_t)__shfl_sync(0xffffffffu, (uint32_t)sv[u], 31);
+          }
+          __syncwarp();
+        }
+        cnt2 = dst;
+      }
     }
     if (lane == 0) S.cnt2[w] = cnt2;
     __syncthreads();
@@ -1925,7 +2003,7 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
       }
     }
     __syncthreads();  // every warp has read the old minima and counts
-    if (dirty) chunk_min(cnt2);
+    if (dirty) chunk_stats(cnt2);
     if (lane == 0) S.cnt[w] = cnt2;
     if (round > n) {  // every round merges at least one pair
       if (threadIdx.x == 0) set_error(c.W.status, TK_E_LIMIT, 6);
@@ -1960,7 +2038,7 @@ __device__ int64_t merge_chunks(const Call& c, int64_t s, int64_t n, uint8_t* sm
         cw = (((tot + NW - 1) / NW) + 31) & ~31;
         __syncthreads();
         const int cn = max(0, min(cw, tot - w * cw));
-        chunk_min(cn);
+        chunk_stats(cn);
         if (lane == 0) S.cnt[w] = cn;
         __syncthreads();
       }
