@@ -2636,17 +2636,30 @@ __global__ void k_rebase(const int64_t* raw, int64_t* off, int64_t cnt) {
 // End of the pre-token that starts at byte p: the next start bit, else the
 // first start of a later split tile, else n (reads the start bitmap).
 __device__ int64_t piece_end(const Call& c, int64_t p, int64_t ntiles) {
+  constexpr int B = 8;  // bitmap words (or tile firsts) loaded together per step
   const int64_t tile = p / TILE;
   const int64_t tend = min(c.n, (tile + 1) * TILE);
   int64_t y = p + 1;
-  while (y < tend) {
+  if (y < tend) {
     const uint32_t w = c.W.pbits[y >> 5] >> (y & 31);
     if (w) return min(c.n, y + __ffs(w) - 1);
-    y = (y | 31) + 1;
+    const int64_t wend = (tend + 31) >> 5;  // the tile's words (tiles are whole words)
+    for (int64_t wi = (y >> 5) + 1; wi < wend; wi += B) {
+      uint32_t v[B];
+#pragma unroll
+      for (int k = 0; k < B; k++) v[k] = wi + k < wend ? c.W.pbits[wi + k] : 0u;
+#pragma unroll
+      for (int k = 0; k < B; k++)
+        if (v[k]) return min(c.n, ((wi + k) << 5) + __ffs(v[k]) - 1);
+    }
   }
-  for (int64_t k = tile + 1; k < ntiles; k++) {
-    const uint32_t f = c.W.tile_first[k];
-    if (f != NO_START) return k * TILE + f;
+  for (int64_t k0 = tile + 1; k0 < ntiles; k0 += B) {
+    uint32_t f[B];
+#pragma unroll
+    for (int k = 0; k < B; k++) f[k] = k0 + k < ntiles ? c.W.tile_first[k0 + k] : NO_START;
+#pragma unroll
+    for (int k = 0; k < B; k++)
+      if (f[k] != NO_START) return (k0 + k) * TILE + f[k];
   }
   return c.n;
 }
@@ -2680,7 +2693,7 @@ __device__ __forceinline__ void list_long(const Call& c, int64_t p, int64_t len)
 // start of the word; the text end counts as a start), else piece_end.  The
 // mid entries of a warp take one atomic per list: a count pass, a warp scan,
 // then a write pass.  Specials are one id each, left to the tile kernel.
-constexpr int FIND_WPT = 8;
+constexpr int FIND_WPT = 4;
 __global__ void __launch_bounds__(256) k_find_long(Call c) {
   const int lane = threadIdx.x & 31;
   const int64_t ntiles = (c.n + TILE - 1) / TILE;
@@ -2708,15 +2721,25 @@ __global__ void __launch_bounds__(256) k_find_long(Call c) {
         ia = ba + sa - ia;
         ib = bb + sb - ib;
       }
+      // the thread's words, the one after them and their special starts,
+      // loaded together
+      uint32_t pw[FIND_WPT + 1], sw[FIND_WPT];
+#pragma unroll
+      for (int k = 0; k <= FIND_WPT; k++) {
+        const int64_t wi = ch * FIND_WPT + k;
+        pw[k] = (ch < nch && wi < nwords) ? c.W.pbits[wi] : 0u;
+        if (k < FIND_WPT) sw[k] = (c.T.n_spec && ch < nch && wi < nwords) ? c.W.sbits[wi] : 0u;
+      }
+#pragma unroll
       for (int k = 0; k < FIND_WPT; k++) {
         const int64_t wi = ch * FIND_WPT + k;
         if (ch >= nch || wi >= nwords) break;
-        uint32_t bits = c.W.pbits[wi];
+        uint32_t bits = pw[k];
         if ((wi << 5) + 32 > c.n) bits &= (1u << (c.n - (wi << 5))) - 1u;
         if (!bits) continue;
         uint64_t w = bits;
         if ((wi << 5) + 32 < c.n) {
-          uint32_t nx = c.W.pbits[wi + 1];
+          uint32_t nx = pw[k + 1];
           if ((wi << 5) + 64 > c.n) nx |= ~((1u << (c.n - (wi << 5) - 32)) - 1u);
           w |= (uint64_t)nx << 32;
         } else {
@@ -2724,10 +2747,9 @@ __global__ void __launch_bounds__(256) k_find_long(Call c) {
         }
         static_assert(MID_MIN == 5 && SHORT_MAX <= 32, "one look at the next word covers SHORT_MAX");
         const uint64_t near4 = (w >> 1) | (w >> 2) | (w >> 3) | (w >> 4);
-        for (uint32_t cand = bits & ~(uint32_t)near4; cand; cand &= cand - 1) {
+        for (uint32_t cand = bits & ~(uint32_t)near4 & ~sw[k]; cand; cand &= cand - 1) {
           const int x = __ffs(cand) - 1;
           const int64_t p = (wi << 5) + x;
-          if (c.T.n_spec && bit_get(c.W.sbits, p)) continue;
           const uint64_t nxt = w >> (x + 1);
           const int d = nxt ? __ffsll((long long)nxt) : 0;  // length, if the next start is in w
           if (d >= MID_MIN && d <= SHORT_MAX) {
