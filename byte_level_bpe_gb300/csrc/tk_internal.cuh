@@ -449,6 +449,16 @@ struct tk_workspace {
   cudaEvent_t ev_find, ev_mid;       // fork after the listing, join before the fixup
   cudaEvent_t ev_start, ev_h2d[PIPE_MAX], ev_done[PIPE_MAX];
   int n_events;
+  // a repeated device call (same tokenizer, buffers, sizes and cache) is
+  // captured into a graph the second time it comes and replayed after that,
+  // on s_graph, joined with the caller's stream by events
+  cudaStream_t s_graph;
+  cudaEvent_t ev_gin, ev_gout;
+  cudaGraphExec_t g_exec;
+  uint64_t g_key[12];
+  int g_seen;  // calls in a row with g_key
+  int g_off;   // a capture failed: no graphs for this workspace
+  int prio_hi; // the side streams' priority (the graph's side kernels get it too)
   tk::Status* h_pipe_status;  // [PIPE_MAX] pinned
   int64_t* d_stage_raw;       // segment offsets as copied in, before rebasing
   int64_t* d_pipe_base;       // [PIPE_MAX + 1] ids before each batch

@@ -116,11 +116,20 @@ void tk_workspace_free(tk_workspace* ws);
  *       out_capacity, in which case TK_E_CAPACITY is returned).
  *   cuda_stream: a cudaStream_t (NULL = legacy default stream).  The encode
  *       is ordered on this stream: the kernels of the pre-tokens of 5 bytes
- *       or more run on the workspace's two side streams, forked from and
- *       joined back into cuda_stream by events, so work queued on cuda_stream
- *       before the call is seen and work queued after it waits for the whole
- *       encode.  The one 32-byte device->host status read goes on cuda_stream;
- *       the call returns after that read completes.
+ *       or more run on the workspace's side streams, forked from and joined
+ *       back into cuda_stream by events, so work queued on cuda_stream before
+ *       the call is seen and work queued after it waits for the whole encode.
+ *       The one device->host status read goes on cuda_stream (on the graph's
+ *       stream for a replayed call, below); the call returns after that read
+ *       completes.
+ *
+ * Repeated calls: when a workspace sees the same arguments (tokenizer,
+ * buffer addresses, sizes, tiktoken_safe, attached cache) a second time in a
+ * row, for a call under 16 MiB, it captures the call's launches into a CUDA
+ * graph and replays it from then on (on a stream of its own, joined with cuda_stream by events, with
+ * the same ordering as above).  The buffers' contents may change between
+ * calls; the graph reads them when it runs.  Calls with per-kernel profiling
+ * on, and every call after a capture that failed, launch directly.
  *
  * Errors: TK_E_ARG, TK_E_LIMIT (n_bytes or S above the workspace's limits),
  * TK_E_UTF8 (invalid UTF-8; tk_last_error gives the first bad byte offset),

@@ -552,3 +552,46 @@ def test_long_pieces_stop_rule():
     segs.append(("a" * 5000 + "b" * 3000, False))
     _compare(gpu, enc, segs, False)
     gpu.close()
+
+
+def _repeat_calls(gpu, enc, segments, safe, other):
+    """The same call four times on the same buffers (direct, captured into a
+    graph, replayed twice), an unrelated call, then the first again: every
+    result equals the oracle's (the output is poisoned before each call)."""
+    import torch
+    text, off, allow = gpu.pack(segments)
+    d_text = torch.from_numpy(text.copy()).cuda()
+    d_off = torch.from_numpy(off).cuda()
+    d_allow = torch.from_numpy(allow.copy()).cuda()
+    out = torch.empty(max(text.size, 1), dtype=torch.int32, device="cuda")
+    out_off = torch.empty(off.size, dtype=torch.int64, device="cuda")
+    o_ids, o_off = enc.encode_segments(segments, tiktoken_safe=safe)
+    for k in range(6):
+        if k == 4:
+            _compare(gpu, enc, other, safe)
+            continue
+        out.fill_(-1)
+        out_off.fill_(-1)
+        ids, offs = gpu.encode_device(d_text, d_off, d_allow, safe, out=out, out_offsets=out_off)
+        assert np.array_equal(ids.cpu().numpy(), o_ids), f"call {k}"
+        assert np.array_equal(offs.cpu().numpy(), o_off), f"call {k}"
+
+
+def test_repeated_call_graph_small(full_gpu, full_enc, full_table):
+    """A repeated call under 16 MiB (tiktoken_safe: chunk scans, the long
+    pieces' streams) replayed from its captured graph."""
+    segs = workloads.agentic_segments(full_table, seed=3, scale=0.05)
+    other = [(workloads.prose_text(full_table, 20000, seed=12), False)]
+    _repeat_calls(full_gpu, full_enc, segs, True, other)
+
+
+def test_repeated_call_graph_large(full_table, full_enc):
+    """A repeated call of 16 MiB (the mid pieces' stream and word cache too):
+    calls this large launch directly each time, with the same results."""
+    import byte_level_bpe_gb300 as tk
+    text, off = workloads.serving_batch(full_table, seed=5, total=16 << 20, n_req=512)
+    segs = [(bytes(text[off[i]:off[i + 1]]), False) for i in range(len(off) - 1)]
+    gpu = tk.Tokenizer(full_table, workloads.SPECIALS, max_bytes=16 << 20, max_segments=1024)
+    other = [(workloads.prose_text(full_table, 20000, seed=13), False)]
+    _repeat_calls(gpu, full_enc, segs, False, other)
+    gpu.close()
