@@ -533,9 +533,10 @@ def _shuffled_ab_table(seed):
 
 def test_long_pieces_stop_rule():
     """Pre-tokens of random a/b letters over a table with shuffled ranks, at
-    the lengths of every round-merge path (a warp: 129-1,024 bytes; a CTA over
-    chunks: 1,025-32,768; an 8-CTA cluster: longer): rounds stop at merges that
-    create lower-ranked neighbour pairs."""
+    the lengths of every merge path of the long pieces (a warp's list: 17-128
+    bytes; a warp's rounds: 129-1,024; a CTA over chunks: 1,025-32,768; an 8-CTA
+    cluster: longer): rounds stop at merges that create lower-ranked neighbour
+    pairs."""
     import byte_level_bpe_gb300 as tk
     table = _shuffled_ab_table(31)
     rank = {t: i for i, t in enumerate(table)}
@@ -546,7 +547,7 @@ def test_long_pieces_stop_rule():
     gpu = tk.Tokenizer(table, {}, max_bytes=1 << 18, max_segments=64)
     rng = np.random.default_rng(37)
     segs = []
-    for n in (200, 700, 1100, 2500, 6000, 23500, 33000):
+    for n in (17, 40, 77, 100, 128, 200, 700, 1100, 2500, 6000, 23500, 33000):
         segs.append(("".join(np.array(["a", "b"])[rng.integers(0, 2, n)]), False))
     segs.append(("ab" * 3000, False))
     segs.append(("a" * 5000 + "b" * 3000, False))
